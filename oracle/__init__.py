@@ -1,0 +1,182 @@
+"""fp64 CPU oracle for batched speculative-sampling verification.
+
+TEST INFRASTRUCTURE ONLY: tests, ``__graft_entry__.smoke()`` and the CPU
+baseline leg of ``bench.py`` use it; the product package never imports it.
+The arithmetic lives in ``spec_oracle.c`` (plain C, fp64, libm), which cites
+the passages of the tutorial page "5.1 投机解码核心原理" and of the SpecKV
+page that each step restates.  This module only compiles that file with gcc
+and marshals numpy arrays into it.
+
+Logit arrays are numpy ``float32``, ``float64`` or ``uint16`` (raw bf16 bits).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "spec_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+
+GREEDY, SAMPLE, ONEHOT, SIGNALS = 0, 1, 2, 3
+
+# per-request status bits (this oracle's own definitions)
+ST_NONFINITE = 1
+ST_BAD_TOKEN = 2
+ST_BAD_GAMMA = 4
+ST_ZERO_RESIDUAL = 8
+ST_BAD_TEMPERATURE = 64
+ST_BAD_UNIFORM = 128
+
+# planted-mistake ids understood by spec_oracle.c (test-only builds)
+PLANTS = {
+    "resample_from_p": 1,
+    "ratio_inverted": 2,
+    "residual_sign": 3,
+    "bonus_row": 4,
+    "no_temperature": 5,
+    "greedy_tie_high": 6,
+    "entropy_nats": 7,
+    "signal_mean_over_G": 8,
+    "draw_nonstrict": 9,
+    "onehot_keep_y": 10,
+    "no_stop": 11,
+    "accept_nonstrict": 12,
+}
+
+_lock = threading.Lock()
+_cache: dict[int, "Oracle"] = {}
+
+
+def build(plant: int = 0, out_dir: str | None = None) -> str:
+    """Compile spec_oracle.c with gcc (-O2, no fast-math) and return the .so path."""
+    out_dir = out_dir or _BUILD
+    os.makedirs(out_dir, exist_ok=True)
+    name = "libspec_oracle.so" if plant == 0 else f"libspec_oracle_plant{plant}.so"
+    out = os.path.join(out_dir, name)
+    if os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(_SRC):
+        return out
+    tmp = out + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp",
+           "-fno-fast-math", "-ffp-contract=off", f"-DORACLE_PLANT={plant}",
+           _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out)
+    return out
+
+
+def _dtype_code(a: np.ndarray) -> int:
+    if a.dtype == np.float32:
+        return 0
+    if a.dtype == np.uint16:
+        return 1
+    if a.dtype == np.float64:
+        return 2
+    raise TypeError(f"logits must be float32, float64 or uint16 (bf16 bits), got {a.dtype}")
+
+
+def _ptr(a, ctype):
+    if a is None:
+        return None
+    return a.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+class Oracle:
+    """Loaded oracle library (one per planted-mistake id)."""
+
+    def __init__(self, path: str):
+        self.lib = ctypes.CDLL(path)
+        f = self.lib.oracle_run
+        P = ctypes.c_void_p
+        f.argtypes = [ctypes.c_int, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                      P, P, P, P, P, P, P, P, P, P, P, P, P, P, ctypes.c_int]
+        f.restype = ctypes.c_int
+        self.lib.oracle_plant_id.restype = ctypes.c_int
+        self.plant = self.lib.oracle_plant_id()
+
+    def run(self, mode, target=None, draft=None, draft_tokens=None, gamma=None,
+            temperature=None, uniforms=None, *, B=None, G=None, V=None,
+            want_signals=False, want_row_signals=False, probe_token=None,
+            nthreads=None):
+        """Run one mode over a batch; returns a dict of numpy outputs."""
+        ref = target if target is not None else draft
+        if ref is None:
+            raise ValueError("need target or draft logits")
+        dt = _dtype_code(ref)
+        if target is not None:
+            B_, Gp1, V_ = target.shape
+            G_ = Gp1 - 1
+        else:
+            B_, G_, V_ = draft.shape
+        B = B_ if B is None else B
+        G = G_ if G is None else G
+        V = V_ if V is None else V
+        c = lambda a, t: None if a is None else np.ascontiguousarray(a, dtype=t)
+        target = None if target is None else np.ascontiguousarray(target)
+        draft = None if draft is None else np.ascontiguousarray(draft)
+        if draft is not None and _dtype_code(draft) != dt:
+            raise TypeError("target and draft dtypes differ")
+        draft_tokens = c(draft_tokens, np.int32)
+        gamma = c(gamma, np.int32)
+        temperature = c(temperature, np.float32)
+        uniforms = c(uniforms, np.float32)
+        probe_token = c(probe_token, np.int32)
+        out = {
+            "accept_len": np.zeros(B, np.int32),
+            "tokens": np.zeros((B, G + 1), np.int32),
+            "status": np.zeros(B, np.int32),
+            "accept_prob": np.zeros((B, G), np.float64),
+            "accept_margin": np.zeros((B, G), np.float64),
+            "draw_margin": np.zeros(B, np.float64),
+        }
+        if want_signals:
+            out["signals"] = np.zeros((B, 4), np.float64)
+        if want_row_signals:
+            out["row_signals"] = np.zeros((B, G, 2), np.float64)
+        if probe_token is not None:
+            out["probe_distance"] = np.zeros(B, np.float64)
+        nthreads = nthreads or os.cpu_count() or 1
+        rc = self.lib.oracle_run(
+            mode, _ptr(target, ctypes.c_char), _ptr(draft, ctypes.c_char), dt, B, G, V,
+            _ptr(draft_tokens, ctypes.c_int32), _ptr(gamma, ctypes.c_int32),
+            _ptr(temperature, ctypes.c_float), _ptr(uniforms, ctypes.c_float),
+            _ptr(out["accept_len"], ctypes.c_int32), _ptr(out["tokens"], ctypes.c_int32),
+            _ptr(out["status"], ctypes.c_int32), _ptr(out.get("signals"), ctypes.c_double),
+            _ptr(out.get("row_signals"), ctypes.c_double), _ptr(out["accept_prob"], ctypes.c_double),
+            _ptr(out["accept_margin"], ctypes.c_double), _ptr(out["draw_margin"], ctypes.c_double),
+            _ptr(probe_token, ctypes.c_int32), _ptr(out.get("probe_distance"), ctypes.c_double),
+            int(nthreads))
+        if rc != 0:
+            raise ValueError("oracle_run rejected its arguments")
+        return out
+
+    # convenience wrappers named after the four library calls
+    def verify_greedy(self, target, draft_tokens, gamma=None, **kw):
+        return self.run(GREEDY, target=target, draft_tokens=draft_tokens, gamma=gamma, **kw)
+
+    def verify_sample(self, target, draft, draft_tokens, gamma, temperature, uniforms, **kw):
+        return self.run(SAMPLE, target=target, draft=draft, draft_tokens=draft_tokens, gamma=gamma,
+                        temperature=temperature, uniforms=uniforms, **kw)
+
+    def verify_onehot(self, target, draft_tokens, gamma, temperature, uniforms, **kw):
+        return self.run(ONEHOT, target=target, draft_tokens=draft_tokens, gamma=gamma,
+                        temperature=temperature, uniforms=uniforms, **kw)
+
+    def draft_signals(self, draft, gamma, temperature, **kw):
+        kw.setdefault("want_signals", True)
+        return self.run(SIGNALS, draft=draft, gamma=gamma, temperature=temperature, **kw)
+
+
+def load(plant: int = 0, out_dir: str | None = None) -> Oracle:
+    """Build (if needed) and load the oracle; cached per planted-mistake id."""
+    with _lock:
+        if out_dir is None and plant in _cache:
+            return _cache[plant]
+        o = Oracle(build(plant, out_dir))
+        if out_dir is None:
+            _cache[plant] = o
+        return o

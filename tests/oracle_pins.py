@@ -1,0 +1,461 @@
+"""Pins of the fp64 oracle against facts fixed by the pages and by mathematics.
+
+Each ``pin_*`` function takes a loaded oracle and raises AssertionError when the
+oracle disagrees with the fact it checks.  ``test_oracle_pins.py`` runs them on
+the real oracle; ``test_oracle_mutants.py`` runs them on builds of the oracle
+with one planted mistake each and requires that some pin fails.
+
+Sources: the tutorial page "5.1 投机解码核心原理" (sections 3.1-3.3, 4.1-4.3,
+5.1-5.2, 7) and the SpecKV page (draft signal extraction).  Probabilities are
+integrated exactly over the uniforms with a midpoint grid of N points whose
+breakpoints all fall on multiples of 1/N, so grid fractions are exact
+rationals; distributional facts at general p, q use chi-square tests.
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+
+import numpy as np
+from scipy import special, stats
+
+import oracle as O
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+N_GRID = 4200  # multiples of 1/4200: 0.1, 0.3, 1/3, 0.6, 6/7, 0.9 ...
+
+
+def golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def _grid(n=N_GRID):
+    return ((np.arange(n, dtype=np.float64) + 0.5) / n).astype(np.float32)
+
+
+def _f64_logits(rows):
+    """[n_rows, V] probabilities -> fp64 logits ln p (-inf for 0)."""
+    with np.errstate(divide="ignore"):
+        return np.log(np.asarray(rows, np.float64))
+
+
+def _hist(tokens, V):
+    return np.bincount(tokens, minlength=V).astype(np.float64) / len(tokens)
+
+
+# ----------------------------------------------------------------------------
+# exact integrals over the uniforms for the worked example (gamma = 1, V = 3)
+
+def worked_example_paths(o, p, q, bonus, mode=O.SAMPLE, onehot_y=1):
+    """Return (accept_path, reject_path, bonus_dist) integrated exactly.
+
+    accept_path[x] = P(x proposed and accepted); reject_path[x] = P(rejected
+    and residual gives x); bonus_dist = law of the extra token after an accept.
+    """
+    V = len(p)
+    u = _grid()
+    n = len(u)
+    ys = [onehot_y] if mode == O.ONEHOT else list(range(V))
+    qy = {y: (1.0 if mode == O.ONEHOT else q[y]) for y in ys}
+    tgt1 = np.stack([_f64_logits(p), _f64_logits(bonus)])           # rows 0, 1
+    dr1 = _f64_logits(q)[None, :] if q is not None else None
+    # (a) acceptance probability of each proposal y: grid over u_0
+    B = n * len(ys)
+    target = np.broadcast_to(tgt1, (B, 2, V)).copy()
+    draft = np.broadcast_to(dr1, (B, 1, V)).copy() if mode == O.SAMPLE else None
+    y = np.repeat(np.asarray(ys, np.int32), n)[:, None]
+    uni = np.stack([np.tile(u, len(ys)), np.full(B, 0.5, np.float32)], axis=1)
+    T = np.ones(B, np.float32)
+    r = o.run(mode, target=target, draft=draft, draft_tokens=y, gamma=None,
+              temperature=T, uniforms=uni)
+    acc = r["accept_len"].reshape(len(ys), n)
+    p_acc = {yy: float(np.mean(acc[j] == 1)) for j, yy in enumerate(ys)}
+    # (b) residual law after a reject of y (u_0 just below 1 rejects any a < 1)
+    rej = {}
+    for yy in ys:
+        if p_acc[yy] >= 1.0:
+            continue
+        uni2 = np.stack([np.full(n, np.float32(1.0 - 2**-24)), u], axis=1)
+        r2 = o.run(mode, target=np.broadcast_to(tgt1, (n, 2, V)).copy(),
+                   draft=None if draft is None else np.broadcast_to(dr1, (n, 1, V)).copy(),
+                   draft_tokens=np.full((n, 1), yy, np.int32), temperature=np.ones(n, np.float32),
+                   uniforms=uni2)
+        assert np.all(r2["accept_len"] == 0), "u_0 = 1 - 2^-24 must reject when a < 1"
+        rej[yy] = _hist(r2["tokens"][:, 0], V)
+    # (c) the bonus token after an accept: draw grid on u_G with u_0 = 0 (accepts a > 0)
+    yb = max(ys, key=lambda yy: p_acc[yy])
+    uni3 = np.stack([np.zeros(n, np.float32), u], axis=1)
+    r3 = o.run(mode, target=np.broadcast_to(tgt1, (n, 2, V)).copy(),
+               draft=None if draft is None else np.broadcast_to(dr1, (n, 1, V)).copy(),
+               draft_tokens=np.full((n, 1), yb, np.int32), temperature=np.ones(n, np.float32),
+               uniforms=uni3)
+    assert np.all(r3["accept_len"] == 1)
+    bonus_dist = _hist(r3["tokens"][:, 1], V)
+    accept_path = np.zeros(V)
+    reject_path = np.zeros(V)
+    for yy in ys:
+        accept_path[yy] += qy[yy] * p_acc[yy]
+        if yy in rej:
+            reject_path += qy[yy] * (1.0 - p_acc[yy]) * rej[yy]
+    return accept_path, reject_path, bonus_dist
+
+
+def pin_worked_example(o):
+    """Section 4.2 / 7: accept path [0.2,0.3,0.1], 0.4 to token 0, final = p."""
+    g = golden("worked_example.json")
+    bonus = [0.1, 0.2, 0.7]   # a different row 1, so the bonus row is identified
+    acc, rej, bon = worked_example_paths(o, g["p"], g["q"], bonus)
+    np.testing.assert_allclose(acc, g["accept_path"], atol=1e-12)
+    np.testing.assert_allclose(rej, g["reject_path"], atol=1e-12)
+    assert abs(rej.sum() - g["reject_mass"]) < 1e-12
+    np.testing.assert_allclose(acc + rej, g["final"], atol=1e-12)
+    np.testing.assert_allclose(bon, bonus, atol=1e-12)
+
+
+def wrong_rule_final(o):
+    g = golden("worked_example.json")
+    acc, rej, _ = worked_example_paths(o, g["p"], g["q"], g["p"])
+    return acc + rej
+
+
+def pin_worked_example_onehot(o):
+    """Section 3.3 / 7: q = one-hot on token 1 -> acceptance 0.3, final = p."""
+    g = golden("worked_example.json")
+    y = int(np.argmax(g["onehot_q"]))
+    acc, rej, _ = worked_example_paths(o, g["p"], None, g["p"], mode=O.ONEHOT, onehot_y=y)
+    assert abs(acc.sum() - g["onehot_acceptance"]) < 1e-12
+    np.testing.assert_allclose(acc + rej, g["onehot_final"], atol=1e-12)
+
+
+# ----------------------------------------------------------------------------
+
+def pin_acceptance_is_one_minus_tv(o):
+    """Section 4.1 / 4.3: sum_y q(y) a(y) = sum min(p,q) = 1 - TV(p,q) = 1 - sum [p-q]_+."""
+    rng = np.random.default_rng(5)
+    for V, T in [(5, 1.0), (17, 0.7), (64, 1.3)]:
+        T = float(np.float32(T))        # the oracle receives temperature as fp32
+        xt = rng.normal(0, 2, V)
+        xd = xt + rng.normal(0, 1, V)
+        p = special.softmax(xt / T)
+        q = special.softmax(xd / T)
+        B = V
+        r = o.run(O.SAMPLE, target=np.broadcast_to(np.stack([xt, xt]), (B, 2, V)).copy(),
+                  draft=np.broadcast_to(xd[None], (B, 1, V)).copy(),
+                  draft_tokens=np.arange(V, dtype=np.int32)[:, None], temperature=np.full(B, T, np.float32),
+                  uniforms=np.zeros((B, 2), np.float32))
+        a = r["accept_prob"][:, 0]
+        A = float(np.dot(q, a))
+        tv = 0.5 * np.abs(p - q).sum()
+        assert abs(A - (1 - tv)) < 1e-12, (A, 1 - tv)
+        assert abs(A - np.minimum(p, q).sum()) < 1e-12
+        assert abs((1 - A) - np.maximum(p - q, 0).sum()) < 1e-12
+
+
+def _chi2_ok(counts, probs, min_p=1e-3):
+    probs = np.asarray(probs, np.float64)
+    n = counts.sum()
+    keep = probs > 0
+    assert counts[~keep].sum() == 0, "a zero-probability token was produced"
+    res = stats.chisquare(counts[keep], probs[keep] / probs[keep].sum() * n)
+    return res.pvalue > min_p, res.pvalue
+
+
+def pin_chi2_final_is_p(o, trials=1_000_000):
+    """Section 4.2 / 5: accept + correct together give exactly p; accepted-only
+    tokens follow min(p,q)/A (section 4.2 warning); the bonus follows p_{gamma+1}."""
+    rng = np.random.default_rng(42)
+    V, T = 8, float(np.float32(0.8))
+    xt = rng.normal(0, 1.5, (2, V))
+    xd = xt[0] + rng.normal(0, 1.0, V)
+    p0 = special.softmax(xt[0] / T)
+    p1 = special.softmax(xt[1] / T)
+    q = special.softmax(xd / T)
+    y = rng.choice(V, size=trials, p=q).astype(np.int32)
+    uni = rng.random((trials, 2)).astype(np.float32)
+    r = o.run(O.SAMPLE, target=np.broadcast_to(xt.astype(np.float32), (trials, 2, V)).copy(),
+              draft=np.broadcast_to(xd.astype(np.float32)[None], (trials, 1, V)).copy(),
+              draft_tokens=y[:, None], temperature=np.full(trials, T, np.float32), uniforms=uni)
+    # the oracle reads fp32 logits: recompute p, q from the same fp32 values
+    p0 = special.softmax(xt[0].astype(np.float32).astype(np.float64) / T)
+    p1 = special.softmax(xt[1].astype(np.float32).astype(np.float64) / T)
+    q = special.softmax(xd.astype(np.float32).astype(np.float64) / T)
+    tok0 = r["tokens"][:, 0]
+    ok, pv = _chi2_ok(np.bincount(tok0, minlength=V), p0)
+    assert ok, f"final token law != p (p-value {pv:.3g})"
+    accd = r["accept_len"] == 1
+    mn = np.minimum(p0, q)
+    ok, pv = _chi2_ok(np.bincount(tok0[accd], minlength=V), mn / mn.sum())
+    assert ok, f"accepted-only law != min(p,q)/A (p-value {pv:.3g})"
+    assert abs(accd.mean() - mn.sum()) < 5 * math.sqrt(mn.sum() * (1 - mn.sum()) / trials)
+    ok, pv = _chi2_ok(np.bincount(r["tokens"][accd, 1], minlength=V), p1)
+    assert ok, f"bonus law != p_(gamma+1) (p-value {pv:.3g})"
+
+
+def pin_chi2_onehot(o, trials=1_000_000):
+    """Section 3.3: one-hot q stays lossless: final token law = p."""
+    rng = np.random.default_rng(43)
+    V, T = 8, 1.0
+    xt = rng.normal(0, 1.5, (2, V)).astype(np.float32)
+    p0 = special.softmax(xt[0].astype(np.float64) / T)
+    r_prop = special.softmax(rng.normal(0, 1.5, V))        # any proposal law is lossless
+    y = rng.choice(V, size=trials, p=r_prop).astype(np.int32)
+    uni = rng.random((trials, 2)).astype(np.float32)
+    r = o.run(O.ONEHOT, target=np.broadcast_to(xt, (trials, 2, V)).copy(), draft_tokens=y[:, None],
+              temperature=np.full(trials, T, np.float32), uniforms=uni)
+    ok, pv = _chi2_ok(np.bincount(r["tokens"][:, 0], minlength=V), p0)
+    assert ok, f"one-hot final law != p (p-value {pv:.3g})"
+    # acceptance of proposal y is p(y)
+    for yy in range(V):
+        sel = y == yy
+        a = r["accept_len"][sel].mean()
+        assert abs(a - p0[yy]) < 6 * math.sqrt(p0[yy] * (1 - p0[yy]) / sel.sum()) + 1e-9
+
+
+def pin_chi2_gamma0(o, trials=400_000):
+    """gamma = 0: one draw from p_0, i.e. plain categorical sampling."""
+    rng = np.random.default_rng(44)
+    V, T = 8, float(np.float32(0.6))
+    xt = rng.normal(0, 1.0, (1, V)).astype(np.float32)
+    p0 = special.softmax(xt[0].astype(np.float64) / T)
+    uni = rng.random((trials, 1)).astype(np.float32)
+    r = o.run(O.SAMPLE, target=np.broadcast_to(xt, (trials, 1, V)).copy(), draft=None,
+              draft_tokens=None, temperature=np.full(trials, T, np.float32), uniforms=uni)
+    assert np.all(r["accept_len"] == 0)
+    ok, pv = _chi2_ok(np.bincount(r["tokens"][:, 0], minlength=V), p0)
+    assert ok, f"gamma=0 draw law != p (p-value {pv:.3g})"
+
+
+def pin_chain_mean_accept_len(o, trials=200_000):
+    """Sections 4.3 and 5.1: with independent positions, E[k] = sum_{i=1}^{gamma}
+    prod_{j<i} A_j where A_j = sum min(p_j, q_j) = 1 - TV."""
+    rng = np.random.default_rng(45)
+    V, G, T = 16, 4, float(np.float32(0.9))
+    xt = rng.normal(0, 2, (G + 1, V)).astype(np.float32)
+    xd = (xt[:G] + rng.normal(0, 1.2, (G, V))).astype(np.float32)
+    P = special.softmax(xt.astype(np.float64) / T, axis=1)
+    Q = special.softmax(xd.astype(np.float64) / T, axis=1)
+    A = 1.0 - 0.5 * np.abs(P[:G] - Q).sum(axis=1)
+    Ek = sum(np.prod(A[:i]) for i in range(1, G + 1))
+    y = np.stack([rng.choice(V, size=trials, p=Q[i]) for i in range(G)], axis=1).astype(np.int32)
+    uni = rng.random((trials, G + 1)).astype(np.float32)
+    r = o.run(O.SAMPLE, target=np.broadcast_to(xt, (trials, G + 1, V)).copy(),
+              draft=np.broadcast_to(xd, (trials, G, V)).copy(), draft_tokens=y,
+              temperature=np.full(trials, T, np.float32), uniforms=uni)
+    k = r["accept_len"].astype(np.float64)
+    se = k.std() / math.sqrt(trials)
+    assert abs(k.mean() - Ek) < 5 * se, (k.mean(), Ek, se)
+    # each round commits between 1 and gamma+1 tokens (section 5.2)
+    n_commit = (r["tokens"] >= 0).sum(axis=1)
+    assert np.all(n_commit == k + 1)
+
+
+def pin_first_reject_stops(o):
+    """Section 5.1: candidates after the first reject are void."""
+    V = 4
+    xt = np.log(np.array([[0.4, 0.3, 0.2, 0.1]] * 4))
+    xd = np.log(np.array([[0.1, 0.2, 0.3, 0.4]] * 3))
+    y = np.array([[3, 3, 0]], np.int32)            # a = 0.25 at positions 0 and 1, 1 at 2
+    uni = np.array([[0.9, 0.9, 0.1, 0.5]], np.float32)
+    r = o.run(O.SAMPLE, target=xt[None], draft=xd[None], draft_tokens=y,
+              temperature=np.ones(1, np.float32), uniforms=uni)
+    assert r["accept_len"][0] == 0
+    assert r["tokens"][0, 0] in (0, 1)               # residual [p-q]_+ lives on tokens 0, 1
+    assert np.all(r["tokens"][0, 1:] == -1)
+    assert np.isnan(r["accept_prob"][0, 1]) and np.isnan(r["accept_prob"][0, 2])
+
+
+def pin_accept_is_strict(o):
+    """Section 3.2: accept iff u < a; at u == a exactly the proposal is rejected."""
+    V = 4
+    xt = np.zeros((1, 2, V))                       # p uniform: p(0) = 0.25 exactly
+    xd = np.array([[[0.0, 0.0, -np.inf, -np.inf]]])  # q = [0.5, 0.5, 0, 0] exactly
+    uni = np.array([[0.5, 0.5]], np.float32)       # u = a = 0.5
+    r = o.run(O.SAMPLE, target=xt, draft=xd, draft_tokens=np.zeros((1, 1), np.int32),
+              temperature=np.full(1, 0.7, np.float32), uniforms=uni)
+    assert r["accept_prob"][0, 0] == 0.5
+    assert r["accept_len"][0] == 0
+    uni[0, 0] = np.nextafter(np.float32(0.5), np.float32(0))
+    r = o.run(O.SAMPLE, target=xt, draft=xd, draft_tokens=np.zeros((1, 1), np.int32),
+              temperature=np.full(1, 0.7, np.float32), uniforms=uni)
+    assert r["accept_len"][0] == 1
+
+
+def pin_draw_convention(o):
+    """Inverse-CDF convention: smallest x with C(x) > u W (the page's experiment
+    draws with Python's weighted choice, which bisects to the right); tokens of
+    weight 0 are never drawn, even when u W lands exactly on a boundary."""
+    xt = np.array([[[0.0, -np.inf, 0.0, -np.inf]]])   # p = [0.5, 0, 0.5, 0] exactly
+    for u, want in [(0.0, 0), (0.25, 0), (0.5, 2), (0.75, 2), (1 - 2**-24, 2)]:
+        r = o.run(O.SAMPLE, target=xt, draft=None, draft_tokens=None,
+                  temperature=np.ones(1, np.float32), uniforms=np.array([[u]], np.float32))
+        assert r["tokens"][0, 0] == want, (u, r["tokens"][0, 0], want)
+
+
+def pin_p_equals_q(o):
+    """Section 4.2: p = q gives beta = 0, so nothing is ever rejected."""
+    rng = np.random.default_rng(46)
+    B, G, V = 64, 5, 50
+    xt = rng.normal(0, 3, (B, G + 1, V)).astype(np.float32)
+    xd = xt[:, :G, :].copy()
+    Q = special.softmax(xd.astype(np.float64), axis=2)
+    y = np.array([[rng.choice(V, p=Q[b, i]) for i in range(G)] for b in range(B)], np.int32)
+    uni = rng.random((B, G + 1)).astype(np.float32)
+    r = o.run(O.SAMPLE, target=xt, draft=xd, draft_tokens=y, temperature=np.ones(B, np.float32),
+              uniforms=uni)
+    assert np.all(r["accept_len"] == G)
+    assert np.all(r["tokens"][:, :G] == y)
+
+
+def pin_greedy_is_target_argmax(o):
+    """Section 3.1: the committed tokens are the target's own greedy decoding:
+    the accepted prefix equals argmax at each position and the emitted token is
+    the argmax at the first mismatch (or the bonus argmax); ties -> lowest index."""
+    rng = np.random.default_rng(47)
+    B, G, V = 200, 6, 12
+    xt = rng.integers(-3, 3, (B, G + 1, V)).astype(np.float32)   # many ties
+    am = np.argmax(xt, axis=2)                                   # numpy: first maximum
+    y = am[:, :G].copy()
+    flip = rng.random((B, G)) < 0.25
+    y[flip] = rng.integers(0, V, flip.sum())
+    r = o.run(O.GREEDY, target=xt, draft_tokens=y.astype(np.int32))
+    for b in range(B):
+        k = r["accept_len"][b]
+        mism = np.nonzero(y[b] != am[b, :G])[0]
+        assert k == (mism[0] if len(mism) else G)
+        assert np.all(r["tokens"][b, :k + 1] == am[b, :k + 1])
+        assert np.all(r["tokens"][b, k + 1:] == -1)
+    # a draft that always proposes the argmax is accepted to the end
+    r = o.run(O.GREEDY, target=xt, draft_tokens=am[:, :G].astype(np.int32))
+    assert np.all(r["accept_len"] == G)
+
+
+def pin_signals_closed_forms(o):
+    """SpecKV signals: H = -sum q log2 q, c = max q, with per-request mean/max
+    entropy and mean/min confidence over the gamma_b draft rows."""
+    V, G = 64, 4
+    rows = np.full((1, G, V), -1e4)
+    rows[0, 0, :] = 0.0                         # uniform: H = log2 V, c = 1/V
+    rows[0, 1, :2] = 0.0                        # two-way tie: H = 1, c = 1/2
+    rows[0, 2, 5] = 0.0                         # one token: H = 0, c = 1
+    rows[0, 3, :] = 0.0                         # padding row, beyond gamma_b = 3
+    r = o.draft_signals(rows, gamma=np.array([3], np.int32), temperature=np.ones(1, np.float32),
+                        want_row_signals=True)
+    H = np.array([math.log2(V), 1.0, 0.0])
+    c = np.array([1.0 / V, 0.5, 1.0])
+    np.testing.assert_allclose(r["row_signals"][0, :3, 0], H, atol=1e-12)
+    np.testing.assert_allclose(r["row_signals"][0, :3, 1], c, atol=1e-12)
+    assert np.all(np.isnan(r["row_signals"][0, 3]))
+    np.testing.assert_allclose(r["signals"][0], [H.mean(), H.max(), c.mean(), c.min()], atol=1e-12)
+    # temperature: logits [ln 3 * T, 0] at T give q = [3/4, 1/4]
+    T = float(np.float32(0.6))
+    x = np.full((1, 1, 5), -1e4)
+    x[0, 0, 0] = math.log(3.0) * T
+    x[0, 0, 1] = 0.0
+    r = o.draft_signals(x, gamma=np.array([1], np.int32), temperature=np.full(1, T, np.float32))
+    Hq = -(0.75 * math.log2(0.75) + 0.25 * math.log2(0.25))
+    assert abs(r["signals"][0, 0] - Hq) < 1e-6 and abs(r["signals"][0, 2] - 0.75) < 1e-6
+    # random rows against scipy's entropy (base 2)
+    rng = np.random.default_rng(48)
+    x = rng.normal(0, 2, (3, 6, 300))
+    g = np.array([6, 2, 5], np.int32)
+    Tb = np.array([1.0, 0.7, 1.4], np.float32)
+    r = o.draft_signals(x, gamma=g, temperature=Tb)
+    for b in range(3):
+        qs = special.softmax(x[b, :g[b]] / np.float64(Tb[b]), axis=1)
+        Hs = stats.entropy(qs, base=2, axis=1)
+        cs = qs.max(axis=1)
+        np.testing.assert_allclose(r["signals"][b], [Hs.mean(), Hs.max(), cs.mean(), cs.min()],
+                                   rtol=1e-10)
+
+
+def pin_bf16_inputs(o):
+    """bf16 logits widen exactly: a bf16 row and the same values in fp32 give
+    identical results; known bit patterns decode to their values."""
+    pats = np.array([0x3F80, 0xC040, 0x4000, 0x0000, 0xBF80, 0x4040], np.uint16)  # 1,-3,2,0,-1,3
+    r = o.run(O.GREEDY, target=pats[None, None, :], draft_tokens=np.zeros((1, 0), np.int32),
+              G=0)
+    assert r["tokens"][0, 0] == 5
+    vals = np.array([1.0, -3.0, 2.0, 0.0, -1.0, 3.0], np.float32)
+    x = np.stack([pats, pats[::-1].copy()])[None]                 # [1, 2, 6]
+    xf = np.stack([vals, vals[::-1].copy()])[None]
+    d = pats[None, None, :].copy()
+    df = vals[None, None, :].copy()
+    kw = dict(draft_tokens=np.array([[2]], np.int32), temperature=np.full(1, 0.9, np.float32),
+              uniforms=np.array([[0.3, 0.6]], np.float32), want_signals=True)
+    a = o.run(O.SAMPLE, target=x, draft=d, **kw)
+    b = o.run(O.SAMPLE, target=xf, draft=df, **kw)
+    for key in ("accept_len", "tokens", "accept_prob", "signals"):
+        np.testing.assert_array_equal(a[key], b[key])
+
+
+def pin_status_semantics(o):
+    """Readings on bad inputs: errors void the request; rows, tokens and
+    uniforms after the first reject are never looked at."""
+    V, G = 6, 3
+    base_t = np.zeros((1, G + 1, V))
+    base_t[0, :, 0] = 2.0
+    base_d = np.zeros((1, G, V))
+    base_d[0, :, 1] = 3.0                       # q prefers token 1, p token 0
+    y = np.array([[1, 0, 0]], np.int32)
+    T = np.ones(1, np.float32)
+    u = np.array([[0.99, 0.1, 0.1, 0.5]], np.float32)   # position 0 rejects
+
+    def run(mode=O.SAMPLE, **kw):
+        args = dict(target=base_t, draft=base_d, draft_tokens=y, temperature=T, uniforms=u)
+        args.update(kw)
+        if mode != O.SAMPLE:
+            args.pop("draft")
+        if mode == O.GREEDY:
+            args.pop("temperature"); args.pop("uniforms")
+        return o.run(mode, **args)
+
+    r = run()
+    assert r["status"][0] == 0 and r["accept_len"][0] == 0
+    t = base_t.copy(); t[0, 2, 3] = np.nan                   # after the reject: not read
+    assert run(target=t)["status"][0] == 0
+    t = base_t.copy(); t[0, 0, 3] = np.nan
+    r = run(target=t)
+    assert r["status"][0] == O.ST_NONFINITE and np.all(r["tokens"] == -1)
+    t = base_t.copy(); t[0, 0, 3] = np.inf
+    assert run(target=t)["status"][0] == O.ST_NONFINITE
+    t = base_t.copy(); t[0, 0, 3] = -np.inf                  # a masked token is fine
+    assert run(target=t)["status"][0] == 0
+    t = base_t.copy(); t[0, 0, :] = -np.inf                  # no finite maximum
+    assert run(target=t)["status"][0] == O.ST_NONFINITE
+    assert run(draft_tokens=np.array([[V, 0, 0]], np.int32))["status"][0] == O.ST_BAD_TOKEN
+    assert run(draft_tokens=np.array([[1, -1, 0]], np.int32))["status"][0] == 0
+    assert run(gamma=np.array([4], np.int32))["status"][0] == O.ST_BAD_GAMMA
+    assert run(gamma=np.array([-1], np.int32))["status"][0] == O.ST_BAD_GAMMA
+    assert run(temperature=np.zeros(1, np.float32))["status"][0] == O.ST_BAD_TEMPERATURE
+    assert run(temperature=np.full(1, np.nan, np.float32))["status"][0] == O.ST_BAD_TEMPERATURE
+    assert run(uniforms=np.array([[1.0, 0.1, 0.1, 0.5]], np.float32))["status"][0] == O.ST_BAD_UNIFORM
+    assert run(uniforms=np.array([[0.99, 0.1, 0.1, -0.5]], np.float32))["status"][0] == O.ST_BAD_UNIFORM
+    assert run(uniforms=np.array([[0.99, 2.0, 0.1, 0.5]], np.float32))["status"][0] == 0
+    # greedy: mismatch at position 0 stops; a NaN later is not read
+    t = base_t.copy(); t[0, 1, 2] = np.nan
+    r = run(O.GREEDY, target=t)
+    assert r["status"][0] == 0 and r["accept_len"][0] == 0 and r["tokens"][0, 0] == 0
+    # one-hot: proposal 1 has p(1) ~ 0.08, so u = 0.99 rejects it
+    r = run(O.ONEHOT)
+    assert r["status"][0] == 0
+
+
+ALL_PINS = [
+    pin_worked_example,
+    pin_worked_example_onehot,
+    pin_acceptance_is_one_minus_tv,
+    pin_chi2_final_is_p,
+    pin_chi2_onehot,
+    pin_chi2_gamma0,
+    pin_chain_mean_accept_len,
+    pin_first_reject_stops,
+    pin_accept_is_strict,
+    pin_draw_convention,
+    pin_p_equals_q,
+    pin_greedy_is_target_argmax,
+    pin_signals_closed_forms,
+    pin_bf16_inputs,
+    pin_status_semantics,
+]
