@@ -1,0 +1,165 @@
+/*
+ * spec_verify.h -- C ABI of the GB300 (sm_103a) speculative-sampling
+ * verification library.
+ *
+ * One call verifies a batch of B independent requests.  Request b proposed
+ * draft tokens y_0..y_{gamma_b-1}; the target model produced gamma_b + 1 logit
+ * rows (positions 0..gamma_b) and, for full-q verification, the draft model
+ * produced gamma_b logit rows.  The library decides how many draft tokens are
+ * accepted and which token is committed after them.
+ *
+ * Method (tutorial page "5.1 投机解码核心原理", infra-guide):
+ *   section 2.1  p_i, q_i are the distributions used for sampling, temperature
+ *                applied: p_i = softmax(target_row_i / T_b), same for q_i;
+ *   section 3.1  greedy: accept y_i iff y_i = argmax p_i, else emit argmax, stop;
+ *   section 3.2  accept y_i iff u_i < min(1, p_i(y_i) / q_i(y_i)); on reject
+ *                draw from [p_i - q_i]_+ / sum [p_i - q_i]_+;
+ *   section 3.3  one-hot q (draft gives tokens only): accept iff u_i < p_i(y_i);
+ *                on reject draw from p_i with y_i removed, renormalised;
+ *   section 5.1  stop at the first reject, later candidates are void;
+ *   section 5.2  all gamma accepted: one more token from p_gamma (bonus).
+ * Draft signals (SpecKV page, draft signal extraction): per draft row
+ *   H_i = -sum_v q_i(v) log2 q_i(v) (bits) and c_i = max_v q_i(v); per request
+ *   mean_i H_i, max_i H_i, mean_i c_i, min_i c_i over i < gamma_b.
+ *
+ * Conventions shared by every call
+ *   - Index 0-based: target rows i = 0..gamma_b (row gamma_b is the bonus row),
+ *     draft rows and draft tokens i = 0..gamma_b-1.  The pages count from 1.
+ *   - Layouts are row-major and contiguous:
+ *       target_logits [B, G+1, V], draft_logits [B, G, V]  (dtype below),
+ *       draft_tokens [B, G] int32, gamma [B] int32 (NULL: every gamma_b = G),
+ *       temperature [B] float32 (> 0), uniforms [B, G+1] float32 in [0, 1):
+ *       column i < gamma_b drives the test at position i, column G drives the
+ *       final draw;
+ *       accept_len [B] int32, tokens [B, G+1] int32 (committed tokens
+ *       y_0..y_{k-1}, then the drawn token at index k, then -1),
+ *       status [B] int32 bitmask (SPEC_ST_*), signals [B, 4] float32
+ *       (mean H, max H, mean c, min c), row_signals [B, G, 2] float32
+ *       (H_i, c_i), accept_prob [B, G] float32 (a_i for i <= k, NaN after).
+ *   - Every pointer except `workspace` sizes is DEVICE memory owned by the
+ *     caller.  The library never allocates, frees or synchronises: each call
+ *     only enqueues kernels on `stream` and returns.  Outputs are valid once
+ *     the stream reaches them.  `stream` may be NULL (legacy default stream).
+ *   - Logit rows may hold -inf (a token of probability 0).  NaN or +inf in a
+ *     row the method reads, or a row with no finite maximum, is an error.
+ *   - Rows past a request's gamma_b, and rows after its first reject (except
+ *     draft rows needed for signals), are never read.  Reading stops early:
+ *     rows the method does not need may or may not be read; the results do
+ *     not depend on which.
+ *   - Host return codes (SPEC_OK / SPEC_ERR_*) cover what the host can check
+ *     without touching device memory: null required pointers, sizes, dtype,
+ *     workspace size.  Nothing is launched when they are not SPEC_OK.
+ *   - Problems found on the device are reported per request in `status`.
+ *     A request with an error bit other than SPEC_ST_ZERO_RESIDUAL or
+ *     SPEC_ST_GUARDED commits nothing: accept_len = 0, tokens all -1,
+ *     accept_prob and signals NaN.  Other requests are unaffected.
+ *   - Given identical inputs the outputs are bit-identical from call to call.
+ *   - Calls that share a workspace must not overlap on the device (enqueue
+ *     them on one stream, or give each its own workspace).
+ */
+#ifndef SPEC_VERIFY_H
+#define SPEC_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;                       /* the CUDA runtime's cudaStream_t */
+typedef struct CUstream_st* spec_stream_t;
+
+/* logit dtypes */
+enum { SPEC_F32 = 0, SPEC_BF16 = 1 };
+
+/* host return codes */
+enum {
+    SPEC_OK = 0,
+    SPEC_ERR_INVALID_ARG = 1,   /* null pointer, bad size or dtype        */
+    SPEC_ERR_WORKSPACE = 2,     /* workspace NULL or smaller than needed  */
+    SPEC_ERR_CUDA = 3,          /* a CUDA call or launch failed           */
+    SPEC_ERR_UNSUPPORTED = 4    /* device is not sm_103 / sm_100 family   */
+};
+
+/* per-request status bits */
+enum {
+    SPEC_ST_OK = 0,
+    SPEC_ST_NONFINITE = 1,       /* NaN / +inf / no finite max in a read row */
+    SPEC_ST_BAD_TOKEN = 2,       /* draft token outside [0, V)              */
+    SPEC_ST_BAD_GAMMA = 4,       /* gamma_b outside [0, G]                  */
+    SPEC_ST_ZERO_RESIDUAL = 8,   /* residual mass rounded to 0: drew from p */
+    SPEC_ST_GUARDED = 16,        /* a near-tie decision was re-taken in
+                                    extended precision (informational)     */
+    SPEC_ST_TIMEOUT = 32,        /* an internal wait hit its time limit     */
+    SPEC_ST_BAD_TEMPERATURE = 64,/* temperature <= 0 or not finite          */
+    SPEC_ST_BAD_UNIFORM = 128    /* a uniform that was used is not in [0,1) */
+};
+
+/* Limits checked by the host: 1 <= B <= 65535, 0 <= G <= 31, 2 <= V < 2^28. */
+#define SPEC_MAX_B 65535
+#define SPEC_MAX_G 31
+
+/* Bytes of device workspace every call with these sizes needs (0 if the
+ * sizes are outside the limits).  Pure host function; the workspace holds
+ * per-row partial statistics, counters and the row schedule.  It needs no
+ * initialisation and no alignment beyond 256 bytes. */
+size_t spec_workspace_bytes(int B, int G, int V);
+
+/* Human-readable name of a host return code (SPEC_OK, SPEC_ERR_*). */
+const char* spec_status_string(int code);
+
+/* Human-readable name of one per-request status bit (SPEC_ST_*). */
+const char* spec_request_status_string(int bit);
+
+/* Number of kernels this host thread has launched through the library. */
+uint64_t spec_launch_count(void);
+
+/* Greedy verification (tutorial page, section 3.1).  For i = 0..gamma_b-1:
+ * g_i = argmax target row i (lowest index among equal maxima); stop at the
+ * first y_i != g_i with k = i and commit g_i; if none, k = gamma_b and commit
+ * the argmax of row gamma_b.  Temperature and uniforms are not used. */
+int spec_verify_greedy(const void* target_logits, int dtype, int B, int G, int V,
+                       const int32_t* draft_tokens, const int32_t* gamma,
+                       int32_t* accept_len, int32_t* tokens, int32_t* status,
+                       void* workspace, size_t workspace_bytes, spec_stream_t stream);
+
+/* Stochastic verification with full draft distributions (sections 3.2,
+ * 4, 5.1, 5.2).  accept_i  <=>  u_i * q_i(y_i) < p_i(y_i).  The final draw is
+ * inverse-CDF in ascending token order: with weights w (the residual
+ * [p_k - q_k]_+ after a reject at k, else p_gamma), W = sum w, t = u_G * W,
+ * the token is the smallest x with sum_{v<=x} w_v > t.  If the residual mass
+ * rounds to zero the draw uses p_k and sets SPEC_ST_ZERO_RESIDUAL.
+ * signals (optional, [B,4]): the SpecKV signals of q at the request's
+ * temperature over all gamma_b draft rows (NaN when gamma_b = 0); requesting
+ * them makes the call read every draft row.  accept_prob optional.
+ * draft_logits may be NULL only when G = 0. */
+int spec_verify_sample(const void* target_logits, const void* draft_logits, int dtype,
+                       int B, int G, int V,
+                       const int32_t* draft_tokens, const int32_t* gamma,
+                       const float* temperature, const float* uniforms,
+                       int32_t* accept_len, int32_t* tokens,
+                       float* signals, float* accept_prob, int32_t* status,
+                       void* workspace, size_t workspace_bytes, spec_stream_t stream);
+
+/* Stochastic verification with a one-hot q (section 3.3): accept_i <=>
+ * u_i < p_i(y_i); after a reject at k the draw uses p_k with y_k removed
+ * (W summed over v != y_k); else p_gamma.  accept_prob (optional) = p_i(y_i). */
+int spec_verify_onehot(const void* target_logits, int dtype, int B, int G, int V,
+                       const int32_t* draft_tokens, const int32_t* gamma,
+                       const float* temperature, const float* uniforms,
+                       int32_t* accept_len, int32_t* tokens,
+                       float* accept_prob, int32_t* status,
+                       void* workspace, size_t workspace_bytes, spec_stream_t stream);
+
+/* Draft signals only (SpecKV page): signals [B,4] required, row_signals
+ * [B,G,2] optional (NaN for i >= gamma_b), status optional. */
+int spec_draft_signals(const void* draft_logits, int dtype, int B, int G, int V,
+                       const int32_t* gamma, const float* temperature,
+                       float* signals, float* row_signals, int32_t* status,
+                       void* workspace, size_t workspace_bytes, spec_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SPEC_VERIFY_H */

@@ -1,0 +1,234 @@
+// api.cu -- the C ABI declared in include/spec_verify.h.
+//
+// Host side only: argument checks, workspace layout, and the three launches
+// of one call on the caller's stream:
+//   plan_kernel      (1 CTA)        resets counters, builds the row schedule;
+//   stats_kernel     (persistent)   streams the needed logit rows, decides
+//                                   each position as soon as its rows are in;
+//   finalize_kernel  (per request)  first reject, final draw, outputs.
+// The second and third launches use programmatic dependent launch so their
+// start-up overlaps the tail of the kernel before; each waits on
+// griddepcontrol.wait before reading what the previous kernel wrote.  The
+// plan kernel is launched without it, so it starts only after all earlier
+// work on the stream (which may be producing this call's inputs).
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "common.cuh"
+
+using namespace sv;
+
+namespace {
+
+thread_local uint64_t g_launches = 0;
+
+struct DevState {
+  bool ready = false;
+  int sms = 0;
+  int status = SPEC_OK;
+};
+constexpr int kMaxDevices = 64;
+DevState g_dev[kMaxDevices];
+std::mutex g_mu;
+
+int device_state(int* sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SPEC_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return SPEC_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DevState& d = g_dev[dev];
+  if (!d.ready) {
+    int major = 0, minor = 0, n = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return SPEC_ERR_CUDA;
+    if (major != 10 || minor != 3) {
+      d.status = SPEC_ERR_UNSUPPORTED;   // the library carries sm_103a code only
+    } else {
+      const cudaError_t e = configure_stats_kernels();
+      if (e != cudaSuccess) return SPEC_ERR_CUDA;
+      d.status = SPEC_OK;
+    }
+    d.sms = n;
+    d.ready = true;
+  }
+  *sms = d.sms;
+  return d.status;
+}
+
+bool sizes_ok(int B, int G, int V) {
+  if (B < 1 || B > SPEC_MAX_B || G < 0 || G > SPEC_MAX_G || V < 2 || V >= (1 << 28)) return false;
+  // work items are counted in 32 bits
+  const long long ce = chunk_elems(SPEC_F32);
+  const long long rows = (long long)B * (2 * G + 1);
+  return rows * ((V + ce - 1) / ce) < (1ll << 31);
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+struct Call {
+  int mode;
+  const void* target;
+  const void* draft;
+  int dtype, B, G, V;
+  const int32_t* draft_tokens;
+  const int32_t* gamma;
+  const float* temperature;
+  const float* uniforms;
+  int32_t* accept_len;
+  int32_t* tokens;
+  int32_t* status;
+  float* signals;
+  float* row_signals;
+  float* accept_prob;
+  void* workspace;
+  size_t workspace_bytes;
+  cudaStream_t stream;
+};
+
+int run(const Call& c) {
+  if (!sizes_ok(c.B, c.G, c.V) || (c.dtype != SPEC_F32 && c.dtype != SPEC_BF16)) return SPEC_ERR_INVALID_ARG;
+  const size_t es = c.dtype == SPEC_BF16 ? 2 : 4;
+  const bool greedy = c.mode == MODE_GREEDY, sample = c.mode == MODE_SAMPLE, sig = c.mode == MODE_SIGNALS;
+  // required pointers
+  if (!sig && (!c.target || !c.accept_len || !c.tokens)) return SPEC_ERR_INVALID_ARG;
+  if (!sig && c.G > 0 && !c.draft_tokens) return SPEC_ERR_INVALID_ARG;
+  if ((sample || sig) && c.G > 0 && !c.draft) return SPEC_ERR_INVALID_ARG;
+  if (!greedy && !c.temperature) return SPEC_ERR_INVALID_ARG;
+  if ((sample || c.mode == MODE_ONEHOT) && !c.uniforms) return SPEC_ERR_INVALID_ARG;
+  if (sig && !c.signals) return SPEC_ERR_INVALID_ARG;
+  if (!aligned(c.target, es) || !aligned(c.draft, es)) return SPEC_ERR_INVALID_ARG;
+  const void* ptrs4[] = {c.draft_tokens, c.gamma, c.temperature, c.uniforms, c.accept_len, c.tokens,
+                         c.status, c.signals, c.row_signals, c.accept_prob};
+  for (const void* p : ptrs4)
+    if (!aligned(p, 4)) return SPEC_ERR_INVALID_ARG;
+  const Layout L = make_layout(c.B, c.G, c.V, c.dtype);
+  if (!c.workspace || c.workspace_bytes < L.total) return SPEC_ERR_WORKSPACE;
+  if (!aligned(c.workspace, 256)) return SPEC_ERR_INVALID_ARG;
+  int sms = 0;
+  const int ds = device_state(&sms);
+  if (ds != SPEC_OK) return ds;
+
+  unsigned char* ws = static_cast<unsigned char*>(c.workspace);
+  Params P{};
+  P.target = static_cast<const unsigned char*>(c.target);
+  P.draft = static_cast<const unsigned char*>(c.draft);
+  P.dtype = c.dtype; P.B = c.B; P.G = c.G; P.V = c.V; P.mode = c.mode;
+  P.signals_on = sig ? 1 : (sample && c.signals ? 1 : 0);
+  P.draft_tokens = c.draft_tokens; P.gamma = c.gamma; P.temperature = c.temperature; P.uniforms = c.uniforms;
+  P.accept_len = c.accept_len; P.tokens = c.tokens; P.status = c.status;
+  P.signals = c.signals; P.row_signals = c.row_signals; P.accept_prob = c.accept_prob;
+  P.hdr = reinterpret_cast<Header*>(ws + L.hdr);
+  P.req_flags = reinterpret_cast<int*>(ws + L.req_flags);
+  P.known_reject = reinterpret_cast<int*>(ws + L.known_reject);
+  P.row_list = reinterpret_cast<int*>(ws + L.row_list);
+  P.row_arr = reinterpret_cast<unsigned*>(ws + L.row_arr);
+  P.row_done = reinterpret_cast<int*>(ws + L.row_done);
+  P.row_stats = reinterpret_cast<RowStats*>(ws + L.row_stats);
+  P.parts = reinterpret_cast<Part*>(ws + L.parts);
+  P.pair_arr = reinterpret_cast<unsigned*>(ws + L.pair_arr);
+  P.pair_res = reinterpret_cast<int*>(ws + L.pair_res);
+  P.pair_a = reinterpret_cast<double*>(ws + L.pair_a);
+  P.draw_arr = reinterpret_cast<unsigned*>(ws + L.draw_arr);
+  P.draw_parts = reinterpret_cast<double*>(ws + L.draw_parts);
+  P.nrows = L.nrows; P.nch = L.nch; P.nch2 = L.nch2;
+
+  // persistent grid: two CTAs per SM, never more CTAs than work items
+  const long long max_items = (long long)c.B * (2 * c.G + 1) * L.nch;
+  const int grid1 = (int)(max_items < 2ll * sms ? max_items : 2ll * sms);
+  cudaError_t e = launch_plan(P, c.stream);
+  if (e == cudaSuccess) {
+    ++g_launches;
+    e = launch_stats(P, grid1 > 0 ? grid1 : 1, c.stream, true);
+  }
+  if (e == cudaSuccess) {
+    ++g_launches;
+    e = launch_finalize(P, dim3(sample ? L.nch2 : 1, c.B), c.stream, true);
+  }
+  if (e == cudaSuccess) ++g_launches;
+  return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t spec_workspace_bytes(int B, int G, int V) {
+  if (!sizes_ok(B, G, V)) return 0;
+  const Layout a = make_layout(B, G, V, SPEC_F32), b = make_layout(B, G, V, SPEC_BF16);
+  return a.total > b.total ? a.total : b.total;
+}
+
+const char* spec_status_string(int code) {
+  switch (code) {
+    case SPEC_OK: return "ok";
+    case SPEC_ERR_INVALID_ARG: return "invalid argument";
+    case SPEC_ERR_WORKSPACE: return "workspace missing or too small";
+    case SPEC_ERR_CUDA: return "CUDA launch or runtime error";
+    case SPEC_ERR_UNSUPPORTED: return "device is not sm_103";
+    default: break;
+  }
+  return "unknown code";
+}
+
+const char* spec_request_status_string(int bit) {
+  switch (bit) {
+    case SPEC_ST_OK: return "ok";
+    case SPEC_ST_NONFINITE: return "non-finite logits in a row that was read";
+    case SPEC_ST_BAD_TOKEN: return "draft token outside [0, V)";
+    case SPEC_ST_BAD_GAMMA: return "gamma outside [0, G]";
+    case SPEC_ST_ZERO_RESIDUAL: return "residual mass rounded to zero; drew from p";
+    case SPEC_ST_GUARDED: return "near-tie decision re-taken in extended precision";
+    case SPEC_ST_TIMEOUT: return "internal wait timed out";
+    case SPEC_ST_BAD_TEMPERATURE: return "temperature not positive and finite";
+    case SPEC_ST_BAD_UNIFORM: return "uniform outside [0, 1)";
+    default: break;
+  }
+  return "unknown status bit";
+}
+
+uint64_t spec_launch_count(void) { return g_launches; }
+
+int spec_verify_greedy(const void* target_logits, int dtype, int B, int G, int V, const int32_t* draft_tokens,
+                       const int32_t* gamma, int32_t* accept_len, int32_t* tokens, int32_t* status,
+                       void* workspace, size_t workspace_bytes, spec_stream_t stream) {
+  Call c{MODE_GREEDY, target_logits, nullptr, dtype, B, G, V, draft_tokens, gamma, nullptr, nullptr,
+         accept_len, tokens, status, nullptr, nullptr, nullptr, workspace, workspace_bytes,
+         reinterpret_cast<cudaStream_t>(stream)};
+  return run(c);
+}
+
+int spec_verify_sample(const void* target_logits, const void* draft_logits, int dtype, int B, int G, int V,
+                       const int32_t* draft_tokens, const int32_t* gamma, const float* temperature,
+                       const float* uniforms, int32_t* accept_len, int32_t* tokens, float* signals,
+                       float* accept_prob, int32_t* status, void* workspace, size_t workspace_bytes,
+                       spec_stream_t stream) {
+  Call c{MODE_SAMPLE, target_logits, draft_logits, dtype, B, G, V, draft_tokens, gamma, temperature, uniforms,
+         accept_len, tokens, status, signals, nullptr, accept_prob, workspace, workspace_bytes,
+         reinterpret_cast<cudaStream_t>(stream)};
+  return run(c);
+}
+
+int spec_verify_onehot(const void* target_logits, int dtype, int B, int G, int V, const int32_t* draft_tokens,
+                       const int32_t* gamma, const float* temperature, const float* uniforms, int32_t* accept_len,
+                       int32_t* tokens, float* accept_prob, int32_t* status, void* workspace,
+                       size_t workspace_bytes, spec_stream_t stream) {
+  Call c{MODE_ONEHOT, target_logits, nullptr, dtype, B, G, V, draft_tokens, gamma, temperature, uniforms,
+         accept_len, tokens, status, nullptr, nullptr, accept_prob, workspace, workspace_bytes,
+         reinterpret_cast<cudaStream_t>(stream)};
+  return run(c);
+}
+
+int spec_draft_signals(const void* draft_logits, int dtype, int B, int G, int V, const int32_t* gamma,
+                       const float* temperature, float* signals, float* row_signals, int32_t* status,
+                       void* workspace, size_t workspace_bytes, spec_stream_t stream) {
+  Call c{MODE_SIGNALS, nullptr, draft_logits, dtype, B, G, V, nullptr, gamma, temperature, nullptr,
+         nullptr, nullptr, status, signals, row_signals, nullptr, workspace, workspace_bytes,
+         reinterpret_cast<cudaStream_t>(stream)};
+  return run(c);
+}
+
+}  // extern "C"

@@ -1,0 +1,379 @@
+// common.cuh -- shared definitions of the sm_103a verification kernels:
+// launch parameters, workspace layout, inline-PTX wrappers (mbarrier, bulk
+// copy, scoped atomics) and the per-row softmax statistics.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/spec_verify.h"
+
+namespace sv {
+
+// ---------------------------------------------------------------------------
+// modes and codes
+
+enum Mode : int { MODE_GREEDY = 0, MODE_SAMPLE = 1, MODE_ONEHOT = 2, MODE_SIGNALS = 3 };
+enum RowKind : int { KIND_TARGET = 0, KIND_DRAFT = 1 };
+
+// per-position test result written by the stats kernel, read by finalize
+enum PairCode : int {
+  PC_NONE = 0,        // not evaluated (position after a known reject)
+  PC_ACCEPT = 1,
+  PC_REJECT = 2,
+  PC_NONFINITE = 3,
+  PC_BAD_TOKEN = 4,
+  PC_BAD_UNIFORM = 5,
+};
+constexpr int PC_UNCERTAIN = 16;   // or-ed in: |u - a| inside the guard band
+
+// ---------------------------------------------------------------------------
+// geometry
+
+constexpr int kConsumerWarps = 8;
+constexpr int kConsumerThreads = kConsumerWarps * 32;
+constexpr int kStatsThreads = kConsumerThreads + 64;   // + producer warp + epilogue warp
+constexpr int kStageBytes = 16384;                      // one bulk copy
+constexpr int kStages = 6;                              // ring depth per CTA
+constexpr int kChunkBytes = 2 * kStageBytes;            // one work item of a row
+constexpr int kEpiSlots = 8;                            // consumer -> epilogue ring
+constexpr int kDrawChunkElems = 4096;                   // residual pass chunk
+constexpr int kDrawThreads = 256;
+constexpr uint32_t kSkipInc = 1u << 20;                 // arrival mark of a skipped chunk
+constexpr uint32_t kCountMask = kSkipInc - 1;
+constexpr int kNoReject = 0x7fffffff;
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s per wait
+
+// ---------------------------------------------------------------------------
+// partial statistics of a run of logits, relative to its own max m:
+//   s = sum 2^{(x-m)c},  t = sum (x-m)c * 2^{(x-m)c}  (entropy numerator),
+//   idx = lowest index attaining m,  bad = a NaN was seen (argmax mode).
+struct alignas(16) Part {
+  float m, s, t;
+  int idx;   // bit 30 set: NaN seen (argmax mode); low bits: index
+};
+constexpr int kIdxNaN = 1 << 30;
+
+struct alignas(16) RowStats {
+  float m, s, t;
+  int idx;
+};
+
+// ---------------------------------------------------------------------------
+// workspace layout (offsets in bytes, 256-aligned)
+
+struct Layout {
+  size_t hdr, req_flags, known_reject, row_list, row_arr, row_done, row_stats, parts,
+      pair_arr, pair_res, pair_a, draw_arr, draw_parts, total;
+  int nrows;      // B*(G+1) + B*G row ids
+  int nch;        // stats chunks per row
+  int nch2;       // residual-pass chunks per row
+};
+
+struct Header {
+  unsigned int queue;      // next work item to claim
+  unsigned int n_items;    // work items this call
+  unsigned int error;      // SPEC_ST_TIMEOUT when any wait gave up
+  unsigned int n_uncertain;
+};
+
+__host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+__host__ __device__ inline int chunk_elems(int dtype) { return kChunkBytes / (dtype == SPEC_BF16 ? 2 : 4); }
+
+__host__ inline Layout make_layout(int B, int G, int V, int dtype) {
+  Layout L{};
+  const int nrows = B * (G + 1) + B * G;
+  const int ce = chunk_elems(dtype);
+  L.nrows = nrows;
+  L.nch = (V + ce - 1) / ce;
+  L.nch2 = (V + kDrawChunkElems - 1) / kDrawChunkElems;
+  size_t o = 0;
+  L.hdr = o;          o = align256(o + sizeof(Header));
+  L.req_flags = o;    o = align256(o + sizeof(int) * B);
+  L.known_reject = o; o = align256(o + sizeof(int) * B);
+  L.row_list = o;     o = align256(o + sizeof(int) * nrows);
+  L.row_arr = o;      o = align256(o + sizeof(unsigned) * nrows);
+  L.row_done = o;     o = align256(o + sizeof(int) * nrows);
+  L.row_stats = o;    o = align256(o + sizeof(RowStats) * nrows);
+  L.parts = o;        o = align256(o + sizeof(Part) * (size_t)nrows * L.nch);
+  L.pair_arr = o;     o = align256(o + sizeof(unsigned) * B * (G + 1));
+  L.pair_res = o;     o = align256(o + sizeof(int) * B * (G + 1));
+  L.pair_a = o;       o = align256(o + sizeof(double) * B * (G + 1));
+  L.draw_arr = o;     o = align256(o + sizeof(unsigned) * B);
+  L.draw_parts = o;   o = align256(o + sizeof(double) * (size_t)B * L.nch2);
+  L.total = o;
+  return L;
+}
+
+// ---------------------------------------------------------------------------
+// launch parameters (passed by value to every kernel)
+
+struct Params {
+  const unsigned char* target;   // [B, G+1, V]
+  const unsigned char* draft;    // [B, G, V] or null
+  int dtype, B, G, V, mode, signals_on;
+  const int32_t* draft_tokens;
+  const int32_t* gamma;
+  const float* temperature;
+  const float* uniforms;
+  int32_t* accept_len;
+  int32_t* tokens;
+  int32_t* status;
+  float* signals;
+  float* row_signals;
+  float* accept_prob;
+  // workspace views
+  Header* hdr;
+  int* req_flags;
+  int* known_reject;
+  int* row_list;
+  unsigned* row_arr;
+  int* row_done;
+  RowStats* row_stats;
+  Part* parts;
+  unsigned* pair_arr;
+  int* pair_res;
+  double* pair_a;
+  unsigned* draw_arr;
+  double* draw_parts;
+  int nrows, nch, nch2;
+};
+
+// row ids: target rows first, then draft rows
+__host__ __device__ inline int target_row_id(int b, int i, int G) { return b * (G + 1) + i; }
+__host__ __device__ inline int draft_row_id(int b, int i, int B, int G) { return B * (G + 1) + b * G + i; }
+
+__device__ inline void decode_row(int rid, int B, int G, int& kind, int& b, int& i) {
+  const int nt = B * (G + 1);
+  if (rid < nt) { kind = KIND_TARGET; b = rid / (G + 1); i = rid - b * (G + 1); }
+  else { rid -= nt; kind = KIND_DRAFT; b = rid / G; i = rid - b * G; }
+}
+
+// flat element offset of a row inside its tensor
+__device__ inline long long row_elem_offset(int kind, int b, int i, int G, int V) {
+  return kind == KIND_TARGET ? ((long long)b * (G + 1) + i) * V : ((long long)b * G + i) * V;
+}
+
+// ---------------------------------------------------------------------------
+// inline PTX
+
+__device__ __forceinline__ float ex2(float x) {   // 2^x, hardware approximation, ftz
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ unsigned long long globaltimer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for phase `parity` of `bar` to complete; gives up after kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (globaltimer() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+// 1-D bulk copy global -> shared, completion counted on `bar` (bytes % 16 == 0,
+// both addresses 16-byte aligned).
+__device__ __forceinline__ void bulk_load(void* smem_dst, const void* gmem_src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(smem_dst)),
+      "l"(gmem_src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ unsigned atom_add_acqrel(unsigned* p, unsigned v) {
+  unsigned old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
+__device__ __forceinline__ void red_add_release(unsigned* p, unsigned v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ int ld_relaxed(const int* p) {
+  int v;
+  asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// ---------------------------------------------------------------------------
+// logits
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// One logit from global memory (for the few scalar accesses).
+__device__ __forceinline__ float load_logit(const unsigned char* base, int dtype, long long elem) {
+  if (dtype == SPEC_BF16) {
+    unsigned short h = __ldg(reinterpret_cast<const unsigned short*>(base) + elem);
+    return __uint_as_float(static_cast<uint32_t>(h) << 16);
+  }
+  return __ldg(reinterpret_cast<const float*>(base) + elem);
+}
+
+// log2(e) / T, rounded once to fp32 (the scale used by every kernel)
+__device__ __forceinline__ float scale_of(float T) { return (float)(1.4426950408889634 / (double)T); }
+
+__device__ __forceinline__ bool temperature_ok(float T) { return T > 0.f && isfinite(T); }
+
+// A row is usable iff its max is finite, its sum is finite and positive and
+// no NaN was seen.
+__device__ __forceinline__ bool row_ok(const RowStats& r, bool argmax_mode) {
+  if (!isfinite(r.m)) return false;
+  if (argmax_mode) return (r.idx & kIdxNaN) == 0;
+  return isfinite(r.s) && r.s > 0.f;
+}
+
+// Merge of two partials of the same row (online-softmax rule):
+//   m = max(m1, m2); s = sum_j s_j 2^{(m_j - m)c}; t = sum_j 2^{d_j}(t_j + d_j s_j).
+__device__ __forceinline__ Part merge_parts(const Part& a, const Part& b, float c, bool ent) {
+  Part r;
+  const float m = fmaxf(a.m, b.m);
+  r.m = m;
+  if (m == -INFINITY) {          // both empty
+    r.s = 0.f; r.t = 0.f;
+  } else {
+    float sa = 0.f, ta = 0.f, sb = 0.f, tb = 0.f;
+    if (a.s != 0.f) {
+      const float d = (a.m - m) * c;
+      const float f = ex2(d);
+      sa = a.s * f;
+      if (ent) ta = f * fmaf(d, a.s, a.t);
+    }
+    if (b.s != 0.f) {
+      const float d = (b.m - m) * c;
+      const float f = ex2(d);
+      sb = b.s * f;
+      if (ent) tb = f * fmaf(d, b.s, b.t);
+    }
+    // NaN partial sums stay NaN (the row is then rejected as non-finite)
+    if (a.s != a.s) sa = a.s;
+    if (b.s != b.s) sb = b.s;
+    r.s = sa + sb;
+    r.t = ta + tb;
+  }
+  const int ia = a.idx & ~kIdxNaN, ib = b.idx & ~kIdxNaN;
+  int idx;
+  if (a.m > b.m) idx = ia;
+  else if (b.m > a.m) idx = ib;
+  else idx = ia < ib ? ia : ib;
+  r.idx = idx | ((a.idx | b.idx) & kIdxNaN);
+  return r;
+}
+
+__device__ __forceinline__ Part shfl_part(const Part& p, int src_lane_xor) {
+  Part q;
+  q.m = __shfl_xor_sync(0xffffffffu, p.m, src_lane_xor);
+  q.s = __shfl_xor_sync(0xffffffffu, p.s, src_lane_xor);
+  q.t = __shfl_xor_sync(0xffffffffu, p.t, src_lane_xor);
+  q.idx = __shfl_xor_sync(0xffffffffu, p.idx, src_lane_xor);
+  return q;
+}
+
+// Merge of two argmax-only partials (greedy rows).
+__device__ __forceinline__ Part merge_argmax(const Part& a, const Part& b) {
+  Part r;
+  r.m = fmaxf(a.m, b.m);
+  r.s = 0.f; r.t = 0.f;
+  const int ia = a.idx & ~kIdxNaN, ib = b.idx & ~kIdxNaN;
+  int idx;
+  if (a.m > b.m) idx = ia;
+  else if (b.m > a.m) idx = ib;
+  else idx = ia < ib ? ia : ib;
+  r.idx = idx | ((a.idx | b.idx) & kIdxNaN);
+  return r;
+}
+
+// 16-byte loads/stores that bypass L1 (data written by other CTAs of the grid)
+__device__ __forceinline__ Part ldcg_part(const Part* p) {
+  const float4 v = __ldcg(reinterpret_cast<const float4*>(p));
+  Part r;
+  r.m = v.x; r.s = v.y; r.t = v.z; r.idx = __float_as_int(v.w);
+  return r;
+}
+__device__ __forceinline__ RowStats ldcg_stats(const RowStats* p) {
+  const float4 v = __ldcg(reinterpret_cast<const float4*>(p));
+  RowStats r;
+  r.m = v.x; r.s = v.y; r.t = v.z; r.idx = __float_as_int(v.w);
+  return r;
+}
+__device__ __forceinline__ void stcg_part(Part* p, const Part& v) {
+  __stcg(reinterpret_cast<float4*>(p), make_float4(v.m, v.s, v.t, __int_as_float(v.idx)));
+}
+
+__device__ __forceinline__ Part empty_part() {
+  Part p;
+  p.m = -INFINITY; p.s = 0.f; p.t = 0.f; p.idx = 0x3fffffff;
+  return p;
+}
+
+// kernels (defined in the .cu files)
+__global__ void plan_kernel(Params P);
+
+// Host-side launchers, one per translation unit that defines the kernels.
+// The caller's stream; `pdl` enables programmatic dependent launch.
+cudaError_t launch_plan(const Params& P, cudaStream_t s);
+cudaError_t launch_stats(const Params& P, int grid, cudaStream_t s, bool pdl);
+cudaError_t launch_finalize(const Params& P, dim3 grid, cudaStream_t s, bool pdl);
+cudaError_t configure_stats_kernels();   // dynamic shared-memory limit, current device
+
+template <class K>
+inline cudaError_t launch_ex(K kern, dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl, const Params& P) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = pdl ? attr : nullptr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, P);
+}
+
+}  // namespace sv

@@ -1,0 +1,179 @@
+"""GPU path against the fp64 oracle, element by element, through the C ABI."""
+import numpy as np
+import pytest
+
+import oracle as O
+import parity as PT
+from speculative_decoding_verification_26_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import speculative_decoding_verification_26_gb300 as sv
+    sv.lib()
+    return torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module")
+def o():
+    return O.load()
+
+
+def _run(o, dev, name, mode, rounds=1, tally=None, **kw):
+    tally = tally or PT.Tally()
+    for r in range(rounds):
+        wl = PT.make_workload(o, name, r, **kw)
+        g = PT.run_gpu(mode, wl, dev)
+        ref = PT.run_oracle(o, mode, wl)
+        PT.compare(o, mode, wl, g, ref, tally)
+    return tally
+
+
+# ---- small case (several tiles and a ragged tail are covered below) ----------
+
+@pytest.mark.parametrize("mode", ["greedy", "sample", "onehot"])
+def test_c1_small_fp32(o, dev, mode):
+    t = _run(o, dev, "c1", mode, rounds=8)
+    assert t.disagree == 0, t
+
+
+@pytest.mark.parametrize("V", [2, 3, 7, 1000, 1001, 4093, 16385, 40000, 65537])
+@pytest.mark.parametrize("dtype", [W.BF16, W.F32])
+@pytest.mark.parametrize("mode", ["greedy", "sample", "onehot"])
+def test_ragged_vocab(o, dev, V, dtype, mode):
+    """Vocabularies that are not multiples of the vector width or of a chunk:
+    unaligned rows, scalar heads/tails, several chunks plus a ragged one."""
+    over = {"dtype": dtype, "zipf": True, "sigma_d": 1.0, "T": 0.8, "draft": "sample_q"}
+    t = PT.Tally()
+    for r in range(2):
+        wl = PT.make_workload(o, "c3", r, B=5, G=3, V=V, overrides=over)
+        g = PT.run_gpu(mode, wl, dev)
+        ref = PT.run_oracle(o, mode, wl)
+        PT.compare(o, mode, wl, g, ref, t)
+    assert t.disagree == 0, t
+
+
+# ---- the workloads at full size ---------------------------------------------
+
+def test_c2_greedy_full(o, dev):
+    t = _run(o, dev, "c2", "greedy", rounds=2)
+    assert t.disagree == 0
+
+
+def test_c3_sample_signals_full(o, dev):
+    t = _run(o, dev, "c3", "sample", rounds=2)
+    print(t)
+    assert t.disagree <= max(1, t.flagged)
+
+
+def test_c4_onehot_full(o, dev):
+    t = _run(o, dev, "c4", "onehot", rounds=2)
+    print(t)
+    assert t.disagree <= max(1, t.flagged)
+
+
+def test_c5_ragged_gamma_full(o, dev):
+    t = _run(o, dev, "c5", "sample", rounds=1)
+    print(t)
+    assert t.disagree <= max(1, t.flagged)
+
+
+def test_m_headline_full(o, dev):
+    t = _run(o, dev, "m", "sample", rounds=2)
+    print(t)
+    assert t.disagree <= max(1, t.flagged)
+
+
+# ---- edge cases ---------------------------------------------------------------
+
+def test_gamma_zero_and_mixed(o, dev):
+    """gamma_b = 0 (a plain draw from p_0) mixed with full-length requests."""
+    wl = PT.make_workload(o, "c3", 3, B=12, G=4, V=3000)
+    wl.gamma[:] = np.array([0, 1, 2, 3, 4, 0, 4, 4, 1, 0, 2, 3], np.int32)
+    for mode in ["greedy", "sample", "onehot"]:
+        g = PT.run_gpu(mode, wl, dev)
+        PT.compare(o, mode, wl, g, PT.run_oracle(o, mode, wl), PT.Tally())
+
+
+def test_G_zero(o, dev):
+    wl = PT.make_workload(o, "c3", 4, B=6, G=0, V=5000)
+    for mode in ["greedy", "sample", "onehot"]:
+        g = PT.run_gpu(mode, wl, dev)
+        PT.compare(o, mode, wl, g, PT.run_oracle(o, mode, wl), PT.Tally())
+
+
+def test_p_equals_q_never_rejects(o, dev):
+    wl = PT.make_workload(o, "c3", 5, B=16, G=6, V=20000)
+    wl.draft = np.ascontiguousarray(wl.target[:, :6, :])
+    W.resolve_draft_tokens(wl, *PT.oracle_samplers(o))
+    g = PT.run_gpu("sample", wl, dev)
+    assert np.all(g["accept_len"] == 6)
+    PT.compare(o, "sample", wl, g, PT.run_oracle(o, "sample", wl), PT.Tally())
+
+
+def test_greedy_ties_lowest_index(o, dev):
+    """Integer-valued logits: many equal maxima; the lowest index must win."""
+    rng = np.random.default_rng(9)
+    wl = PT.make_workload(o, "c1", 0, B=32, G=5, V=3000)
+    wl.target = rng.integers(-4, 4, wl.target.shape).astype(np.float32)
+    am = o.run(O.GREEDY, target=wl.target.reshape(-1, 1, 3000), G=0)["tokens"][:, 0].reshape(32, 6)
+    wl.draft_tokens = np.ascontiguousarray(am[:, :5]).astype(np.int32)
+    flip = rng.random((32, 5)) < 0.2
+    wl.draft_tokens[flip] = rng.integers(0, 3000, flip.sum())
+    g = PT.run_gpu("greedy", wl, dev)
+    PT.compare(o, "greedy", wl, g, PT.run_oracle(o, "greedy", wl), PT.Tally())
+
+
+def test_bad_inputs_are_reported_per_request(o, dev):
+    wl = PT.make_workload(o, "c3", 6, B=10, G=3, V=4000, overrides={"dtype": W.F32})
+    wl.target = wl.target.copy()
+    wl.target[0, 0, 17] = np.nan                      # NaN in a row that is read
+    wl.target[1, 0, 5] = np.inf                       # +inf
+    wl.target[2, 0, :] = -np.inf                      # no finite max
+    wl.target[3, 0, 100:200] = -np.inf                # masked tokens: fine
+    wl.draft_tokens = wl.draft_tokens.copy()
+    wl.draft_tokens[4, 0] = 4000                      # bad token
+    wl.gamma = wl.gamma.copy()
+    wl.gamma[5] = 4                                   # bad gamma
+    wl.temperature = wl.temperature.copy()
+    wl.temperature[6] = 0.0                           # bad temperature
+    wl.uniforms = wl.uniforms.copy()
+    wl.uniforms[7, 3] = 1.0                           # bad draw uniform
+    wl.target[8, 3, 9] = np.nan                       # after gamma: never read
+    for mode in ["greedy", "sample", "onehot"]:
+        g = PT.run_gpu(mode, wl, dev)
+        ref = PT.run_oracle(o, mode, wl)
+        PT.compare(o, mode, wl, g, ref, PT.Tally())
+        assert ref["status"][0] == O.ST_NONFINITE
+
+
+def test_repeatable(o, dev):
+    wl = PT.make_workload(o, "m", 0, B=16)
+    a = PT.run_gpu("sample", wl, dev)
+    b = PT.run_gpu("sample", wl, dev)
+    for k in a:
+        np.testing.assert_array_equal(a[k], b[k])
+
+
+def test_draft_signals_standalone(o, dev):
+    import torch
+
+    import speculative_decoding_verification_26_gb300 as sv
+    for name in ["c1", "c5"]:
+        wl = PT.make_workload(o, name, 7, B=min(W.CONFIGS[name]["B"], 48))
+        r = sv.draft_signals(PT.logits_dev(wl, "draft", dev), PT.to_dev(wl.gamma, dev),
+                             PT.to_dev(wl.temperature, dev), row_signals=True)
+        torch.cuda.synchronize()
+        g = {k: v.cpu().numpy().astype(np.float64) for k, v in r.items()}
+        ref = o.draft_signals(wl.draft, wl.gamma, wl.temperature, want_row_signals=True)
+        for key in ("signals", "row_signals"):
+            so, sg = ref[key], g[key]
+            both_nan = np.isnan(so) & np.isnan(sg)
+            ok = both_nan | (np.abs(sg - so) <= PT.REL * np.abs(so) + 1e-6)
+            assert ok.all(), (name, key, sg[~ok][:4], so[~ok][:4])
+        np.testing.assert_array_equal(g["status"], ref["status"])
