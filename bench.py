@@ -1,0 +1,454 @@
+#!/usr/bin/env python3
+"""Throughput of batched speculative-sampling verification on GB300.
+
+One step = one spec_verify_sample call (plan + stats + finalize kernels) over
+one synthetic round of the headline workload: B = 64 requests, gamma = 7,
+V = 151936 bf16 logits, full-q verification with the SpecKV draft signals.
+The metric is verify rounds/s (whole job, all ranks); the roofline is the HBM
+bandwidth of the statistics kernel on the bytes the method must read.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+N > 1 is launched by torchrun: every rank verifies its own request batches
+(requests are independent, so the work shards with no data-path exchange:
+weak scaling); rank 0 prints one JSON line with the max time over ranks.
+--impl reference times the fp64 CPU oracle on the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from speculative_decoding_verification_26_gb300 import workloads as W  # noqa: E402
+
+METRIC = "verify rounds/s and HBM GB/s (% of 8 TB/s) at B=64, gamma=7, V=151936 bf16"
+UNIT = "rounds/s"
+WORKLOAD = "m"
+WORKLOAD_DESC = ("B=64 gamma=7 V=151936 bf16, full-q stochastic verify + draft signals; T=0.7, "
+                 "target N(0,3^2)+Zipf(1.1) bias, draft = target + N(0,1.5^2), y ~ q")
+L2_BYTES = 129 * 2**20
+
+
+# ----------------------------------------------------------------------------
+# multi-rank plumbing (also exercised by the gloo tests on CPU)
+
+def rank_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """Max of a per-rank scalar over all ranks (identity for one rank)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, world: int, device=None) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def job_rate(units_all_ranks: float, t_max_s: float) -> float:
+    return units_all_ranks / t_max_s if t_max_s > 0 else 0.0
+
+
+def rank_round_index(rank: int, s: int) -> int:
+    """Seed index of input set s on `rank`: every rank verifies its own requests."""
+    return 1000 * rank + s
+
+
+# ----------------------------------------------------------------------------
+# clocks during the timed region
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(self.gpu)], stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                p = [x.strip() for x in line.split(",")]
+                if len(p) >= 9:
+                    rows.append(p)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------
+# our arm
+
+def source_sha() -> str:
+    h = hashlib.sha256()
+    for rel in ("speculative_decoding_verification_26_gb300/csrc/stats.cu",
+                "speculative_decoding_verification_26_gb300/csrc/common.cuh"):
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """Per-launch DRAM bytes of the statistics kernel from the committed ncu
+    summary, if it was taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "stats_kernel_m_traffic.txt")
+    try:
+        with open(path) as f:
+            d = json.loads(f.read().split("\n---\n")[0])
+    except (OSError, ValueError):
+        return None
+    if d.get("source_sha") != source_sha():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def build_inputs(dev, rank, nsets, sv, torch):
+    """Seeded input sets resident on the device (draft tokens drawn from q by
+    the library's own gamma = 0 draw on the draft rows)."""
+    sets = []
+    for s in range(nsets):
+        wl = W.make(WORKLOAD, rank_round_index(rank, s))
+        B, G, V = wl.B, wl.G, wl.V
+        tgt = torch.from_numpy(wl.target.view(np.int16)).to(dev).view(torch.bfloat16)
+        dr = torch.from_numpy(wl.draft.view(np.int16)).to(dev).view(torch.bfloat16)
+        rows = dr.view(B * G, 1, V)
+        temps = torch.from_numpy(np.repeat(wl.temperature, G)).to(dev)
+        u = torch.from_numpy(wl.draft_aux["uniforms"].reshape(B * G, 1)).to(dev)
+        r = sv.verify_sample(rows, None, torch.zeros(B * G, 0, dtype=torch.int32, device=dev), None, temps, u,
+                             signals=False)
+        torch.cuda.synchronize()
+        assert int(r["status"].abs().sum()) == 0
+        y = r["tokens"][:, 0].reshape(B, G).contiguous()
+        sets.append(dict(target=tgt, draft=dr, tokens=y, gamma=torch.from_numpy(wl.gamma).to(dev),
+                         temperature=torch.from_numpy(wl.temperature).to(dev),
+                         uniforms=torch.from_numpy(wl.uniforms).to(dev), host=wl))
+    return sets
+
+
+def run_ours(args):
+    import torch
+
+    import speculative_decoding_verification_26_gb300 as sv
+    rank, world, local = rank_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", init_method="env://")
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    L = sv.lib()
+    stream = torch.cuda.current_stream(dev)
+    sets = build_inputs(dev, rank, args.sets, sv, torch)
+    B, G, V = sets[0]["host"].B, sets[0]["host"].G, sets[0]["host"].V
+    ws = torch.empty(sv.workspace_bytes(B, G, V), dtype=torch.uint8, device=dev)
+    out = dict(accept_len=torch.empty(B, dtype=torch.int32, device=dev),
+               tokens=torch.empty(B, G + 1, dtype=torch.int32, device=dev),
+               status=torch.empty(B, dtype=torch.int32, device=dev),
+               signals=torch.empty(B, 4, dtype=torch.float32, device=dev))
+
+    def step(k):
+        s = sets[k % len(sets)]
+        return sv.verify_sample(s["target"], s["draft"], s["tokens"], s["gamma"], s["temperature"], s["uniforms"],
+                                signals=True, ws=ws, out=out)
+
+    # per-set outcome (accept lengths) -> committed tokens and algorithmic bytes
+    rows_needed, committed = [], []
+    for k in range(len(sets)):
+        r = step(k)
+        torch.cuda.synchronize()
+        kk = r["accept_len"].cpu().numpy().astype(np.int64)
+        gam = sets[k]["host"].gamma.astype(np.int64)
+        rows_needed.append(int(np.sum(kk + 1) + np.sum(gam)))      # target 0..k, every draft row
+        committed.append(int(np.sum(kk + 1)))
+        assert int(r["status"].abs().sum()) == 0
+    es = 2
+    F_bytes = int((2 * sets[0]["host"].gamma.astype(np.int64) + 1).sum()) * V * es   # every valid row once
+
+    # warm-up (at least W calls and ~0.5 s so clocks settle)
+    props = torch.cuda.get_device_properties(dev)
+    uuid = getattr(props, "uuid", None)
+    sampler = ClockSampler(f"GPU-{uuid}" if uuid is not None else local)
+    sampler.start()
+    t0 = time.time()
+    n = 0
+    while n < args.warmup or time.time() - t0 < args.min_warmup_s:
+        step(n)
+        n += 1
+    torch.cuda.synchronize()
+
+    # timed region: exactly K steps, CUDA events on the launching stream
+    K = args.steps
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    lc0 = sv.launch_count()
+    e0.record(stream)
+    for k in range(K):
+        step(k)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    launches = sv.launch_count() - lc0
+    t_local = e0.elapsed_time(e1) / 1e3
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    t_max = max_over_ranks(t_local, world, dev)
+    rounds_all = sum_over_ranks(float(K), world, dev)
+    value = job_rate(rounds_all, t_max)
+
+    # statistics-kernel duration, live, with events around that kernel only
+    nprof = min(K, 200)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nprof)]
+    for a, b in evs:
+        a.record(stream)
+        b.record(stream)
+    torch.cuda.synchronize()
+    for k in range(nprof):
+        sv.profile_next_call(*evs[k])
+        step(k)
+    torch.cuda.synchronize()
+    t_stats = statistics.mean(a.elapsed_time(b) for a, b in evs) / 1e3
+    nsets = len(sets)
+    N_bytes = statistics.mean(rows_needed[k % nsets] for k in range(nprof)) * V * es
+    hbm_peak, peak_kind = peaks()
+    achieved = N_bytes / t_stats / 1e9
+    traffic = profiled_traffic()
+
+    # end to end: pinned host inputs -> device, call, results -> host, every step
+    e2e = None
+    if not args.no_e2e:
+        host = []
+        for s in sets:
+            h = {}
+            for key in ("target", "draft", "tokens", "gamma", "temperature", "uniforms"):
+                h[key] = torch.empty_like(s[key], device="cpu").pin_memory()
+                h[key].copy_(s[key])
+            host.append(h)
+        dbuf = {key: torch.empty_like(sets[0][key]) for key in host[0]}
+        hout = {key: torch.empty_like(v, device="cpu").pin_memory() for key, v in out.items()}
+        h2d = sum(v.numel() * v.element_size() for v in host[0].values())
+        d2h = sum(v.numel() * v.element_size() for v in hout.values())
+        Ke = min(K, args.e2e_steps)
+
+        def e2e_step(k):
+            h = host[k % len(host)]
+            for key in h:
+                dbuf[key].copy_(h[key], non_blocking=True)
+            r = sv.verify_sample(dbuf["target"], dbuf["draft"], dbuf["tokens"], dbuf["gamma"], dbuf["temperature"],
+                                 dbuf["uniforms"], signals=True, ws=ws, out=out)
+            for key in hout:
+                hout[key].copy_(r[key], non_blocking=True)
+            stream.synchronize()
+        for k in range(3):
+            e2e_step(k)
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for k in range(Ke):
+            e2e_step(k)
+        b.record(stream)
+        torch.cuda.synchronize()
+        te = max_over_ranks(a.elapsed_time(b) / 1e3, world, dev)
+        e2e = {"value": job_rate(sum_over_ranks(float(Ke), world, dev), te), "unit": UNIT,
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": Ke}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        cpu = cpu_baseline(sets[0]["host"], sets[0]["tokens"].cpu().numpy(), args.cpu_seconds)
+
+    if rank == 0:
+        mean_committed = statistics.mean(committed)
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
+            "ms_per_step": t_max / K * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": WORKLOAD_DESC, "B": B, "gamma": G, "V": V,
+                       "l2": f"{nsets} rotating input sets of {F_bytes/1e6:.0f} MB "
+                             f"({nsets*F_bytes/1e9:.2f} GB > 4x L2)",
+                       "parallelism": f"{world} independent request shards, no collective"},
+            "roofline": {"bound": "hbm", "kernel": "stats_kernel", "achieved": achieved, "peak": hbm_peak,
+                         "unit": "GB/s", "frac": achieved / hbm_peak, "peak_kind": peak_kind,
+                         "traffic": traffic, "algorithmic_bytes_per_launch": N_bytes,
+                         "kernel_ms": t_stats * 1e3},
+            "gpu_launches": int(launches),
+            "clocks": clocks,
+            "tokens_per_s": value * mean_committed,
+            "committed_tokens_per_round": mean_committed,
+            "hbm_gbs_step": N_bytes * value / world / 1e9,
+            "all_rows_bytes": F_bytes,
+            "needed_bytes_mean": N_bytes,
+            "rounds_per_s_at_peak_all_rows": hbm_peak * 1e9 / F_bytes,
+            "rounds_per_s_at_peak_needed_rows": hbm_peak * 1e9 / N_bytes,
+        }
+        if e2e:
+            line["e2e"] = e2e
+        if cpu:
+            line["cpu_baseline"] = cpu
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------
+# the oracle on the host cores
+
+def cpu_baseline(wl, tokens, seconds):
+    """The fp64 oracle (test infrastructure, as it stands) on full rounds of the
+    same workload, repeated on one input set for about `seconds` of wall time."""
+    import oracle
+    o = oracle.load()
+    cores = os.cpu_count() or 1
+    wl.draft_tokens = tokens.astype(np.int32)
+    t0 = time.perf_counter()
+    n = 0
+    while n < 1 or time.perf_counter() - t0 < seconds:
+        o.verify_sample(wl.target, wl.draft, wl.draft_tokens, wl.gamma, wl.temperature, wl.uniforms,
+                        want_signals=True, nthreads=cores)
+        n += 1
+    dt = time.perf_counter() - t0
+    return {"value": n / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{n} full rounds (B={wl.B} requests each) of one input set, {dt:.1f} s, "
+                      f"OpenMP over requests on {cores} threads"}
+
+
+def run_reference(args):
+    rank, world, _ = rank_env()
+    if rank != 0:
+        return
+    import oracle
+    o = oracle.load()
+    cores = os.cpu_count() or 1
+    wl = W.make(WORKLOAD, rank_round_index(0, 0))
+    B, G, V = wl.B, wl.G, wl.V
+    # draft tokens y ~ q drawn by the oracle's own categorical draw
+    rows = wl.draft.reshape(B * G, V)
+    wl.draft_tokens = o.run(oracle.SAMPLE, target=rows[:, None, :], temperature=np.repeat(wl.temperature, G),
+                            uniforms=wl.draft_aux["uniforms"].reshape(B * G, 1), G=0)["tokens"][:, 0]
+    wl.draft_tokens = wl.draft_tokens.reshape(B, G).astype(np.int32)
+
+    def sub(idx):
+        return dict(target=wl.target[idx], draft=wl.draft[idx], tok=wl.draft_tokens[idx], gamma=wl.gamma[idx],
+                    T=wl.temperature[idx], u=wl.uniforms[idx])
+
+    # size each step (a sample of n_req requests) so the whole run stays within ~2 minutes
+    one = sub(np.arange(1))
+    t0 = time.perf_counter()
+    o.verify_sample(one["target"], one["draft"], one["tok"], one["gamma"], one["T"], one["u"], want_signals=True,
+                    nthreads=1)
+    t_req = time.perf_counter() - t0                      # one request on one core
+    budget = 120.0 / max(1, args.steps + args.warmup)     # seconds per step
+    n_req = int(max(1, min(B, budget * cores / max(t_req, 1e-6))))
+    threads = min(cores, n_req)
+
+    def step(k):
+        idx = (np.arange(n_req) + k * n_req) % B
+        s = sub(idx)
+        o.verify_sample(s["target"], s["draft"], s["tok"], s["gamma"], s["T"], s["u"], want_signals=True,
+                        nthreads=threads)
+    for k in range(args.warmup):
+        step(k)
+    t0 = time.perf_counter()
+    for k in range(args.steps):
+        step(k)
+    dt = time.perf_counter() - t0
+    value = args.steps * n_req / B / dt
+    sample = f"each step: {n_req} of the {B} requests of one round (fp64, OpenMP over requests, {threads} threads)"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD_DESC, "B": B, "gamma": G, "V": V},
+            "cpu_baseline": {"kind": "oracle", "cores": threads, "sample": sample, "value": value, "unit": UNIT},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--sets", type=int, default=4, help="rotating input sets (L2 flush by footprint)")
+    ap.add_argument("--e2e-steps", type=int, default=500)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--min-warmup-s", type=float, default=0.5, help="keep warming up at least this long")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -115,6 +115,14 @@ const char* spec_request_status_string(int bit);
 /* Number of kernels this host thread has launched through the library. */
 uint64_t spec_launch_count(void);
 
+/* Profiling aid.  The next verification call made by this host thread records
+ * `begin_event` on its stream just before its statistics kernel (the kernel
+ * that streams the logits) and `end_event` just after it; the hook then
+ * clears itself.  Both are cudaEvent_t handles owned by the caller; NULL
+ * clears the hook.  The event records sit between two launches of the call,
+ * so that call's start-up overlap with the kernel before is lost. */
+int spec_profile_next_call(void* begin_event, void* end_event);
+
 /* Greedy verification (tutorial page, section 3.1).  For i = 0..gamma_b-1:
  * g_i = argmax target row i (lowest index among equal maxima); stop at the
  * first y_i != g_i with k = i and commit g_i; if none, k = gamma_b and commit

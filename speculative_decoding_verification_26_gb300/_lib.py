@@ -50,6 +50,8 @@ def lib(path: str | None = None) -> ctypes.CDLL:
         L.spec_request_status_string.restype = ctypes.c_char_p
         L.spec_launch_count.argtypes = []
         L.spec_launch_count.restype = ctypes.c_uint64
+        L.spec_profile_next_call.argtypes = [P, P]
+        L.spec_profile_next_call.restype = I
         L.spec_verify_greedy.argtypes = [P, I, I, I, I, P, P, P, P, P, P, SZ, P]
         L.spec_verify_greedy.restype = I
         L.spec_verify_sample.argtypes = [P, P, I, I, I, I, P, P, P, P, P, P, P, P, P, P, SZ, P]
@@ -77,6 +79,14 @@ def workspace_bytes(B: int, G: int, V: int) -> int:
 
 def launch_count() -> int:
     return int(lib().spec_launch_count())
+
+
+def profile_next_call(begin, end) -> None:
+    """Record torch.cuda.Event `begin`/`end` around the statistics kernel of
+    the next call made by this thread (see spec_profile_next_call)."""
+    rc = lib().spec_profile_next_call(ctypes.c_void_p(begin.cuda_event), ctypes.c_void_p(end.cuda_event))
+    if rc != OK:
+        raise SpecVerifyError(rc, "spec_profile_next_call")
 
 
 # ----------------------------------------------------------------------------

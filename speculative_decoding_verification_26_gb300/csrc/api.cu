@@ -23,6 +23,7 @@ using namespace sv;
 namespace {
 
 thread_local uint64_t g_launches = 0;
+thread_local cudaEvent_t g_prof_begin = nullptr, g_prof_end = nullptr;
 
 struct DevState {
   bool ready = false;
@@ -128,6 +129,7 @@ int run(const Call& c) {
   P.row_arr = reinterpret_cast<unsigned*>(ws + L.row_arr);
   P.row_done = reinterpret_cast<int*>(ws + L.row_done);
   P.row_stats = reinterpret_cast<RowStats*>(ws + L.row_stats);
+  P.row_xy = reinterpret_cast<float*>(ws + L.row_xy);
   P.parts = reinterpret_cast<Part*>(ws + L.parts);
   P.pair_arr = reinterpret_cast<unsigned*>(ws + L.pair_arr);
   P.pair_res = reinterpret_cast<int*>(ws + L.pair_res);
@@ -139,15 +141,19 @@ int run(const Call& c) {
   // persistent grid: two CTAs per SM, never more CTAs than work items
   const long long max_items = (long long)c.B * (2 * c.G + 1) * L.nch;
   const int grid1 = (int)(max_items < 2ll * sms ? max_items : 2ll * sms);
+  const cudaEvent_t pb = g_prof_begin, pe = g_prof_end;
+  g_prof_begin = g_prof_end = nullptr;
   cudaError_t e = launch_plan(P, c.stream);
   if (e == cudaSuccess) {
     ++g_launches;
-    e = launch_stats(P, grid1 > 0 ? grid1 : 1, c.stream, true);
+    if (pb) e = cudaEventRecord(pb, c.stream);
   }
+  if (e == cudaSuccess) e = launch_stats(P, grid1 > 0 ? grid1 : 1, c.stream, pb == nullptr);
   if (e == cudaSuccess) {
     ++g_launches;
-    e = launch_finalize(P, dim3(sample ? L.nch2 : 1, c.B), c.stream, true);
+    if (pe) e = cudaEventRecord(pe, c.stream);
   }
+  if (e == cudaSuccess) e = launch_finalize(P, dim3(sample ? L.nch2 : 1, c.B), c.stream, pe == nullptr);
   if (e == cudaSuccess) ++g_launches;
   return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
@@ -191,6 +197,12 @@ const char* spec_request_status_string(int bit) {
 }
 
 uint64_t spec_launch_count(void) { return g_launches; }
+
+int spec_profile_next_call(void* begin_event, void* end_event) {
+  g_prof_begin = static_cast<cudaEvent_t>(begin_event);
+  g_prof_end = static_cast<cudaEvent_t>(end_event);
+  return SPEC_OK;
+}
 
 int spec_verify_greedy(const void* target_logits, int dtype, int B, int G, int V, const int32_t* draft_tokens,
                        const int32_t* gamma, int32_t* accept_len, int32_t* tokens, int32_t* status,

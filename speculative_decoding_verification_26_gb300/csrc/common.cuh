@@ -32,10 +32,11 @@ constexpr int PC_UNCERTAIN = 16;   // or-ed in: |u - a| inside the guard band
 
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
-constexpr int kStatsThreads = kConsumerThreads + 64;   // + producer warp + epilogue warp
+constexpr int kEpiWarps = 2;                           // epilogue warps (items alternate)
+constexpr int kStatsThreads = kConsumerThreads + 32 * (1 + kEpiWarps);   // + producer + epilogue warps
 constexpr int kStageBytes = 16384;                      // one bulk copy
 constexpr int kStages = 6;                              // ring depth per CTA
-constexpr int kChunkBytes = 2 * kStageBytes;            // one work item of a row
+constexpr int kChunkBytes = 4 * kStageBytes;            // one work item of a row
 constexpr int kEpiSlots = 8;                            // consumer -> epilogue ring
 constexpr int kDrawChunkElems = 4096;                   // residual pass chunk
 constexpr int kDrawThreads = 256;
@@ -63,7 +64,7 @@ struct alignas(16) RowStats {
 // workspace layout (offsets in bytes, 256-aligned)
 
 struct Layout {
-  size_t hdr, req_flags, known_reject, row_list, row_arr, row_done, row_stats, parts,
+  size_t hdr, req_flags, known_reject, row_list, row_arr, row_done, row_stats, row_xy, parts,
       pair_arr, pair_res, pair_a, draw_arr, draw_parts, total;
   int nrows;      // B*(G+1) + B*G row ids
   int nch;        // stats chunks per row
@@ -96,6 +97,7 @@ __host__ inline Layout make_layout(int B, int G, int V, int dtype) {
   L.row_arr = o;      o = align256(o + sizeof(unsigned) * nrows);
   L.row_done = o;     o = align256(o + sizeof(int) * nrows);
   L.row_stats = o;    o = align256(o + sizeof(RowStats) * nrows);
+  L.row_xy = o;       o = align256(o + sizeof(float) * nrows);
   L.parts = o;        o = align256(o + sizeof(Part) * (size_t)nrows * L.nch);
   L.pair_arr = o;     o = align256(o + sizeof(unsigned) * B * (G + 1));
   L.pair_res = o;     o = align256(o + sizeof(int) * B * (G + 1));
@@ -131,6 +133,7 @@ struct Params {
   unsigned* row_arr;
   int* row_done;
   RowStats* row_stats;
+  float* row_xy;        // logit of the row at its draft token (rows i < gamma_b)
   Part* parts;
   unsigned* pair_arr;
   int* pair_res;

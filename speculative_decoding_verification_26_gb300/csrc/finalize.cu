@@ -35,32 +35,54 @@ struct Decision {
 constexpr int kVoidMask = ~(SPEC_ST_ZERO_RESIDUAL | SPEC_ST_GUARDED);
 constexpr double kDrawGuard = 1e-6;   // draws closer than this (relative to W) are counted
 
-__device__ Decision decide(const Params& P, int b) {
+// Decision of request b, taken by warp 0 of the CTA: lane i reads what
+// position i left (draft row state for the signals, the test result), so all
+// loads are issued at once; ballots then find the first reject or error in
+// position order.  The result is valid in lane 0.
+__device__ Decision decide_warp(const Params& P, int b) {
   Decision D{0, 0, 0, DK_NONE, -1};
-  const int G = P.G;
-  D.status = P.req_flags[b];
-  if (D.status) return D;
+  const int G = P.G, lane = threadIdx.x & 31;
+  const int flags = P.req_flags[b];
   const int gam = P.gamma ? P.gamma[b] : G;
+  const unsigned err = P.hdr->error;
   D.gam = gam;
-  if (P.hdr->error) { D.status = SPEC_ST_TIMEOUT; return D; }
+  if (flags) { D.status = flags; return D; }
+  if (err) { D.status = SPEC_ST_TIMEOUT; return D; }
+  const bool in = lane < gam;
+  // draft rows that feed the signals: all must be complete and finite
   if (P.signals_on) {
-    for (int i = 0; i < gam; ++i) {
-      const int rid = draft_row_id(b, i, P.B, G);
-      if (!P.row_done[rid]) { D.status = SPEC_ST_TIMEOUT; return D; }
-      if (!row_ok(P.row_stats[rid], false)) { D.status = SPEC_ST_NONFINITE; return D; }
+    int bad_missing = 0, bad_nonfinite = 0;
+    if (in) {
+      const int rid = draft_row_id(b, lane, P.B, G);
+      const int done = P.row_done[rid];
+      const RowStats r = P.row_stats[rid];
+      bad_missing = !done;
+      bad_nonfinite = done && !row_ok(r, false);
+    }
+    const unsigned mm = __ballot_sync(0xffffffffu, bad_missing), mn = __ballot_sync(0xffffffffu, bad_nonfinite);
+    if (mm | mn) {
+      // first bad draft row in order decides which error is reported
+      const int f = __ffs(mm | mn) - 1;
+      D.status = (mm >> f) & 1u ? SPEC_ST_TIMEOUT : SPEC_ST_NONFINITE;
+      return D;
     }
   }
   if (P.mode == MODE_SIGNALS) return D;
+  const int code = in ? (P.pair_res[(size_t)b * (G + 1) + lane] & 15) : PC_ACCEPT;
+  const unsigned notacc = __ballot_sync(0xffffffffu, code != PC_ACCEPT);
   int k = gam;
   bool rejected = false;
-  for (int i = 0; i < gam; ++i) {
-    const int code = P.pair_res[(size_t)b * (G + 1) + i] & 15;
-    if (code == PC_ACCEPT) continue;
-    if (code == PC_REJECT) { k = i; rejected = true; break; }
-    D.status = code == PC_NONFINITE ? SPEC_ST_NONFINITE
-             : code == PC_BAD_TOKEN ? SPEC_ST_BAD_TOKEN
-             : code == PC_BAD_UNIFORM ? SPEC_ST_BAD_UNIFORM : SPEC_ST_TIMEOUT;
-    return D;
+  if (notacc) {
+    const int f = __ffs(notacc) - 1;
+    const int cf = __shfl_sync(0xffffffffu, code, f);
+    if (cf != PC_REJECT) {
+      D.status = cf == PC_NONFINITE ? SPEC_ST_NONFINITE
+               : cf == PC_BAD_TOKEN ? SPEC_ST_BAD_TOKEN
+               : cf == PC_BAD_UNIFORM ? SPEC_ST_BAD_UNIFORM : SPEC_ST_TIMEOUT;
+      return D;
+    }
+    k = f;
+    rejected = true;
   }
   D.k = k;
   const int trow = target_row_id(b, k, G);
@@ -80,11 +102,16 @@ __device__ Decision decide(const Params& P, int b) {
 // ---------------------------------------------------------------------------
 // block helpers (256 threads)
 
+constexpr int kTile = 4096;              // rescan tile (elements)
+
 struct Scratch {
   double d[kDrawThreads / 32];
   double carry, excl, cprev, cat;
   int found, lastpos, z, last;
   float sig[kDrawThreads];
+  float w[kTile + kTile / 16];           // tile weights, one pad word per 16
+  float tw[kDrawThreads / 32][8];        // per-warp tile sums
+  double tiles[8], tiles_y[8];           // tile sums of a chunk (fp64 totals)
   double h[32], cf[32];
   Decision D;
 };
@@ -159,48 +186,130 @@ __device__ int block_locate(int n, Get get, double t, double* excl, Scratch& sh,
 }
 
 // Find the token inside row elements [e0, e1) where the running sum of
-// wf(e), started at 0, first exceeds tl.  Per-thread contiguous ranges: fp32
-// range sums locate the thread, whose fp64 walk decides.  Returns the token
-// (every thread) and the fp64 sums before/after it in *cprev / *cat.
+// wf(e), started at 0, first exceeds tl.  The range is processed in tiles of
+// kTile elements: the block evaluates the tile's weights with coalesced loads
+// into shared memory, takes fp32 sums over 16 consecutive elements per thread,
+// and an fp64 block scan of those sums (plus the fp64 sum of earlier tiles)
+// locates the thread whose range crosses tl; that thread's fp64 walk over its
+// 16 weights (continuing into the following ones if rounding requires)
+// decides.  Returns the token (every thread) and the fp64 running sums just
+// before and after it in *cprev / *cat; when rounding leaves no crossing, the
+// last element with positive weight and *cprev = *cat = the full sum.
 template <class WF>
 __device__ int block_rescan(int e0, int e1, WF wf, double tl, double* cprev, double* cat, Scratch& sh) {
-  const int n = e1 - e0;
-  const int per = (n + kDrawThreads - 1) / kDrawThreads;
-  const int a = min(e0 + (int)threadIdx.x * per, e1), bnd = min(a + per, e1);
-  float s = 0.f;
-  int lastpos = -1;
-  for (int e = a; e < bnd; ++e) {
-    const float w = wf(e);
-    s += w;
-    if (w > 0.f) lastpos = e;
-  }
-  sh.sig[threadIdx.x] = s;
+  constexpr int kPer = kTile / kDrawThreads;   // 16
+  double base = 0.0;
   if (threadIdx.x == 0) sh.last = -1;
-  __syncthreads();
-  if (lastpos >= 0) atomicMax(&sh.last, lastpos);
-  double ex;
-  const int js = block_locate(kDrawThreads, [&](int j) { return (double)sh.sig[j]; }, tl, &ex, sh);
-  if (threadIdx.x == 0) { sh.z = -1; sh.cprev = 0.0; sh.cat = 0.0; }
-  __syncthreads();
-  if (js >= 0 && (int)threadIdx.x == js) {
-    double C = ex, Cp = ex;
-    int z = -1;
-    for (int e = a; e < e1; ++e) {
-      const float w = wf(e);
-      Cp = C;
-      C += (double)w;
-      if (C > tl) { z = e; break; }
+  for (int t0 = e0; t0 < e1; t0 += kTile) {
+    const int n = min(kTile, e1 - t0);
+    int lastpos = -1;
+    for (int i = threadIdx.x; i < kTile; i += kDrawThreads) {
+      const float w = i < n ? wf(t0 + i) : 0.f;
+      sh.w[i + i / kPer] = w;                          // one pad word per 16: conflict-free rows
+      if (w > 0.f) lastpos = t0 + i;
     }
-    if (z < 0) { z = sh.last; Cp = C; }
-    sh.z = z; sh.cprev = Cp; sh.cat = C;
+    if (lastpos >= 0) atomicMax(&sh.last, lastpos);
+    __syncthreads();
+    const float* mine = sh.w + threadIdx.x * (kPer + 1);
+    float sum = 0.f;
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) sum += mine[k];
+    sh.sig[threadIdx.x] = sum;
+    double ex, tile_total;
+    const int js = block_locate(kDrawThreads, [&](int j) { return (double)sh.sig[j]; }, tl - base, &ex, sh,
+                                &tile_total);
+    // block_locate returns a crossing only when one exists; otherwise the last positive thread
+    const bool crossed = js >= 0 && base + ex + (double)sh.sig[js] > tl;
+    if (crossed) {
+      if ((int)threadIdx.x == js) {
+        double C = base + ex, Cp = C;
+        int z = -1;
+        // walk this thread's weights, then the rest of the tile, in order
+        for (int i = js * kPer; i < n; ++i) {
+          const float w = sh.w[i + i / kPer];
+          Cp = C;
+          C += (double)w;
+          if (C > tl) { z = t0 + i; break; }
+        }
+        sh.z = z; sh.cprev = Cp; sh.cat = C;
+      }
+      __syncthreads();
+      if (sh.z >= 0) {
+        const int z = sh.z;
+        *cprev = sh.cprev;
+        *cat = sh.cat;
+        __syncthreads();
+        return z;
+      }
+    }
+    // no crossing in this tile: carry its total into the next one
+    double tot = 0.0;
+    {
+      double e2;
+      block_locate(kDrawThreads, [&](int j) { return (double)sh.sig[j]; }, INFINITY, &e2, sh, &tot);
+    }
+    base += tot;
+    __syncthreads();
   }
-  __syncthreads();
-  int z = sh.z;
-  if (z < 0) z = sh.last;
-  *cprev = sh.cprev;
-  *cat = sh.cat;
+  const int z = sh.last;
+  *cprev = base;
+  *cat = base;
   __syncthreads();
   return z;
+}
+
+// Sums of wf over the kTile-element tiles of [e0, e1) (at most 8 tiles):
+// every thread takes elements e0 + tid + 256 j (coalesced, all loads in
+// flight together), fp32 per thread and tile, fp64 over the block in a fixed
+// order.  Results in out[0 .. ntiles-1] (shared), valid after return.
+template <class WF>
+__device__ int tile_sums(int e0, int e1, WF wf, double* out, Scratch& sh) {
+  constexpr int kJ = kTile / kDrawThreads;            // 16 elements per thread and tile
+  const int n = e1 - e0;
+  const int ntiles = (n + kTile - 1) / kTile;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  float acc[8];
+#pragma unroll
+  for (int t = 0; t < 8; ++t) {
+    acc[t] = 0.f;
+    if (t < ntiles) {
+#pragma unroll
+      for (int j = 0; j < kJ; ++j) {
+        const int i = (int)threadIdx.x + kDrawThreads * (t * kJ + j);
+        if (i < n) acc[t] += wf(e0 + i);
+      }
+    }
+  }
+#pragma unroll
+  for (int t = 0; t < 8; ++t) {
+    float v = acc[t];
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    if (lane == 0) sh.tw[warp][t] = v;
+  }
+  __syncthreads();
+  if (threadIdx.x < 8) {
+    double v = 0.0;
+    for (int w = 0; w < kDrawThreads / 32; ++w) v += (double)sh.tw[w][threadIdx.x];
+    out[threadIdx.x] = v;
+  }
+  __syncthreads();
+  return ntiles;
+}
+
+// First tile whose fp64 prefix exceeds tl (in order; else the last positive
+// tile), with the prefix before it.  Every thread computes the same answer.
+__device__ __forceinline__ int tile_locate(const double* tiles, int ntiles, double tl, double* before) {
+  double acc = 0.0;
+  int last = -1;
+  double last_before = 0.0;
+  for (int t = 0; t < ntiles; ++t) {
+    if (tiles[t] > 0.0) { last = t; last_before = acc; }
+    if (acc + tiles[t] > tl) { *before = acc; return t; }
+    acc += tiles[t];
+  }
+  *before = last_before;
+  return last;
 }
 
 // ---------------------------------------------------------------------------
@@ -279,14 +388,6 @@ __device__ double residual_chunk_sum(const ResidualWeight<DT>& R, int e0, int e1
   return block_sum((double)s, sh);
 }
 
-// fp32 sum of unnormalised p over one chunk without token excl (fp64 total)
-template <int DT>
-__device__ double p_chunk_sum(const PWeight<DT>& W, int e0, int e1, Scratch& sh) {
-  float s = 0.f;
-  for (int e = e0 + (int)threadIdx.x; e < e1; e += kDrawThreads) s += W(e);
-  return block_sum((double)s, sh);
-}
-
 // Draw from unnormalised p of target row `rid` (without token excl >= 0).
 // Chunk sums come from the statistics pass, except the chunk holding excl,
 // which is summed afresh.  Returns the token; sets ZERO_RESIDUAL if the mass
@@ -312,28 +413,42 @@ __device__ int draw_from_p(const Params& P, int b, int rid, int excl, float ud, 
     if (!(q.s > 0.f)) return 0.0;
     return (double)(q.s * ex2((q.m - m) * c));
   };
-  int cy = -1;
+  // the chunk holding the excluded token is summed afresh without it
+  int cy = -1, nty = 0;
   double sy = 0.0;
   if (excl >= 0) {
     cy = excl / ce;
-    sy = p_chunk_sum<DT>(W, cy * ce, min(cy * ce + ce, P.V), sh);
+    nty = tile_sums(cy * ce, min(cy * ce + ce, P.V), W, sh.tiles_y, sh);
+    for (int t = 0; t < nty; ++t) sy += sh.tiles_y[t];
   }
   auto chunk_w = [&](int j) -> double { return j == cy ? sy : part_sum(j); };
   double ex, Wt;
   block_locate(nch, chunk_w, INFINITY, &ex, sh, &Wt);
-  double excl_pref;
   if (!(Wt > 0.0)) {
     if (excl < 0) return -1;
     *st |= SPEC_ST_ZERO_RESIDUAL;
     return draw_from_p<DT>(P, b, rid, -1, ud, st, sh, n_close);
   }
   const double t = (double)ud * Wt;
+  double excl_pref;
   const int cs = block_locate(nch, chunk_w, t, &excl_pref, sh);
   if (cs < 0) return -1;
-  double cp, ca;
-  const int z = block_rescan(cs * ce, min(cs * ce + ce, P.V), W, t - excl_pref, &cp, &ca, sh);
+  // tiles of the located chunk, then the token inside the located tile
+  const int e0 = cs * ce, e1 = min(e0 + ce, P.V);
+  const double* tiles = sh.tiles_y;
+  int nt = nty;
+  if (cs != cy) {
+    nt = tile_sums(e0, e1, W, sh.tiles, sh);
+    tiles = sh.tiles;
+  }
   const double tl = t - excl_pref;
-  const double margin = fmin(tl - cp, ca - tl) / Wt;
+  double tb;
+  const int ts = tile_locate(tiles, nt, tl, &tb);
+  if (ts < 0) return -1;
+  double cp, ca;
+  const int z = block_rescan(e0 + ts * kTile, min(e0 + (ts + 1) * kTile, e1), W, tl - tb, &cp, &ca, sh);
+  const double tt = tl - tb;
+  const double margin = fmin(tt - cp, ca - tt) / Wt;
   if (threadIdx.x == 0 && !(margin >= kDrawGuard)) atomicAdd(n_close, 1u);
   return z;
 }
@@ -447,7 +562,10 @@ __global__ void __launch_bounds__(kDrawThreads) finalize_kernel(Params P) {
   __shared__ Scratch sh;
   griddep_wait();
   const int b = blockIdx.y, chunk = blockIdx.x;
-  if (threadIdx.x == 0) sh.D = decide(P, b);
+  if (threadIdx.x < 32) {
+    const Decision D = decide_warp(P, b);
+    if (threadIdx.x == 0) sh.D = D;
+  }
   __syncthreads();
   const Decision D = sh.D;
   if (D.status == 0 && D.kind == DK_RESIDUAL) {

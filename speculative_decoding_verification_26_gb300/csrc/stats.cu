@@ -34,26 +34,29 @@ struct Block {
 };
 
 // Schedule blocks in position-major order.  Full-q with signals reads every
-// draft row anyway, so the draft rows of position i are placed between the
-// target rows of positions i-1 and i: by the time target row i of a request
-// is claimed, the test at i-1 has usually been decided.
-__device__ inline int n_blocks(int mode, int signals_on, int G) {
-  if (mode == MODE_SIGNALS) return G;
-  if (mode == MODE_SAMPLE && signals_on) return G == 0 ? 1 : 2 * G;
-  return G + 1;
-}
-
-__device__ inline Block block_at(int mode, int signals_on, int G, int k) {
-  if (mode == MODE_SIGNALS) return {BT_D, k};
-  if (mode == MODE_SAMPLE && signals_on) {
-    if (G == 0) return {BT_T, 0};
-    if (k == 0) return {BT_PAIR, 0};
-    if (k == 2 * G - 1) return {BT_T, G};
-    const int i = (k + 1) / 2;
-    return {(k & 1) ? BT_D : BT_T, i};
+// draft row anyway, so draft blocks are used as filler between target
+// positions: PAIR(0) | D1 D2 | T1 | D3 D4 | T2 | ... | T_G.  Between the
+// target rows of positions i-1 and i there are then about 2B rows of other
+// work, longer than the reading window of the whole GPU, so the test at i-1
+// is usually decided before target row i of the request is claimed.  Draft
+// block j always precedes target block j, as the test at j needs both.
+__device__ inline int build_blocks(int mode, int signals_on, int G, Block* out) {
+  int n = 0;
+  if (mode == MODE_SIGNALS) {
+    for (int i = 0; i < G; ++i) out[n++] = {BT_D, i};
+  } else if (mode == MODE_SAMPLE && signals_on && G > 0) {
+    out[n++] = {BT_PAIR, 0};
+    int dnext = 1;
+    for (int i = 1; i <= G; ++i) {
+      for (int f = 0; f < 2 && dnext <= G - 1; ++f) out[n++] = {BT_D, dnext++};
+      out[n++] = {BT_T, i};
+    }
+  } else if (mode == MODE_SAMPLE) {
+    for (int i = 0; i <= G; ++i) out[n++] = {BT_PAIR, i};
+  } else {
+    for (int i = 0; i <= G; ++i) out[n++] = {BT_T, i};
   }
-  if (mode == MODE_SAMPLE) return {BT_PAIR, k};
-  return {BT_T, k};
+  return n;
 }
 
 __device__ inline int rows_for(const Block& bl, int gam) {
@@ -72,6 +75,8 @@ __global__ void __launch_bounds__(1024) plan_kernel(Params P) {
   const int lane = tid & 31, warp = tid >> 5, nwarps = nth >> 5;
   __shared__ int s_count[64];
   __shared__ int s_off[65];
+  __shared__ Block s_blk[64];
+  __shared__ int s_nb;
 
   for (int j = tid; j < P.nrows; j += nth) {
     P.row_arr[j] = 0u;
@@ -91,12 +96,13 @@ __global__ void __launch_bounds__(1024) plan_kernel(Params P) {
     if (P.mode != MODE_GREEDY && !temperature_ok(P.temperature[b])) st |= SPEC_ST_BAD_TEMPERATURE;
     P.req_flags[b] = st;
   }
-  __syncthreads();   // req_flags visible to the whole block
+  if (tid == 0) s_nb = build_blocks(P.mode, P.signals_on, G, s_blk);
+  __syncthreads();   // req_flags and the block table visible to the whole block
 
-  const int nb = n_blocks(P.mode, P.signals_on, G);
+  const int nb = s_nb;
   // rows per block
   for (int k = warp; k < nb; k += nwarps) {
-    const Block bl = block_at(P.mode, P.signals_on, G, k);
+    const Block bl = s_blk[k];
     int cnt = 0;
     for (int b0 = 0; b0 < B; b0 += 32) {
       const int b = b0 + lane;
@@ -119,7 +125,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(Params P) {
   __syncthreads();
   // write the compacted row ids
   for (int k = warp; k < nb; k += nwarps) {
-    const Block bl = block_at(P.mode, P.signals_on, G, k);
+    const Block bl = s_blk[k];
     int off = s_off[k];
     for (int b0 = 0; b0 < B; b0 += 32) {
       const int b = b0 + lane;
@@ -158,12 +164,15 @@ struct StageDesc {
   int chunk, elem0, nvec, flags;
   int head0, nhead, tail0, ntail;
   float c;
-  int pad[3];
+  int y;          // draft token whose logit the test needs (-1: none)
+  int pad[2];
 };
 
 struct EpiSlot {
   int row_id, b, i, kind;
-  int chunk, term, pad[2];
+  int chunk, term;
+  float xy;       // logit at the draft token if this item held it, else NaN
+  int pad;
   Part part[kConsumerWarps];
 };
 
@@ -228,12 +237,78 @@ __device__ __forceinline__ void run_reset(RunState& r) {
   r.m = -INFINITY; r.s = 0.f; r.t = 0.f; r.mc = 0.f; r.idx = 0x3fffffff; r.nan = 0;
 }
 
-// softmax statistics over one vector of N logits
-template <int N, bool ENT>
-__device__ __forceinline__ void run_softmax(RunState& r, const float* x, float c) {
-  float vm = x[0];
+// ---- per-stage processing ---------------------------------------------------
+// Each consumer thread owns 4 of the stage's 1024 16-byte vectors (strided by
+// 256, so every shared load of a warp is one contiguous 512-byte run).  The
+// stage max is taken first with a max tree (one running-max update per stage,
+// not per vector), then the 32 (bf16) or 16 (fp32) terms are independent, so
+// their exp2 and adds pipeline.  Vectors past the staged bytes read as -inf.
+
+constexpr int kVecPerThread = kStageBytes / 16 / kConsumerThreads;   // 4
+
+__device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {       // NaN-ignoring
+  uint32_t d;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t bmax2_nan(uint32_t a, uint32_t b) {   // NaN-propagating
+  uint32_t d;
+  asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+template <int DT>
+__device__ __forceinline__ void load_stage(const uint4* vec, int nvec, int tid, uint4 (&w)[kVecPerThread]) {
+  const uint32_t ninf = DT == SPEC_BF16 ? 0xff80ff80u : 0xff800000u;
 #pragma unroll
-  for (int e = 1; e < N; ++e) vm = fmaxf(vm, x[e]);
+  for (int r = 0; r < kVecPerThread; ++r) {
+    const int v = tid + r * kConsumerThreads;
+    w[r] = v < nvec ? vec[v] : make_uint4(ninf, ninf, ninf, ninf);
+  }
+}
+
+// max over the thread's stage elements (NaN ignored or propagated)
+template <int DT, bool NANP>
+__device__ __forceinline__ float stage_max(const uint4 (&w)[kVecPerThread]) {
+  if (DT == SPEC_BF16) {
+    uint32_t h[2 * kVecPerThread];
+#pragma unroll
+    for (int r = 0; r < kVecPerThread; ++r) {
+      h[2 * r] = NANP ? bmax2_nan(w[r].x, w[r].y) : bmax2(w[r].x, w[r].y);
+      h[2 * r + 1] = NANP ? bmax2_nan(w[r].z, w[r].w) : bmax2(w[r].z, w[r].w);
+    }
+#pragma unroll
+    for (int n = 2 * kVecPerThread; n > 1; n >>= 1)
+#pragma unroll
+      for (int k = 0; k < n / 2; ++k) h[k] = NANP ? bmax2_nan(h[2 * k], h[2 * k + 1]) : bmax2(h[2 * k], h[2 * k + 1]);
+    const float lo = bf16_lo(h[0]), hi = bf16_hi(h[0]);
+    if (NANP && (lo != lo || hi != hi)) return __int_as_float(0x7fc00000);
+    return fmaxf(lo, hi);
+  } else {
+    float f[4 * kVecPerThread];
+#pragma unroll
+    for (int r = 0; r < kVecPerThread; ++r) {
+      f[4 * r] = __uint_as_float(w[r].x); f[4 * r + 1] = __uint_as_float(w[r].y);
+      f[4 * r + 2] = __uint_as_float(w[r].z); f[4 * r + 3] = __uint_as_float(w[r].w);
+    }
+    bool nan = false;
+    if (NANP) {
+#pragma unroll
+      for (int k = 0; k < 4 * kVecPerThread; ++k) nan |= f[k] != f[k];
+    }
+#pragma unroll
+    for (int n = 4 * kVecPerThread; n > 1; n >>= 1)
+#pragma unroll
+      for (int k = 0; k < n / 2; ++k) f[k] = fmaxf(f[2 * k], f[2 * k + 1]);
+    return nan ? __int_as_float(0x7fc00000) : f[0];
+  }
+}
+
+template <int DT, bool ENT>
+__device__ __forceinline__ void stage_softmax(RunState& r, const uint4 (&w)[kVecPerThread], float c) {
+  using Vec = VecT<DT>;
+  constexpr int N = Vec::N;
+  const float vm = stage_max<DT, false>(w);
   if (vm > r.m) {
     if (r.m != -INFINITY) {
       const float d = (r.m - vm) * c;
@@ -244,43 +319,49 @@ __device__ __forceinline__ void run_softmax(RunState& r, const float* x, float c
     r.m = vm;
     r.mc = vm * c;
   }
-  float e[N], a[N];
+  const float mc = r.mc;
+  float sv[kVecPerThread], tv[kVecPerThread];
 #pragma unroll
-  for (int k = 0; k < N; ++k) {
-    a[k] = fmaf(x[k], c, -r.mc);
-    e[k] = ex2(a[k]);
-  }
-  // pairwise sum of the vector, then into the running sum
-  float s;
-  if (N == 8) s = ((e[0] + e[1]) + (e[2] + e[3])) + ((e[4] + e[5]) + (e[6] + e[7]));
-  else s = (e[0] + e[1]) + (e[2] + e[3]);
-  r.s += s;
-  if (ENT) {
-    float t = 0.f;
+  for (int q = 0; q < kVecPerThread; ++q) {
+    float x[N], e[N];
+    Vec::unpack(w[q], x);
 #pragma unroll
-    for (int k = 0; k < N; ++k) t = fmaf(fmaxf(a[k], -256.f), e[k], t);
-    r.t += t;
+    for (int k = 0; k < N; ++k) {
+      const float a = fmaf(x[k], c, -mc);
+      e[k] = ex2(a);
+      if (ENT) x[k] = fmaxf(a, -256.f);       // reuse x for the clamped exponent
+    }
+    if (N == 8) sv[q] = ((e[0] + e[1]) + (e[2] + e[3])) + ((e[4] + e[5]) + (e[6] + e[7]));
+    else sv[q] = (e[0] + e[1]) + (e[2] + e[3]);
+    if (ENT) {
+      float t = 0.f;
+#pragma unroll
+      for (int k = 0; k < N; ++k) t = fmaf(x[k], e[k], t);
+      tv[q] = t;
+    }
   }
+  r.s += (sv[0] + sv[1]) + (sv[2] + sv[3]);
+  if (ENT) r.t += (tv[0] + tv[1]) + (tv[2] + tv[3]);
 }
 
-// argmax over one vector (lowest index among equal maxima), NaN noted
-template <int N>
-__device__ __forceinline__ void run_argmax(RunState& r, const float* x, int e0) {
-  float vm = x[0];
-  int nan = x[0] != x[0];
-#pragma unroll
-  for (int e = 1; e < N; ++e) {
-    vm = fmaxf(vm, x[e]);
-    nan |= x[e] != x[e];
-  }
-  r.nan |= nan;
+template <int DT>
+__device__ __forceinline__ void stage_argmax(RunState& r, const uint4 (&w)[kVecPerThread], int elem0, int tid) {
+  using Vec = VecT<DT>;
+  constexpr int N = Vec::N;
+  const float vm = stage_max<DT, true>(w);
+  if (vm != vm) { r.nan = 1; return; }
   if (vm > r.m) {
-    int j = N - 1;
+    int idx = 0x3fffffff;
 #pragma unroll
-    for (int e = N - 1; e >= 0; --e)
-      if (x[e] == vm) j = e;
+    for (int q = kVecPerThread - 1; q >= 0; --q) {
+      float x[N];
+      Vec::unpack(w[q], x);
+#pragma unroll
+      for (int k = N - 1; k >= 0; --k)
+        if (x[k] == vm) idx = elem0 + (tid + q * kConsumerThreads) * N + k;
+    }
     r.m = vm;
-    r.idx = e0 + j;
+    r.idx = idx;
   }
 }
 
@@ -317,39 +398,61 @@ __device__ __forceinline__ Part to_part(const RunState& r) {
 
 // ---- producer --------------------------------------------------------------
 
+// What the producer needs to stage one claimed item.
+struct ItemMeta {
+  unsigned q;
+  int rid, b, i, kind, chunk, y;
+  bool valid, skip;
+  float c;
+};
+
+template <bool GREEDY>
+__device__ __forceinline__ ItemMeta fetch_meta(const Params& P, unsigned q, unsigned n_items) {
+  ItemMeta m;
+  m.q = q;
+  m.valid = q < n_items;
+  m.skip = false;
+  m.y = -1;
+  m.c = 0.f;
+  m.rid = m.b = m.i = m.kind = m.chunk = 0;
+  if (!m.valid) return m;
+  const int nch = P.nch, G = P.G;
+  const int slot = (int)(q / (unsigned)nch);
+  m.chunk = (int)(q - (unsigned)slot * nch);
+  m.rid = __ldg(P.row_list + slot);
+  decode_row(m.rid, P.B, G, m.kind, m.b, m.i);
+  const int b = m.b, i = m.i;
+  // independent loads, issued together
+  const int kr = (m.kind == KIND_TARGET || !P.signals_on) ? ld_relaxed(P.known_reject + b) : kNoReject;
+  const float T = GREEDY ? 1.f : P.temperature[b];
+  const int gam = P.gamma ? P.gamma[b] : G;
+  int y = -1;
+  // the draft token (sample / one-hot only: signals-only calls have no tokens)
+  if (!GREEDY && P.mode != MODE_SIGNALS && i < gam) y = P.draft_tokens[(size_t)b * G + i];
+  m.skip = kr < i;             // a reject at an earlier position voids this row
+  m.c = GREEDY ? 0.f : scale_of(T);
+  m.y = y;
+  return m;
+}
+
 template <int DT, bool GREEDY>
 __device__ void producer_role(const Params& P, StatsSmem& S) {
   constexpr int ES = DT == SPEC_BF16 ? 2 : 4;
-  const int B = P.B, G = P.G, V = P.V, nch = P.nch;
+  const int G = P.G, V = P.V;
   const int ce = chunk_elems(DT);
   const unsigned n_items = P.hdr->n_items;
   int stage = 0;
   uint32_t phase = 0;
   bool ok = true;
-  unsigned next = atomicAdd(&P.hdr->queue, 2u);
-  while (ok) {
-    const unsigned base = next;
-    if (base >= n_items) break;
-    next = atomicAdd(&P.hdr->queue, 2u);
-    for (int j = 0; j < 2 && ok; ++j) {
-      const unsigned q = base + j;
-      if (q >= n_items) break;
-      const int slot = (int)(q / (unsigned)nch);
-      const int chunk = (int)(q - (unsigned)slot * nch);
-      const int rid = __ldg(P.row_list + slot);
-      int kind, b, i;
-      decode_row(rid, B, G, kind, b, i);
-      if (kind == KIND_TARGET || !P.signals_on) {
-        const int kr = ld_relaxed(P.known_reject + b);
-        if (kr < i) {            // a reject at an earlier position voids this row
-          red_add_release(P.row_arr + rid, 1u + kSkipInc);
-          continue;
-        }
-      }
-      const float c = GREEDY ? 0.f : scale_of(P.temperature[b]);
-      const unsigned char* tens = kind == KIND_TARGET ? P.target : P.draft;
-      const long long row0 = row_elem_offset(kind, b, i, G, V);
-      const int e_begin = chunk * ce;
+  ItemMeta cur = fetch_meta<GREEDY>(P, atomicAdd(&P.hdr->queue, 1u), n_items);
+  while (ok && cur.valid) {
+    const unsigned qn = atomicAdd(&P.hdr->queue, 1u);   // next claim, in flight while staging
+    if (cur.skip) {
+      red_add_release(P.row_arr + cur.rid, 1u + kSkipInc);
+    } else {
+      const unsigned char* tens = cur.kind == KIND_TARGET ? P.target : P.draft;
+      const long long row0 = row_elem_offset(cur.kind, cur.b, cur.i, G, V);
+      const int e_begin = cur.chunk * ce;
       const int e_end = min(e_begin + ce, V);
       const uintptr_t rowaddr = reinterpret_cast<uintptr_t>(tens) + (uintptr_t)(row0 * ES);
       const uintptr_t a_start = rowaddr + (uintptr_t)e_begin * ES;
@@ -372,14 +475,15 @@ __device__ void producer_role(const Params& P, StatsSmem& S) {
         const long long off = (long long)p * kStageBytes;
         const uint32_t bytes = mid > 0 ? (uint32_t)(mid - off < kStageBytes ? mid - off : kStageBytes) : 0u;
         StageDesc& d = S.desc[stage];
-        d.row_id = rid; d.b = b; d.i = i; d.kind = kind;
-        d.chunk = chunk;
+        d.row_id = cur.rid; d.b = cur.b; d.i = cur.i; d.kind = cur.kind;
+        d.chunk = cur.chunk;
         d.elem0 = (int)((A0 + (uintptr_t)off - rowaddr) / ES);
         d.nvec = (int)(bytes / 16);
         d.flags = (p == 0 ? F_FIRST : 0) | (p == npieces - 1 ? F_LAST : 0);
         d.head0 = e_begin; d.nhead = nhead;
         d.tail0 = e_end - ntail; d.ntail = ntail;
-        d.c = c;
+        d.c = cur.c;
+        d.y = cur.y;
         if (bytes > 0) {
           mbar_arrive_expect_tx(&S.full[stage], bytes);
           bulk_load(S.ring[stage], reinterpret_cast<const void*>(A0 + (uintptr_t)off), bytes, &S.full[stage]);
@@ -389,6 +493,7 @@ __device__ void producer_role(const Params& P, StatsSmem& S) {
         if (++stage == kStages) { stage = 0; phase ^= 1u; }
       }
     }
+    cur = fetch_meta<GREEDY>(P, qn, n_items);
   }
   if (ok && wait_bar(S, &S.empty[stage], phase ^ 1u)) {
     S.desc[stage].flags = F_TERM;
@@ -410,8 +515,7 @@ __device__ void producer_role(const Params& P, StatsSmem& S) {
 
 template <int DT, bool GREEDY>
 __device__ void consumer_role(const Params& P, StatsSmem& S, int cw, int lane) {
-  using Vec = VecT<DT>;
-  constexpr int N = Vec::N;
+  constexpr int N = VecT<DT>::N;
   const int tid = cw * 32 + lane;
   int stage = 0;
   uint32_t phase = 0;
@@ -419,58 +523,58 @@ __device__ void consumer_role(const Params& P, StatsSmem& S, int cw, int lane) {
   RunState r;
   run_reset(r);
   bool ent = false;
-  float c = 0.f;
+  float c = 0.f, xy = __int_as_float(0x7fc00000);
   while (true) {
     if (!wait_bar(S, &S.full[stage], phase)) { set_abort(P, S); return; }
     const StageDesc d = S.desc[stage];
-    const int eslot = seq % kEpiSlots;
-    const uint32_t epar = ((uint32_t)(seq / kEpiSlots) & 1u) ^ 1u;
     if (d.flags & F_TERM) {
-      if (!wait_bar(S, &S.epi_empty[eslot], epar)) { set_abort(P, S); return; }
-      if (tid == 0) S.slot[eslot].term = 1;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&S.epi_full[eslot]);
+      // both epilogue warps must see the end: mark two consecutive slots
+      for (int e = 0; e < kEpiWarps; ++e) {
+        const int es = (seq + e) % kEpiSlots;
+        const uint32_t ep = ((uint32_t)((seq + e) / kEpiSlots) & 1u) ^ 1u;
+        if (!wait_bar(S, &S.epi_empty[es], ep)) { set_abort(P, S); return; }
+        if (tid == 0) S.slot[es].term = 1;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.epi_full[es]);
+      }
       return;
     }
     if (d.flags & F_FIRST) {
       run_reset(r);
       ent = !GREEDY && d.kind == KIND_DRAFT && P.signals_on;
       c = d.c;
+      xy = __int_as_float(0x7fc00000);
     }
     const uint4* vec = reinterpret_cast<const uint4*>(S.ring[stage]);
-    const int nvec = d.nvec;
-    if (GREEDY) {
-#pragma unroll 4
-      for (int v = tid; v < nvec; v += kConsumerThreads) {
-        float x[N];
-        Vec::unpack(vec[v], x);
-        run_argmax<N>(r, x, d.elem0 + v * N);
-      }
-    } else if (ent) {
-#pragma unroll 4
-      for (int v = tid; v < nvec; v += kConsumerThreads) {
-        float x[N];
-        Vec::unpack(vec[v], x);
-        run_softmax<N, true>(r, x, c);
-      }
-    } else {
-#pragma unroll 4
-      for (int v = tid; v < nvec; v += kConsumerThreads) {
-        float x[N];
-        Vec::unpack(vec[v], x);
-        run_softmax<N, false>(r, x, c);
+    uint4 w[kVecPerThread];
+    load_stage<DT>(vec, d.nvec, tid, w);
+    // the logit at the draft token, if this stage holds it (one shared load)
+    if (!GREEDY && tid == 0) {
+      const int off = d.y - d.elem0;
+      if (off >= 0 && off < d.nvec * N) {
+        xy = DT == SPEC_BF16 ? __uint_as_float((uint32_t)reinterpret_cast<const unsigned short*>(vec)[off] << 16)
+                             : reinterpret_cast<const float*>(vec)[off];
       }
     }
+    if (GREEDY) stage_argmax<DT>(r, w, d.elem0, tid);
+    else if (ent) stage_softmax<DT, true>(r, w, c);
+    else stage_softmax<DT, false>(r, w, c);
     __syncwarp();
     if (lane == 0) mbar_arrive(&S.empty[stage]);
     if (d.flags & F_LAST) {
       if (tid == 0 && (d.nhead > 0 || d.ntail > 0)) {
         const unsigned char* tens = d.kind == KIND_TARGET ? P.target : P.draft;
         const long long row0 = row_elem_offset(d.kind, d.b, d.i, P.G, P.V);
-        for (int k = 0; k < d.nhead; ++k)
-          run_scalar<GREEDY>(r, load_logit(tens, DT, row0 + d.head0 + k), d.head0 + k, c, ent);
-        for (int k = 0; k < d.ntail; ++k)
-          run_scalar<GREEDY>(r, load_logit(tens, DT, row0 + d.tail0 + k), d.tail0 + k, c, ent);
+        for (int k = 0; k < d.nhead; ++k) {
+          const float x = load_logit(tens, DT, row0 + d.head0 + k);
+          if (d.head0 + k == d.y) xy = x;
+          run_scalar<GREEDY>(r, x, d.head0 + k, c, ent);
+        }
+        for (int k = 0; k < d.ntail; ++k) {
+          const float x = load_logit(tens, DT, row0 + d.tail0 + k);
+          if (d.tail0 + k == d.y) xy = x;
+          run_scalar<GREEDY>(r, x, d.tail0 + k, c, ent);
+        }
       }
       Part p = to_part(r);
 #pragma unroll
@@ -478,12 +582,15 @@ __device__ void consumer_role(const Params& P, StatsSmem& S, int cw, int lane) {
         const Part o = shfl_part(p, off);
         p = GREEDY ? merge_argmax(p, o) : merge_parts(p, o, c, ent);
       }
+      const int eslot = seq % kEpiSlots;
+      const uint32_t epar = ((uint32_t)(seq / kEpiSlots) & 1u) ^ 1u;
       if (!wait_bar(S, &S.epi_empty[eslot], epar)) { set_abort(P, S); return; }
       if (lane == 0) {
         S.slot[eslot].part[cw] = p;
         if (cw == 0) {
           EpiSlot& E = S.slot[eslot];
           E.row_id = d.row_id; E.b = d.b; E.i = d.i; E.kind = d.kind; E.chunk = d.chunk;
+          E.xy = xy;
         }
       }
       __syncwarp();
@@ -496,68 +603,68 @@ __device__ void consumer_role(const Params& P, StatsSmem& S, int cw, int lane) {
 
 // ---- epilogue --------------------------------------------------------------
 
-// Acceptance test of position i of request b; both rows are complete.
+// Acceptance test of position i of request b, both rows complete (tutorial
+// page, sections 3.1-3.3).  fp32 on the fp32 row statistics:
+//   p(y) = 2^{(x_y - m_p) c} / s_p,  q(y) likewise (1 for one-hot q),
+//   accept <=> u q(y) < p(y),  a = min(1, p(y)/q(y)).
+// A test closer than 1e-5 (relative) to its threshold is marked and does not
+// stop the reading of later rows.
 template <bool GREEDY>
 __device__ void evaluate_position(const Params& P, int b, int i) {
   const int G = P.G, V = P.V;
-  const RowStats tr = ldcg_stats(P.row_stats + target_row_id(b, i, G));
-  int code;
-  double a = __longlong_as_double(0x7ff8000000000000ll);
+  const int tid_t = target_row_id(b, i, G);
+  const RowStats tr = ldcg_stats(P.row_stats + tid_t);
   const int y = P.draft_tokens[(size_t)b * G + i];
+  int code;
+  float a = __int_as_float(0x7fc00000);
   if (GREEDY) {
     if (!row_ok(tr, true)) code = PC_NONFINITE;
     else if (y < 0 || y >= V) code = PC_BAD_TOKEN;
     else code = (y == (tr.idx & ~kIdxNaN)) ? PC_ACCEPT : PC_REJECT;
   } else {
+    const bool sample = P.mode == MODE_SAMPLE;
+    const int did = draft_row_id(b, i, P.B, G);
+    const float u = P.uniforms[(size_t)b * (G + 1) + i];
+    const float c = scale_of(P.temperature[b]);
+    const float xt = __ldcg(P.row_xy + tid_t);
     RowStats dr{};
-    bool ok = row_ok(tr, false);
-    if (ok && P.mode == MODE_SAMPLE) {
-      dr = ldcg_stats(P.row_stats + draft_row_id(b, i, P.B, G));
-      ok = row_ok(dr, false);
+    float xd = 0.f;
+    if (sample) {
+      dr = ldcg_stats(P.row_stats + did);
+      xd = __ldcg(P.row_xy + did);
     }
-    if (!ok) code = PC_NONFINITE;
+    if (!row_ok(tr, false) || (sample && !row_ok(dr, false))) code = PC_NONFINITE;
     else if (y < 0 || y >= V) code = PC_BAD_TOKEN;
+    else if (!(u >= 0.f && u < 1.f)) code = PC_BAD_UNIFORM;
     else {
-      const float u = P.uniforms[(size_t)b * (G + 1) + i];
-      if (!(u >= 0.f && u < 1.f)) code = PC_BAD_UNIFORM;
-      else {
-        const double c = (double)scale_of(P.temperature[b]);
-        const float xt = load_logit(P.target, P.dtype, row_elem_offset(KIND_TARGET, b, i, G, V) + y);
-        const double py = exp2(((double)xt - (double)tr.m) * c) / (double)tr.s;
-        double qy = 1.0;
-        if (P.mode == MODE_SAMPLE) {
-          const float xd = load_logit(P.draft, P.dtype, row_elem_offset(KIND_DRAFT, b, i, G, V) + y);
-          qy = exp2(((double)xd - (double)dr.m) * c) / (double)dr.s;
-        }
-        const double uq = (double)u * qy;
-        const bool accept = uq < py;
-        a = qy > 0.0 ? fmin(1.0, py / qy) : (py > 0.0 ? 1.0 : 0.0);
-        code = accept ? PC_ACCEPT : PC_REJECT;
-        // fp32 row sums carry a relative error far below 1e-5; closer calls
-        // are marked (diagnostic) and do not stop the reading of later rows
-        if (fabs(uq - py) <= 1e-5 * fmax(uq, py)) {
-          code |= PC_UNCERTAIN;
-          atomicAdd(&P.hdr->n_uncertain, 1u);
-        }
+      const float py = ex2((xt - tr.m) * c) / tr.s;
+      const float qy = sample ? ex2((xd - dr.m) * c) / dr.s : 1.f;
+      const float uq = u * qy;
+      code = uq < py ? PC_ACCEPT : PC_REJECT;
+      a = qy > 0.f ? fminf(1.f, py / qy) : (py > 0.f ? 1.f : 0.f);
+      if (fabsf(uq - py) <= 1e-5f * fmaxf(uq, py)) {
+        code |= PC_UNCERTAIN;
+        atomicAdd(&P.hdr->n_uncertain, 1u);
       }
     }
   }
   __stcg(P.pair_res + (size_t)b * (G + 1) + i, code);
-  __stcg(P.pair_a + (size_t)b * (G + 1) + i, a);
+  __stcg(P.pair_a + (size_t)b * (G + 1) + i, (double)a);
   if (code != PC_ACCEPT && !(code & PC_UNCERTAIN)) atomicMin(P.known_reject + b, i);
 }
 
+// Epilogue warp e handles the items with sequence number = e (mod kEpiWarps).
 template <bool GREEDY>
-__device__ void epilogue_role(const Params& P, StatsSmem& S, int lane) {
+__device__ void epilogue_role(const Params& P, StatsSmem& S, int lane, int e) {
   const int G = P.G, nch = P.nch;
-  int seq = 0;
-  while (true) {
+  for (int seq = e;; seq += kEpiWarps) {
     const int eslot = seq % kEpiSlots;
     const uint32_t epar = (uint32_t)(seq / kEpiSlots) & 1u;
     if (!wait_bar(S, &S.epi_full[eslot], epar)) { set_abort(P, S); return; }
     const EpiSlot& E = S.slot[eslot];
     if (E.term) return;
     const int rid = E.row_id, b = E.b, i = E.i, kind = E.kind, chunk = E.chunk;
+    const float xy = E.xy;
     Part p = lane < kConsumerWarps ? E.part[lane] : empty_part();
     __syncwarp();
     if (lane == 0) mbar_arrive(&S.epi_empty[eslot]);
@@ -571,7 +678,8 @@ __device__ void epilogue_role(const Params& P, StatsSmem& S, int lane) {
     unsigned old = 0;
     if (lane == 0) {
       stcg_part(P.parts + (size_t)rid * nch + chunk, p);
-      old = atom_add_acqrel(P.row_arr + rid, 1u);
+      if (!(xy != xy)) __stcg(P.row_xy + rid, xy);
+      old = atom_add_acqrel(P.row_arr + rid, 1u);   // release: the partial before the count
     }
     old = __shfl_sync(0xffffffffu, old, 0);
     if (((old + 1u) & kCountMask) == (unsigned)nch && (old >> 20) == 0u) {
@@ -602,7 +710,6 @@ __device__ void epilogue_role(const Params& P, StatsSmem& S, int lane) {
         }
       }
     }
-    ++seq;
   }
 }
 
@@ -631,7 +738,7 @@ __global__ void __launch_bounds__(kStatsThreads, 2) stats_kernel(Params P) {
   if (warp < kConsumerWarps) consumer_role<DT, GREEDY>(P, S, warp, lane);
   else if (warp == kConsumerWarps) {
     if (lane == 0) producer_role<DT, GREEDY>(P, S);
-  } else epilogue_role<GREEDY>(P, S, lane);
+  } else epilogue_role<GREEDY>(P, S, lane, warp - kConsumerWarps - 1);
   griddep_launch();
 }
 
