@@ -1,16 +1,16 @@
 // api.cu -- the C ABI declared in include/spec_verify.h.
 //
-// Host side only: argument checks, workspace layout, and the three launches
-// of one call on the caller's stream:
-//   plan_kernel      (1 CTA)        resets counters, builds the row schedule;
-//   stats_kernel     (persistent)   streams the needed logit rows, decides
-//                                   each position as soon as its rows are in;
-//   finalize_kernel  (per request)  first reject, final draw, outputs.
-// The second and third launches use programmatic dependent launch so their
-// start-up overlaps the tail of the kernel before; each waits on
-// griddepcontrol.wait before reading what the previous kernel wrote.  The
-// plan kernel is launched without it, so it starts only after all earlier
-// work on the stream (which may be producing this call's inputs).
+// Host side only: argument checks, workspace layout, and the two launches of
+// one call on the caller's stream:
+//   plan_kernel    (1 CTA)        resets counters, settles requests with bad
+//                                 arguments, builds the row schedule;
+//   verify_kernel  (persistent)   streams the needed logit rows, decides each
+//                                 position as soon as its rows are in, and
+//                                 runs each request's final draw.
+// The second launch uses programmatic dependent launch, so its start-up
+// overlaps the plan kernel; it waits on griddepcontrol.wait before reading
+// the schedule.  The plan kernel is launched without it, so it starts only
+// after all earlier work on the stream (which may be producing the inputs).
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -49,7 +49,7 @@ int device_state(int* sms) {
     if (major != 10 || minor != 3) {
       d.status = SPEC_ERR_UNSUPPORTED;   // the library carries sm_103a code only
     } else {
-      const cudaError_t e = configure_stats_kernels();
+      const cudaError_t e = configure_kernels();
       if (e != cudaSuccess) return SPEC_ERR_CUDA;
       d.status = SPEC_OK;
     }
@@ -133,10 +133,19 @@ int run(const Call& c) {
   P.parts = reinterpret_cast<Part*>(ws + L.parts);
   P.pair_arr = reinterpret_cast<unsigned*>(ws + L.pair_arr);
   P.pair_res = reinterpret_cast<int*>(ws + L.pair_res);
-  P.pair_a = reinterpret_cast<double*>(ws + L.pair_a);
-  P.draw_arr = reinterpret_cast<unsigned*>(ws + L.draw_arr);
-  P.draw_parts = reinterpret_cast<double*>(ws + L.draw_parts);
-  P.nrows = L.nrows; P.nch = L.nch; P.nch2 = L.nch2;
+  P.pair_a = reinterpret_cast<float*>(ws + L.pair_a);
+  P.req_state = reinterpret_cast<unsigned long long*>(ws + L.req_state);
+  P.req_cnt = reinterpret_cast<unsigned*>(ws + L.req_cnt);
+  P.req_k = reinterpret_cast<int*>(ws + L.req_k);
+  P.req_status = reinterpret_cast<int*>(ws + L.req_status);
+  P.req_z = reinterpret_cast<int*>(ws + L.req_z);
+  P.rsum_arr = reinterpret_cast<unsigned*>(ws + L.rsum_arr);
+  P.rsum_parts = reinterpret_cast<double*>(ws + L.rsum_parts);
+  P.rsum_gs = reinterpret_cast<float*>(ws + L.rsum_gs);
+  P.search = reinterpret_cast<SearchDesc*>(ws + L.search);
+  P.dq = reinterpret_cast<DynItem*>(ws + L.dq);
+  P.nrows = L.nrows; P.nch = L.nch; P.nres = L.nres; P.dq_cap = L.dq_cap;
+  P.aligned_rows = ((size_t)c.V * es) % 16 == 0 && aligned(c.target, 16) && aligned(c.draft, 16);
 
   // persistent grid: two CTAs per SM, never more CTAs than work items
   const long long max_items = (long long)c.B * (2 * c.G + 1) * L.nch;
@@ -148,13 +157,11 @@ int run(const Call& c) {
     ++g_launches;
     if (pb) e = cudaEventRecord(pb, c.stream);
   }
-  if (e == cudaSuccess) e = launch_stats(P, grid1 > 0 ? grid1 : 1, c.stream, pb == nullptr);
+  if (e == cudaSuccess) e = launch_verify(P, grid1 > 0 ? grid1 : 1, c.stream, pb == nullptr);
   if (e == cudaSuccess) {
     ++g_launches;
     if (pe) e = cudaEventRecord(pe, c.stream);
   }
-  if (e == cudaSuccess) e = launch_finalize(P, dim3(sample ? L.nch2 : 1, c.B), c.stream, pe == nullptr);
-  if (e == cudaSuccess) ++g_launches;
   return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 

@@ -27,6 +27,21 @@ enum PairCode : int {
 };
 constexpr int PC_UNCERTAIN = 16;   // or-ed in: |u - a| inside the guard band
 
+// work items of the persistent kernel
+enum ItemType : int {
+  IT_STATS = 1,    // 64 KB chunk of one logit row: softmax statistics
+  IT_RSUM = 2,     // one stage of rows k of both models: sum of [p - q]_+
+  IT_PSUM = 3,     // one statistics chunk of the target row k: sum of p without y
+  IT_SEARCH = 4,   // inverse-CDF search inside one located chunk, then outputs
+};
+
+// search kinds
+enum SearchKind : int { SK_P = 0, SK_RESID = 1 };
+
+// state word bits of a request: bit i (< 31) position i evaluated, bit 32+i
+// position i accepted, bit 63 the bonus row complete
+constexpr unsigned long long kBonusBit = 1ull << 63;
+
 // ---------------------------------------------------------------------------
 // geometry
 
@@ -38,8 +53,8 @@ constexpr int kStageBytes = 16384;                      // one bulk copy
 constexpr int kStages = 6;                              // ring depth per CTA
 constexpr int kChunkBytes = 4 * kStageBytes;            // one work item of a row
 constexpr int kEpiSlots = 8;                            // consumer -> epilogue ring
-constexpr int kDrawChunkElems = 4096;                   // residual pass chunk
-constexpr int kDrawThreads = 256;
+constexpr int kGroupVecs = 8;                           // residual group: 8 vectors (64 bf16 / 32 fp32 tokens)
+constexpr int kGroupsPerStage = kStageBytes / 16 / kGroupVecs;   // 128
 constexpr uint32_t kSkipInc = 1u << 20;                 // arrival mark of a skipped chunk
 constexpr uint32_t kCountMask = kSkipInc - 1;
 constexpr int kNoReject = 0x7fffffff;
@@ -64,31 +79,65 @@ struct alignas(16) RowStats {
 // workspace layout (offsets in bytes, 256-aligned)
 
 struct Layout {
-  size_t hdr, req_flags, known_reject, row_list, row_arr, row_done, row_stats, row_xy, parts,
-      pair_arr, pair_res, pair_a, draw_arr, draw_parts, total;
+  size_t hdr, req_flags, known_reject, row_list, row_arr, row_done, row_stats, row_xy, parts, pair_arr,
+      pair_res, pair_a, req_state, req_cnt, req_k, req_status, req_z, rsum_arr, rsum_parts, rsum_gs, search, dq,
+      total;
   int nrows;      // B*(G+1) + B*G row ids
-  int nch;        // stats chunks per row
-  int nch2;       // residual-pass chunks per row
+  int nch;        // statistics chunks per row
+  int nres;       // residual chunks per row (one stage each)
+  int dq_cap;     // dynamic queue capacity
+};
+
+// Counters of one call, each on its own 128-byte line: they are hit by
+// atomics from every CTA, and sharing a line would serialise unrelated ones.
+struct alignas(128) Counter {
+  unsigned int v;
+  unsigned int pad[31];
 };
 
 struct Header {
-  unsigned int queue;      // next work item to claim
-  unsigned int n_items;    // work items this call
-  unsigned int error;      // SPEC_ST_TIMEOUT when any wait gave up
-  unsigned int n_uncertain;
+  Counter queue;        // next static (statistics) item to claim
+  Counter dq_head;      // next dynamic-queue ticket
+  Counter dq_tail;      // dynamic items reserved
+  Counter done;         // requests whose outputs are written
+  Counter error;        // SPEC_ST_TIMEOUT when any wait gave up
+  Counter misc;         // n_items, n_valid, exited, n_uncertain (rarely written)
+};
+#define HDR_N_ITEMS(h) ((h)->misc.pad[0])
+#define HDR_N_VALID(h) ((h)->misc.pad[1])
+#define HDR_EXITED(h) ((h)->misc.pad[2])
+#define HDR_UNCERTAIN(h) ((h)->misc.pad[3])
+
+// a dynamically created work item (type 0 = slot reserved, not yet written)
+struct alignas(16) DynItem {
+  int type, b, c, aux;
+};
+
+// where the final draw of a request searches (written before its IT_SEARCH item)
+struct alignas(16) SearchDesc {
+  double tl;       // target cumulative weight, relative to the chunk start
+  double W;        // total weight of the draw
+  int kind;        // SK_P or SK_RESID
+  int e0, e1;      // element range of the located chunk
+  int excl;        // token left out (one-hot residual), or -1
+  int status;      // informational status bits gathered so far
+  int row_t, row_d;
+  int pad;
 };
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 __host__ __device__ inline int chunk_elems(int dtype) { return kChunkBytes / (dtype == SPEC_BF16 ? 2 : 4); }
+__host__ __device__ inline int stage_elems(int dtype) { return kStageBytes / (dtype == SPEC_BF16 ? 2 : 4); }
 
 __host__ inline Layout make_layout(int B, int G, int V, int dtype) {
   Layout L{};
   const int nrows = B * (G + 1) + B * G;
-  const int ce = chunk_elems(dtype);
+  const int ce = chunk_elems(dtype), se = stage_elems(dtype);
   L.nrows = nrows;
   L.nch = (V + ce - 1) / ce;
-  L.nch2 = (V + kDrawChunkElems - 1) / kDrawChunkElems;
+  L.nres = (V + se - 1) / se;
+  L.dq_cap = B * (L.nres + 2);
   size_t o = 0;
   L.hdr = o;          o = align256(o + sizeof(Header));
   L.req_flags = o;    o = align256(o + sizeof(int) * B);
@@ -101,9 +150,17 @@ __host__ inline Layout make_layout(int B, int G, int V, int dtype) {
   L.parts = o;        o = align256(o + sizeof(Part) * (size_t)nrows * L.nch);
   L.pair_arr = o;     o = align256(o + sizeof(unsigned) * B * (G + 1));
   L.pair_res = o;     o = align256(o + sizeof(int) * B * (G + 1));
-  L.pair_a = o;       o = align256(o + sizeof(double) * B * (G + 1));
-  L.draw_arr = o;     o = align256(o + sizeof(unsigned) * B);
-  L.draw_parts = o;   o = align256(o + sizeof(double) * (size_t)B * L.nch2);
+  L.pair_a = o;       o = align256(o + sizeof(float) * B * (G + 1));
+  L.req_state = o;    o = align256(o + sizeof(unsigned long long) * B);
+  L.req_cnt = o;      o = align256(o + sizeof(unsigned) * 2 * B);
+  L.req_k = o;        o = align256(o + sizeof(int) * B);
+  L.req_status = o;   o = align256(o + sizeof(int) * B);
+  L.req_z = o;        o = align256(o + sizeof(int) * B);
+  L.rsum_arr = o;     o = align256(o + sizeof(unsigned) * B);
+  L.rsum_parts = o;   o = align256(o + sizeof(double) * (size_t)B * L.nres);
+  L.rsum_gs = o;      o = align256(o + sizeof(float) * (size_t)B * L.nres * kGroupsPerStage);
+  L.search = o;       o = align256(o + sizeof(SearchDesc) * B);
+  L.dq = o;           o = align256(o + sizeof(DynItem) * (size_t)L.dq_cap);
   L.total = o;
   return L;
 }
@@ -115,6 +172,7 @@ struct Params {
   const unsigned char* target;   // [B, G+1, V]
   const unsigned char* draft;    // [B, G, V] or null
   int dtype, B, G, V, mode, signals_on;
+  int aligned_rows;              // every row starts on a 16-byte boundary
   const int32_t* draft_tokens;
   const int32_t* gamma;
   const float* temperature;
@@ -133,14 +191,22 @@ struct Params {
   unsigned* row_arr;
   int* row_done;
   RowStats* row_stats;
-  float* row_xy;        // logit of the row at its draft token (rows i < gamma_b)
+  float* row_xy;                 // logit of the row at its draft token (rows i < gamma_b)
   Part* parts;
   unsigned* pair_arr;
   int* pair_res;
-  double* pair_a;
-  unsigned* draw_arr;
-  double* draw_parts;
-  int nrows, nch, nch2;
+  float* pair_a;
+  unsigned long long* req_state;
+  unsigned* req_cnt;             // [B][2]: draft rows complete, conditions met
+  int* req_k;
+  int* req_status;
+  int* req_z;
+  unsigned* rsum_arr;
+  double* rsum_parts;
+  float* rsum_gs;                // residual sums per group of kGroupVecs vectors
+  SearchDesc* search;
+  DynItem* dq;
+  int nrows, nch, nres, dq_cap;
 };
 
 // row ids: target rows first, then draft rows
@@ -354,15 +420,11 @@ __device__ __forceinline__ Part empty_part() {
   return p;
 }
 
-// kernels (defined in the .cu files)
-__global__ void plan_kernel(Params P);
-
-// Host-side launchers, one per translation unit that defines the kernels.
-// The caller's stream; `pdl` enables programmatic dependent launch.
+// Host-side launchers (defined in verify.cu).  `pdl` enables programmatic
+// dependent launch on the caller's stream.
 cudaError_t launch_plan(const Params& P, cudaStream_t s);
-cudaError_t launch_stats(const Params& P, int grid, cudaStream_t s, bool pdl);
-cudaError_t launch_finalize(const Params& P, dim3 grid, cudaStream_t s, bool pdl);
-cudaError_t configure_stats_kernels();   // dynamic shared-memory limit, current device
+cudaError_t launch_verify(const Params& P, int grid, cudaStream_t s, bool pdl);
+cudaError_t configure_kernels();   // dynamic shared-memory limit, current device
 
 template <class K>
 inline cudaError_t launch_ex(K kern, dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl, const Params& P) {

@@ -1,0 +1,1743 @@
+// verify.cu -- the two kernels of one verification call.
+//
+// plan_kernel (1 CTA): resets the workspace counters, settles the requests
+// whose inputs are invalid up front, and writes the position-major row
+// schedule.
+//
+// verify_kernel: a persistent, warp-specialised kernel (2 CTAs per SM) that
+// takes a request from its logits to its committed tokens.  Work items come
+// from two queues: the static schedule of 64 KB chunks of logit rows, and a
+// device-side queue of items created on the fly (drained first):
+//   IT_STATS   softmax statistics of one chunk of a row (max m, s = sum
+//              2^{(x-m)c}, for signal rows t = sum (x-m)c 2^{(x-m)c}, greedy
+//              rows the max and its lowest index);
+//   IT_RSUM    sum of the residual [p_k - q_k]_+ over one 16 KB slice of
+//              rows k of both models (after a reject at k);
+//   IT_PSUM    sum of p_k without y_k over one chunk (one-hot reject);
+//   IT_SEARCH  the inverse-CDF search inside the located chunk.
+// Roles inside a CTA:
+//   producer warp   claims items (dynamic queue first), skips rows that an
+//                   earlier reject has voided, stages the bytes into a 6-deep
+//                   ring of 16 KB shared-memory buffers with cp.async.bulk
+//                   completed on mbarriers;
+//   8 consumer warps  read the staged bytes with 128-bit shared loads and do
+//                   the arithmetic of the item;
+//   2 epilogue warps  publish per-item partials; the CTA that completes a row
+//                   merges its chunks (fixed order, so results do not depend
+//                   on scheduling), evaluates the acceptance test of the
+//                   position (tutorial page "5.1 投机解码核心原理", sections
+//                   3.1-3.3), and tracks per request when its first reject k
+//                   (section 5.1) and its signal rows are known; then it
+//                   settles the request or creates its draw items.
+// Rows of a request after a decided reject are skipped (early exit).  Draw
+// items run right after the decision, while rows k are still in L2.
+// Every spin is bounded in time; a wait that gives up sets SPEC_ST_TIMEOUT,
+// and the last CTA to leave voids any request left unfinished.
+#include <climits>
+
+#include "common.cuh"
+
+namespace sv {
+namespace {
+
+constexpr int kVoidMask = ~(SPEC_ST_ZERO_RESIDUAL | SPEC_ST_GUARDED);
+constexpr int kFinished = 1 << 30;                 // req_status: outputs written
+constexpr float kDrawGuard = 1e-6f;                // draws this close to an edge are counted
+
+__device__ __forceinline__ float qnan() { return __int_as_float(0x7fc00000); }
+
+__device__ __forceinline__ int gamma_of(const Params& P, int b) { return P.gamma ? P.gamma[b] : P.G; }
+
+// Outputs of a request that commits nothing (an error found up front or on
+// the way); `st` holds the error bits.  Any number of threads, strided by n.
+__device__ void write_void_outputs(const Params& P, int b, int st, int t, int n) {
+  const int G = P.G;
+  if (P.mode != MODE_SIGNALS) {
+    for (int j = t; j <= G; j += n) P.tokens[(size_t)b * (G + 1) + j] = -1;
+    if (P.accept_prob)
+      for (int j = t; j < G; j += n) P.accept_prob[(size_t)b * G + j] = qnan();
+    if (t == 0) P.accept_len[b] = 0;
+  }
+  if (P.signals && t == 0)
+    for (int j = 0; j < 4; ++j) P.signals[(size_t)b * 4 + j] = qnan();
+  if (P.row_signals)
+    for (int j = t; j < 2 * G; j += n) P.row_signals[(size_t)b * 2 * G + j] = qnan();
+  if (t == 0 && P.status) P.status[b] = st;
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// plan: reset the counters and build the compacted row schedule
+
+namespace {
+
+enum BlockType : int { BT_T = 0, BT_D = 1, BT_PAIR = 2 };
+
+struct Block {
+  int type, i;
+};
+
+// Schedule blocks in position-major order.  Full-q with signals reads every
+// draft row anyway, so draft blocks are used as filler between target
+// positions: PAIR(0) | D1 D2 | T1 | D3 D4 | T2 | ... | T_G.  Between the
+// target rows of positions i-1 and i there are then about 2B rows of other
+// work, longer than the reading window of the whole GPU, so the test at i-1
+// is usually decided before target row i of the request is claimed.  Draft
+// block j always precedes target block j, as the test at j needs both.
+__device__ inline int build_blocks(int mode, int signals_on, int G, Block* out) {
+  int n = 0;
+  if (mode == MODE_SIGNALS) {
+    for (int i = 0; i < G; ++i) out[n++] = {BT_D, i};
+  } else if (mode == MODE_SAMPLE && signals_on && G > 0) {
+    out[n++] = {BT_PAIR, 0};
+    int dnext = 1;
+    for (int i = 1; i <= G; ++i) {
+      for (int f = 0; f < 2 && dnext <= G - 1; ++f) out[n++] = {BT_D, dnext++};
+      out[n++] = {BT_T, i};
+    }
+  } else if (mode == MODE_SAMPLE) {
+    for (int i = 0; i <= G; ++i) out[n++] = {BT_PAIR, i};
+  } else {
+    for (int i = 0; i <= G; ++i) out[n++] = {BT_T, i};
+  }
+  return n;
+}
+
+__device__ inline int rows_for(const Block& bl, int gam) {
+  const int nt = gam >= bl.i ? 1 : 0;
+  const int nd = gam > bl.i ? 1 : 0;
+  if (bl.type == BT_T) return nt;
+  if (bl.type == BT_D) return nd;
+  return nt + nd;
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(1024) plan_kernel(Params P) {
+  griddep_launch();
+  const int B = P.B, G = P.G, tid = threadIdx.x, nth = blockDim.x;
+  const int lane = tid & 31, warp = tid >> 5, nwarps = nth >> 5;
+  __shared__ int s_count[64];
+  __shared__ int s_off[65];
+  __shared__ Block s_blk[64];
+  __shared__ int s_nb;
+  __shared__ unsigned s_settled;
+
+  if (tid == 0) s_settled = 0u;
+  for (int j = tid; j < P.nrows; j += nth) {
+    P.row_arr[j] = 0u;
+    P.row_done[j] = 0;
+  }
+  for (int j = tid; j < B * (G + 1); j += nth) {
+    P.pair_arr[j] = 0u;
+    P.pair_res[j] = PC_NONE;
+    P.pair_a[j] = qnan();
+  }
+  for (int j = tid; j < P.dq_cap; j += nth) P.dq[j].type = 0;
+  __syncthreads();
+  for (int b = tid; b < B; b += nth) {
+    P.known_reject[b] = kNoReject;
+    P.req_state[b] = 0ull;
+    P.rsum_arr[b] = 0u;
+    P.req_k[b] = 0;
+    int st = 0;
+    const int gam = gamma_of(P, b);
+    if (gam < 0 || gam > G) st |= SPEC_ST_BAD_GAMMA;
+    if (P.mode != MODE_GREEDY && !temperature_ok(P.temperature[b])) st |= SPEC_ST_BAD_TEMPERATURE;
+    P.req_flags[b] = st;
+    // a request with no signal rows has its signal condition met already
+    P.req_cnt[2 * b] = 0u;
+    P.req_cnt[2 * b + 1] = (P.signals_on && st == 0 && gam == 0) ? 1u : 0u;
+    if (st != 0) {
+      write_void_outputs(P, b, st, 0, 1);
+      P.req_status[b] = st | kFinished;
+      atomicAdd(&s_settled, 1u);
+    } else if (P.mode == MODE_SIGNALS && gam == 0) {
+      write_void_outputs(P, b, 0, 0, 1);      // signals of an empty draft are NaN
+      P.req_status[b] = kFinished;
+      atomicAdd(&s_settled, 1u);
+    } else {
+      P.req_status[b] = 0;
+    }
+  }
+  if (tid == 0) s_nb = build_blocks(P.mode, P.signals_on, G, s_blk);
+  __syncthreads();   // req_flags and the block table visible to the whole block
+
+  const int nb = s_nb;
+  // rows per block
+  for (int k = warp; k < nb; k += nwarps) {
+    const Block bl = s_blk[k];
+    int cnt = 0;
+    for (int b0 = 0; b0 < B; b0 += 32) {
+      const int b = b0 + lane;
+      int n = 0;
+      if (b < B && P.req_flags[b] == 0) n = rows_for(bl, gamma_of(P, b));
+      cnt += __reduce_add_sync(0xffffffffu, n);
+    }
+    if (lane == 0) s_count[k] = cnt;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int acc = 0;
+    for (int k = 0; k < nb; ++k) { s_off[k] = acc; acc += s_count[k]; }
+    s_off[nb] = acc;
+    P.hdr->queue.v = 0u;
+    HDR_N_ITEMS(P.hdr) = (unsigned)acc * (unsigned)P.nch;
+    P.hdr->error.v = 0u;
+    HDR_UNCERTAIN(P.hdr) = 0u;
+    P.hdr->dq_head.v = 0u;
+    P.hdr->dq_tail.v = 0u;
+    P.hdr->done.v = 0u;
+    HDR_N_VALID(P.hdr) = (unsigned)B - s_settled;
+    HDR_EXITED(P.hdr) = 0u;
+  }
+  __syncthreads();
+  // write the compacted row ids
+  for (int k = warp; k < nb; k += nwarps) {
+    const Block bl = s_blk[k];
+    int off = s_off[k];
+    for (int b0 = 0; b0 < B; b0 += 32) {
+      const int b = b0 + lane;
+      int n = 0, gam = 0;
+      if (b < B && P.req_flags[b] == 0) {
+        gam = gamma_of(P, b);
+        n = rows_for(bl, gam);
+      }
+      int incl = n;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, d);
+        if (lane >= d) incl += v;
+      }
+      int pos = off + incl - n;
+      if (n > 0) {
+        const bool want_t = bl.type != BT_D && gam >= bl.i;
+        const bool want_d = bl.type != BT_T && gam > bl.i;
+        if (want_t) P.row_list[pos++] = target_row_id(b, bl.i, G);
+        if (want_d) P.row_list[pos++] = draft_row_id(b, bl.i, B, G);
+      }
+      off += __shfl_sync(0xffffffffu, incl, 31);
+    }
+  }
+}
+
+
+// ---------------------------------------------------------------------------
+// persistent kernel: shared state
+
+namespace {
+
+constexpr int F_FIRST = 1, F_LAST = 2, F_TERM = 4, F_DIRECT = 8;
+
+// One staged piece of an item (producer -> consumers).
+struct StageDesc {
+  int type, b, i, kind;
+  int row_id, chunk, elem0, nvec;
+  int flags, head0, nhead, tail0;
+  int ntail, y, aux, n_elems;       // n_elems: direct stages
+  long long src_elem;               // direct stages: flat element offset of the source
+  float c, m1, s1, m2;              // scale; row statistics of the rows used
+  float s2, tl;                     // search: target weight within the chunk (fp32 view)
+  int pad[2];
+};
+
+// One finished item (consumers -> epilogue).
+struct EpiSlot {
+  int type, row_id, b, i;
+  int kind, chunk, term, z;
+  float xy, margin;
+  int pad[2];
+  float wsum[kConsumerWarps];       // p sums per consumer warp (IT_PSUM)
+  double dsum[kConsumerWarps];      // residual sums per consumer warp (IT_RSUM)
+  Part part[kConsumerWarps];        // statistics per consumer warp
+};
+
+constexpr int kVecPerStage = kStageBytes / 16;     // 1024
+
+struct __align__(128) VSmem {
+  unsigned char ring[kStages][kStageBytes];
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t epi_full[kEpiSlots];
+  uint64_t epi_empty[kEpiSlots];
+  StageDesc desc[kStages];
+  EpiSlot slot[kEpiSlots];
+  // search scratch (consumer warps only)
+  float vs[kVecPerStage];
+  double wtot[kConsumerWarps];
+  double carry, cprev, cat;
+  int found_thread, z, last_elem, found;
+  int abort;
+};
+
+}  // namespace
+
+namespace {
+
+__device__ __forceinline__ bool aborted(const VSmem& S) {
+  return *reinterpret_cast<const volatile int*>(&S.abort) != 0;
+}
+
+__device__ __forceinline__ void set_abort(const Params& P, VSmem& S) {
+  *reinterpret_cast<volatile int*>(&S.abort) = 1;
+  atomicOr(&P.hdr->error.v, (unsigned)SPEC_ST_TIMEOUT);
+}
+
+// Bounded wait that also gives up when another role of the CTA aborted.
+__device__ __forceinline__ bool wait_bar(VSmem& S, uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (aborted(S)) return false;
+    if (globaltimer() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+template <int DT>
+struct VecT;
+template <>
+struct VecT<SPEC_BF16> {
+  static constexpr int N = 8;
+  __device__ static __forceinline__ void unpack(const uint4& w, float* x) {
+    x[0] = bf16_lo(w.x); x[1] = bf16_hi(w.x); x[2] = bf16_lo(w.y); x[3] = bf16_hi(w.y);
+    x[4] = bf16_lo(w.z); x[5] = bf16_hi(w.z); x[6] = bf16_lo(w.w); x[7] = bf16_hi(w.w);
+  }
+};
+template <>
+struct VecT<SPEC_F32> {
+  static constexpr int N = 4;
+  __device__ static __forceinline__ void unpack(const uint4& w, float* x) {
+    x[0] = __uint_as_float(w.x); x[1] = __uint_as_float(w.y);
+    x[2] = __uint_as_float(w.z); x[3] = __uint_as_float(w.w);
+  }
+};
+
+// Per-thread running state of one chunk.
+struct RunState {
+  float m, s, t, mc;
+  int idx;
+  int nan;
+};
+
+__device__ __forceinline__ void run_reset(RunState& r) {
+  r.m = -INFINITY; r.s = 0.f; r.t = 0.f; r.mc = 0.f; r.idx = 0x3fffffff; r.nan = 0;
+}
+
+// ---- per-stage processing ---------------------------------------------------
+// Each consumer thread owns 4 of the stage's 1024 16-byte vectors (strided by
+// 256, so every shared load of a warp is one contiguous 512-byte run).  The
+// stage max is taken first with a max tree (one running-max update per stage,
+// not per vector), then the 32 (bf16) or 16 (fp32) terms are independent, so
+// their exp2 and adds pipeline.  Vectors past the staged bytes read as -inf.
+
+constexpr int kVecPerThread = kStageBytes / 16 / kConsumerThreads;   // 4
+
+__device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {       // NaN-ignoring
+  uint32_t d;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t bmax2_nan(uint32_t a, uint32_t b) {   // NaN-propagating
+  uint32_t d;
+  asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+template <int DT>
+__device__ __forceinline__ void load_stage(const uint4* vec, int nvec, int tid, uint4 (&w)[kVecPerThread]) {
+  const uint32_t ninf = DT == SPEC_BF16 ? 0xff80ff80u : 0xff800000u;
+#pragma unroll
+  for (int r = 0; r < kVecPerThread; ++r) {
+    const int v = tid + r * kConsumerThreads;
+    w[r] = v < nvec ? vec[v] : make_uint4(ninf, ninf, ninf, ninf);
+  }
+}
+
+// max over the thread's stage elements (NaN ignored or propagated)
+template <int DT, bool NANP>
+__device__ __forceinline__ float stage_max(const uint4 (&w)[kVecPerThread]) {
+  if (DT == SPEC_BF16) {
+    uint32_t h[2 * kVecPerThread];
+#pragma unroll
+    for (int r = 0; r < kVecPerThread; ++r) {
+      h[2 * r] = NANP ? bmax2_nan(w[r].x, w[r].y) : bmax2(w[r].x, w[r].y);
+      h[2 * r + 1] = NANP ? bmax2_nan(w[r].z, w[r].w) : bmax2(w[r].z, w[r].w);
+    }
+#pragma unroll
+    for (int n = 2 * kVecPerThread; n > 1; n >>= 1)
+#pragma unroll
+      for (int k = 0; k < n / 2; ++k) h[k] = NANP ? bmax2_nan(h[2 * k], h[2 * k + 1]) : bmax2(h[2 * k], h[2 * k + 1]);
+    const float lo = bf16_lo(h[0]), hi = bf16_hi(h[0]);
+    if (NANP && (lo != lo || hi != hi)) return __int_as_float(0x7fc00000);
+    return fmaxf(lo, hi);
+  } else {
+    float f[4 * kVecPerThread];
+#pragma unroll
+    for (int r = 0; r < kVecPerThread; ++r) {
+      f[4 * r] = __uint_as_float(w[r].x); f[4 * r + 1] = __uint_as_float(w[r].y);
+      f[4 * r + 2] = __uint_as_float(w[r].z); f[4 * r + 3] = __uint_as_float(w[r].w);
+    }
+    bool nan = false;
+    if (NANP) {
+#pragma unroll
+      for (int k = 0; k < 4 * kVecPerThread; ++k) nan |= f[k] != f[k];
+    }
+#pragma unroll
+    for (int n = 4 * kVecPerThread; n > 1; n >>= 1)
+#pragma unroll
+      for (int k = 0; k < n / 2; ++k) f[k] = fmaxf(f[2 * k], f[2 * k + 1]);
+    return nan ? __int_as_float(0x7fc00000) : f[0];
+  }
+}
+
+// -inf logits must contribute 0 to t = sum a 2^a, not -inf * 0.  For bf16
+// signal rows the staged words are clamped at -2^100 with one packed max per
+// two logits (the stage max is taken before, on the raw words, so a row of
+// -inf still has no finite max); 2^{-2^100 c} is 0 and its product with the
+// finite exponent is 0.  For fp32 rows, or scales large enough that the
+// clamped exponent could overflow, the exponent itself is clamped.
+constexpr uint32_t kClampWords = 0xF180F180u;   // bf16 pair (-2^100, -2^100)
+constexpr float kClampScaleMax = 1048576.f;
+
+// Packed fp32 pairs (Blackwell FFMA2 / FADD2): the exponent, the sum tree
+// and the entropy product run two logits per instruction.
+__device__ __forceinline__ float2 f2(float a, float b) { return make_float2(a, b); }
+
+template <int DT, bool ENT>
+__device__ __forceinline__ void stage_softmax(RunState& r, uint4 (&w)[kVecPerThread], float c) {
+  using Vec = VecT<DT>;
+  constexpr int N = Vec::N;
+  constexpr int NP = N / 2;                     // pairs per vector
+  const float vm = stage_max<DT, false>(w);
+  if (vm > r.m) {
+    if (r.m != -INFINITY) {
+      const float d = (r.m - vm) * c;
+      const float f = ex2(d);
+      if (ENT) r.t = f * fmaf(d, r.s, r.t);
+      r.s *= f;
+    }
+    r.m = vm;
+    r.mc = vm * c;
+  }
+  const bool packed_clamp = ENT && DT == SPEC_BF16 && c <= kClampScaleMax;
+  if (packed_clamp) {
+#pragma unroll
+    for (int q = 0; q < kVecPerThread; ++q) {
+      w[q].x = bmax2_nan(w[q].x, kClampWords); w[q].y = bmax2_nan(w[q].y, kClampWords);
+      w[q].z = bmax2_nan(w[q].z, kClampWords); w[q].w = bmax2_nan(w[q].w, kClampWords);
+    }
+  }
+  const float2 C2 = f2(c, c), NMC2 = f2(-r.mc, -r.mc), LO2 = f2(-256.f, -256.f);
+  float2 s2 = f2(0.f, 0.f), t2 = f2(0.f, 0.f);
+#pragma unroll
+  for (int q = 0; q < kVecPerThread; ++q) {
+    float x[N];
+    Vec::unpack(w[q], x);
+    float2 e[NP];
+#pragma unroll
+    for (int k = 0; k < NP; ++k) {
+      float2 a = __ffma2_rn(f2(x[2 * k], x[2 * k + 1]), C2, NMC2);
+      e[k] = f2(ex2(a.x), ex2(a.y));
+      if (ENT) {
+        if (!packed_clamp) a = f2(fmaxf(a.x, LO2.x), fmaxf(a.y, LO2.y));
+        t2 = __ffma2_rn(a, e[k], t2);
+      }
+    }
+    float2 v;
+    if (NP == 4) v = __fadd2_rn(__fadd2_rn(e[0], e[1]), __fadd2_rn(e[2], e[3]));
+    else v = __fadd2_rn(e[0], e[1]);
+    s2 = __fadd2_rn(s2, v);
+  }
+  r.s += s2.x + s2.y;
+  if (ENT) r.t += t2.x + t2.y;
+}
+
+// Warp partial of a softmax run: the warp max first, one rescale of each
+// lane's sums to it, then plain sums (fixed xor tree: deterministic).
+__device__ __forceinline__ Part warp_softmax_part(const RunState& r, float c, bool ent) {
+  float m = r.m;
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+  float s = 0.f, t = 0.f;
+  if (r.s != 0.f) {                       // lanes that saw nothing contribute 0
+    const float d = (r.m - m) * c;
+    const float f = ex2(d);
+    s = r.s * f;
+    if (ent) t = f * fmaf(d, r.s, r.t);
+  }
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) {
+    s += __shfl_xor_sync(0xffffffffu, s, off);
+    if (ent) t += __shfl_xor_sync(0xffffffffu, t, off);
+  }
+  Part p;
+  p.m = m; p.s = s; p.t = t; p.idx = 0x3fffffff;
+  return p;
+}
+
+template <int DT>
+__device__ __forceinline__ void stage_argmax(RunState& r, const uint4 (&w)[kVecPerThread], int elem0, int tid) {
+  using Vec = VecT<DT>;
+  constexpr int N = Vec::N;
+  const float vm = stage_max<DT, true>(w);
+  if (vm != vm) { r.nan = 1; return; }
+  if (vm > r.m) {
+    int idx = 0x3fffffff;
+#pragma unroll
+    for (int q = kVecPerThread - 1; q >= 0; --q) {
+      float x[N];
+      Vec::unpack(w[q], x);
+#pragma unroll
+      for (int k = N - 1; k >= 0; --k)
+        if (x[k] == vm) idx = elem0 + (tid + q * kConsumerThreads) * N + k;
+    }
+    r.m = vm;
+    r.idx = idx;
+  }
+}
+
+// one scalar logit at row element `e` (head/tail of a chunk)
+template <bool GREEDY>
+__device__ __forceinline__ void run_scalar(RunState& r, float x, int e, float c, bool ent) {
+  if (GREEDY) {
+    r.nan |= x != x;
+    if (x > r.m || (x == r.m && e < r.idx)) { r.m = x; r.idx = e; }
+    return;
+  }
+  if (x > r.m) {
+    if (r.m != -INFINITY) {
+      const float d = (r.m - x) * c;
+      const float f = ex2(d);
+      if (ent) r.t = f * fmaf(d, r.s, r.t);
+      r.s *= f;
+    }
+    r.m = x;
+    r.mc = x * c;
+  }
+  const float a = fmaf(x, c, -r.mc);
+  const float ev = ex2(a);
+  r.s += ev;
+  if (ent) r.t = fmaf(fmaxf(a, -256.f), ev, r.t);
+}
+
+__device__ __forceinline__ Part to_part(const RunState& r) {
+  Part p;
+  p.m = r.m; p.s = r.s; p.t = r.t;
+  p.idx = (r.idx & ~kIdxNaN) | (r.nan ? kIdxNaN : 0);
+  return p;
+}
+
+
+// ---------------------------------------------------------------------------
+// small memory-model helpers
+
+__device__ __forceinline__ unsigned ld_relaxed_u32(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ int ld_acquire_i32(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_i32(int* p, int v) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long atom_or_acqrel_u64(unsigned long long* p, unsigned long long v) {
+  unsigned long long old;
+  asm volatile("atom.acq_rel.gpu.global.or.b64 %0, [%1], %2;" : "=l"(old) : "l"(p), "l"(v) : "memory");
+  return old;
+}
+__device__ __forceinline__ void consumer_bar() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumerThreads) : "memory"); }
+
+// ---------------------------------------------------------------------------
+// device work queue
+
+// Reserve n consecutive entries (chunk indices c0 .. c0+n-1); every lane of
+// the calling warp writes the entries j = lane, lane + 32, ... (payload
+// first, then the type with release, which publishes the entry).  Warp-wide.
+__device__ void enqueue_items(const Params& P, int n, int type, int b, int c0, int aux, int lane) {
+  unsigned base = 0;
+  if (lane == 0) base = atomicAdd(&P.hdr->dq_tail.v, (unsigned)n);
+  base = __shfl_sync(0xffffffffu, base, 0);
+  for (int j = lane; j < n; j += 32) {
+    const unsigned slot = base + (unsigned)j;
+    if (slot >= (unsigned)P.dq_cap) {       // cannot happen; keeps every write in bounds
+      atomicOr(&P.hdr->error.v, (unsigned)SPEC_ST_TIMEOUT);
+      continue;
+    }
+    DynItem* e = P.dq + slot;
+    __stcg(&e->b, b);
+    __stcg(&e->c, c0 + j);
+    __stcg(&e->aux, aux);
+    st_release_i32(&e->type, type);
+  }
+  __syncwarp();
+}
+
+// Dynamic items are handed out by ticket: a producer holds one ticket (an
+// index into the queue, from one atomicAdd) and takes the item stored there
+// once an enqueuer has published it.  Tickets past the last item are never
+// served; their holders leave when every request is done.
+__device__ __forceinline__ int ticket_peek(const Params& P, unsigned ticket) {   // relaxed, non-blocking
+  if (ticket >= (unsigned)P.dq_cap) return 0;
+  int v;
+  asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(&P.dq[ticket].type) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void ticket_take(const Params& P, unsigned ticket, DynItem& it) {
+  const DynItem* e = P.dq + ticket;
+  it.type = ld_acquire_i32(&e->type);          // orders the payload reads after the publish
+  it.b = __ldcg(&e->b);
+  it.c = __ldcg(&e->c);
+  it.aux = __ldcg(&e->aux);
+}
+
+// ---------------------------------------------------------------------------
+// producer
+
+struct ItemMeta {
+  unsigned q;
+  int rid, b, i, kind, chunk, y;
+  bool valid, skip;
+  float c;
+};
+
+// Metadata of a claimed static item, in two dependent levels so the producer
+// can keep them in flight while it stages earlier items: the row id (from the
+// schedule), then per-request values (first known reject, temperature,
+// gamma, draft token).
+__device__ __forceinline__ int item_row(const Params& P, unsigned q, unsigned n_items) {
+  return q < n_items ? __ldg(P.row_list + q / (unsigned)P.nch) : 0;
+}
+
+template <bool GREEDY>
+__device__ __forceinline__ ItemMeta item_meta(const Params& P, unsigned q, int rid, unsigned n_items) {
+  ItemMeta m;
+  m.q = q;
+  m.valid = q < n_items;
+  m.skip = false;
+  m.y = -1;
+  m.c = 0.f;
+  m.rid = rid;
+  m.b = m.i = m.kind = 0;
+  m.chunk = (int)(q % (unsigned)P.nch);
+  if (!m.valid) return m;
+  const int G = P.G;
+  decode_row(rid, P.B, G, m.kind, m.b, m.i);
+  const int b = m.b, i = m.i;
+  const int kr = (m.kind == KIND_TARGET || !P.signals_on) ? ld_relaxed(P.known_reject + b) : kNoReject;
+  const float T = GREEDY ? 1.f : P.temperature[b];
+  const int gam = gamma_of(P, b);
+  int y = -1;
+  // the draft token (sample / one-hot only: signals-only calls have no tokens)
+  if (!GREEDY && P.mode != MODE_SIGNALS && i < gam) y = P.draft_tokens[(size_t)b * G + i];
+  m.skip = kr < i;             // a reject at an earlier position voids this row
+  m.c = GREEDY ? 0.f : scale_of(T);
+  m.y = y;
+  return m;
+}
+
+// Stage one piece: wait for a free ring slot, write its descriptor, start the
+// bulk copy (bytes > 0) or just mark it full.
+__device__ __forceinline__ bool put_stage(VSmem& S, int& stage, uint32_t& phase, const StageDesc& d,
+                                          uintptr_t src, uint32_t bytes) {
+  if (!wait_bar(S, &S.empty[stage], phase ^ 1u)) return false;
+  S.desc[stage] = d;
+  if (bytes > 0) {
+    mbar_arrive_expect_tx(&S.full[stage], bytes);
+    bulk_load(S.ring[stage], reinterpret_cast<const void*>(src), bytes, &S.full[stage]);
+  } else {
+    mbar_arrive(&S.full[stage]);
+  }
+  if (++stage == kStages) { stage = 0; phase ^= 1u; }
+  return true;
+}
+
+template <int DT, bool GREEDY>
+__device__ bool stage_stats_item(const Params& P, VSmem& S, int& stage, uint32_t& phase, const ItemMeta& cur) {
+  constexpr int ES = DT == SPEC_BF16 ? 2 : 4;
+  const int G = P.G, V = P.V;
+  const int ce = chunk_elems(DT);
+  const unsigned char* tens = cur.kind == KIND_TARGET ? P.target : P.draft;
+  const long long row0 = row_elem_offset(cur.kind, cur.b, cur.i, G, V);
+  const int e_begin = cur.chunk * ce;
+  const int e_end = min(e_begin + ce, V);
+  const uintptr_t rowaddr = reinterpret_cast<uintptr_t>(tens) + (uintptr_t)(row0 * ES);
+  const uintptr_t a_start = rowaddr + (uintptr_t)e_begin * ES;
+  const uintptr_t a_end = rowaddr + (uintptr_t)e_end * ES;
+  uintptr_t A0 = (a_start + 15) & ~uintptr_t(15);
+  uintptr_t A1 = a_end & ~uintptr_t(15);
+  int nhead, ntail;
+  if (A1 <= A0) {            // no aligned middle: everything is scalar head
+    A0 = A1 = a_end;
+    nhead = e_end - e_begin;
+    ntail = 0;
+  } else {
+    nhead = (int)((A0 - a_start) / ES);
+    ntail = (int)((a_end - A1) / ES);
+  }
+  const long long mid = (long long)(A1 - A0);
+  const int npieces = mid > 0 ? (int)((mid + kStageBytes - 1) / kStageBytes) : 1;
+  StageDesc d{};
+  d.type = IT_STATS;
+  d.row_id = cur.rid; d.b = cur.b; d.i = cur.i; d.kind = cur.kind;
+  d.chunk = cur.chunk;
+  d.head0 = e_begin; d.nhead = nhead;
+  d.tail0 = e_end - ntail; d.ntail = ntail;
+  d.c = cur.c;
+  d.y = cur.y;
+  for (int p = 0; p < npieces; ++p) {
+    const long long off = (long long)p * kStageBytes;
+    const uint32_t bytes = mid > 0 ? (uint32_t)(mid - off < kStageBytes ? mid - off : kStageBytes) : 0u;
+    d.elem0 = (int)((A0 + (uintptr_t)off - rowaddr) / ES);
+    d.nvec = (int)(bytes / 16);
+    d.flags = (p == 0 ? F_FIRST : 0) | (p == npieces - 1 ? F_LAST : 0);
+    if (!put_stage(S, stage, phase, d, A0 + (uintptr_t)off, bytes)) return false;
+  }
+  return true;
+}
+
+// Stage the elements [e0, e1) of one row (at most one stage worth) with a
+// bulk copy when rows are 16-byte aligned, else as a direct stage that the
+// consumers fill themselves.
+template <int DT>
+__device__ __forceinline__ bool put_row_range(const Params& P, VSmem& S, int& stage, uint32_t& phase,
+                                              StageDesc d, int kind, int b, int i, int e0, int e1) {
+  constexpr int ES = DT == SPEC_BF16 ? 2 : 4;
+  const unsigned char* tens = kind == KIND_TARGET ? P.target : P.draft;
+  const long long src = row_elem_offset(kind, b, i, P.G, P.V) + e0;
+  d.elem0 = e0;
+  d.n_elems = e1 - e0;
+  d.src_elem = src;
+  d.kind = kind;
+  if (P.aligned_rows) {
+    const uint32_t bytes = (uint32_t)((e1 - e0) * ES);
+    d.nvec = (int)(bytes / 16);
+    return put_stage(S, stage, phase, d, reinterpret_cast<uintptr_t>(tens) + (uintptr_t)(src * ES), bytes);
+  }
+  d.flags |= F_DIRECT;
+  d.nvec = (e1 - e0 + (16 / ES) - 1) / (16 / ES);
+  return put_stage(S, stage, phase, d, 0, 0u);
+}
+
+template <int DT>
+__device__ bool stage_dyn_item(const Params& P, VSmem& S, int& stage, uint32_t& phase, const DynItem& it) {
+  const int G = P.G, V = P.V, se = stage_elems(DT), ce = chunk_elems(DT);
+  const int b = it.b;
+  const float c = scale_of(P.temperature[b]);
+  StageDesc d{};
+  d.type = it.type;
+  d.b = b;
+  d.c = c;
+  d.y = -1;
+  if (it.type == IT_RSUM) {
+    const int k = it.aux, ch = it.c;
+    const RowStats tr = ldcg_stats(P.row_stats + target_row_id(b, k, G));
+    const RowStats dr = ldcg_stats(P.row_stats + draft_row_id(b, k, P.B, G));
+    d.chunk = ch; d.i = k;
+    d.m1 = tr.m; d.s1 = tr.s; d.m2 = dr.m; d.s2 = dr.s;
+    const int e0 = ch * se, e1 = min(e0 + se, V);
+    d.flags = F_FIRST; d.aux = 0;
+    if (!put_row_range<DT>(P, S, stage, phase, d, KIND_TARGET, b, k, e0, e1)) return false;
+    d.flags = F_LAST; d.aux = 1;
+    return put_row_range<DT>(P, S, stage, phase, d, KIND_DRAFT, b, k, e0, e1);
+  }
+  if (it.type == IT_PSUM) {
+    const int k = it.aux, cy = it.c;
+    const RowStats tr = ldcg_stats(P.row_stats + target_row_id(b, k, G));
+    d.chunk = cy; d.i = k;
+    d.m1 = tr.m; d.s1 = tr.s;
+    d.y = P.draft_tokens[(size_t)b * G + k];
+    const int e0 = cy * ce, e1 = min(e0 + ce, V);
+    for (int s0 = e0; s0 < e1; s0 += se) {
+      d.flags = (s0 == e0 ? F_FIRST : 0) | (s0 + se >= e1 ? F_LAST : 0);
+      if (!put_row_range<DT>(P, S, stage, phase, d, KIND_TARGET, b, k, s0, min(s0 + se, e1))) return false;
+    }
+    return true;
+  }
+  // IT_SEARCH: the located chunk of the draw
+  const SearchDesc* sd = P.search + b;
+  const int kind = __ldcg(&sd->kind), e0 = __ldcg(&sd->e0), e1 = __ldcg(&sd->e1);
+  const int rt = __ldcg(&sd->row_t);
+  int tk, tb, ti;
+  decode_row(rt, P.B, G, tk, tb, ti);
+  const RowStats tr = ldcg_stats(P.row_stats + rt);
+  d.m1 = tr.m; d.s1 = tr.s;
+  d.y = __ldcg(&sd->excl);
+  d.aux = kind;
+  d.i = ti;
+  for (int s0 = e0; s0 < e1; s0 += se) {
+    d.flags = (s0 == e0 ? F_FIRST : 0) | (s0 + se >= e1 ? F_LAST : 0);
+    if (!put_row_range<DT>(P, S, stage, phase, d, KIND_TARGET, b, ti, s0, min(s0 + se, e1))) return false;
+  }
+  return true;
+}
+
+template <int DT, bool GREEDY>
+__device__ void producer_role(const Params& P, VSmem& S) {
+  const unsigned n_items = HDR_N_ITEMS(P.hdr);
+  const unsigned n_valid = HDR_N_VALID(P.hdr);
+  int stage = 0;
+  uint32_t phase = 0;
+  bool ok = true;
+  const bool dyn = !GREEDY && (P.mode == MODE_SAMPLE || P.mode == MODE_ONEHOT);
+  unsigned ticket = dyn ? atomicAdd(&P.hdr->dq_head.v, 1u) : 0xffffffffu;
+  // software pipeline over static items: cur (metadata complete), item n+1
+  // (row id known), item n+2 (claimed)
+  const unsigned q0 = atomicAdd(&P.hdr->queue.v, 1u);
+  const unsigned q1 = atomicAdd(&P.hdr->queue.v, 1u);
+  unsigned q2 = atomicAdd(&P.hdr->queue.v, 1u);
+  ItemMeta cur = item_meta<GREEDY>(P, q0, item_row(P, q0, n_items), n_items);
+  unsigned q_next = q1;
+  int rid_next = item_row(P, q1, n_items);
+  unsigned long long idle_since = 0;
+  unsigned sleep_ns = 64;
+  while (ok) {
+    // one static item and one ready draw item per round: neither kind can
+    // starve the other (late target rows and early draws are both on the
+    // critical path of some request)
+    bool did = false;
+    const int peek = dyn ? ticket_peek(P, ticket) : 0;     // in flight while staging
+    if (cur.valid) {
+      // loads for the next items, issued before the (blocking) staging
+      const ItemMeta nxt = item_meta<GREEDY>(P, q_next, rid_next, n_items);
+      const int rid2 = item_row(P, q2, n_items);
+      const unsigned q3 = q2 < n_items ? atomicAdd(&P.hdr->queue.v, 1u) : q2;
+      if (cur.skip) red_add_release(P.row_arr + cur.rid, 1u + kSkipInc);
+      else ok = stage_stats_item<DT, GREEDY>(P, S, stage, phase, cur);
+      cur = nxt;
+      q_next = q2;
+      rid_next = rid2;
+      q2 = q3;
+      did = true;
+    }
+    if (ok && peek != 0) {
+      DynItem it;
+      ticket_take(P, ticket, it);
+      ticket = atomicAdd(&P.hdr->dq_head.v, 1u);
+      ok = stage_dyn_item<DT>(P, S, stage, phase, it);
+      did = true;
+    }
+    if (did) {
+      idle_since = 0;
+      sleep_ns = 64;
+      continue;
+    }
+    // nothing to stage right now: finished, or draw items are still to come
+    if (ld_relaxed_u32(&P.hdr->done.v) >= n_valid) break;
+    if (ld_relaxed_u32(&P.hdr->error.v) != 0u) break;
+    const unsigned long long now = globaltimer();
+    if (idle_since == 0) idle_since = now;
+    else if (now - idle_since > kWaitLimitNs) { ok = false; break; }
+    __nanosleep(sleep_ns);
+    if (sleep_ns < 1024) sleep_ns *= 2;
+  }
+  if (ok && wait_bar(S, &S.empty[stage], phase ^ 1u)) {
+    S.desc[stage].flags = F_TERM;
+    mbar_arrive(&S.full[stage]);
+    return;
+  }
+  // gave up: tell the other roles, then let the copies already in flight land
+  set_abort(P, S);
+  for (int s = 0; s < kStages; ++s) {
+    const uint32_t par = s < stage ? phase : phase ^ 1u;
+    const unsigned long long t0 = globaltimer();
+    while (!mbar_try_wait(&S.full[s], par) && globaltimer() - t0 < kWaitLimitNs) {
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// consumers
+
+// A direct stage (rows not 16-byte aligned): the consumers copy its elements
+// from global memory into the stage buffer, padding the last vector with -inf.
+template <int DT>
+__device__ void fill_direct(const Params& P, VSmem& S, int stage, const StageDesc& d, int tid) {
+  constexpr int N = VecT<DT>::N;
+  const unsigned char* tens = d.kind == KIND_TARGET ? P.target : P.draft;
+  const int n = d.n_elems, npad = d.nvec * N;
+  if (DT == SPEC_BF16) {
+    unsigned short* dst = reinterpret_cast<unsigned short*>(S.ring[stage]);
+    const unsigned short* src = reinterpret_cast<const unsigned short*>(tens) + d.src_elem;
+    for (int j = tid; j < npad; j += kConsumerThreads) dst[j] = j < n ? __ldg(src + j) : (unsigned short)0xff80u;
+  } else {
+    float* dst = reinterpret_cast<float*>(S.ring[stage]);
+    const float* src = reinterpret_cast<const float*>(tens) + d.src_elem;
+    for (int j = tid; j < npad; j += kConsumerThreads) dst[j] = j < n ? __ldg(src + j) : -INFINITY;
+  }
+  consumer_bar();
+}
+
+// residual weight [p - q]_+ of one element pair (the same expression
+// everywhere, so sums and the search agree term by term)
+struct ResidW {
+  float c, mpc, mqc, rp, rq;
+  __device__ __forceinline__ float operator()(float xp, float xq) const {
+    const float p = ex2(fmaf(xp, c, -mpc)) * rp;
+    const float q = ex2(fmaf(xq, c, -mqc)) * rq;
+    return fmaxf(p - q, 0.f);
+  }
+};
+
+// One search step over a staged piece of the located chunk (see the file
+// comment of the epilogue for the protocol): vector sums, an fp64 scan over
+// contiguous 4-vector groups of the 256 consumer threads, and an fp64 walk by
+// the thread whose group crosses the target.  wfun(v, w) gives the N weights
+// of vector v of the piece.
+template <int DT, class WF>
+__device__ void search_step(VSmem& S, int tid, int lane, int cw, int nvec, int elem0, double tl, WF wfun) {
+  constexpr int N = VecT<DT>::N;
+  int lastpos = -1;
+#pragma unroll
+  for (int q = 0; q < kVecPerThread; ++q) {
+    const int v = tid + q * kConsumerThreads;
+    float vsum = 0.f;
+    if (v < nvec) {
+      float w[N];
+      wfun(v, w);
+#pragma unroll
+      for (int k = 0; k < N; ++k) {
+        vsum += w[k];
+        if (w[k] > 0.f) lastpos = elem0 + v * N + k;
+      }
+    }
+    S.vs[v] = vsum;
+  }
+  if (lastpos >= 0) atomicMax(&S.last_elem, lastpos);
+  consumer_bar();
+  const float s4 = (S.vs[4 * tid] + S.vs[4 * tid + 1]) + (S.vs[4 * tid + 2] + S.vs[4 * tid + 3]);
+  double incl = (double)s4;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const double o = __shfl_up_sync(0xffffffffu, incl, d);
+    if (lane >= d) incl += o;
+  }
+  double exw = __shfl_up_sync(0xffffffffu, incl, 1);
+  if (lane == 0) exw = 0.0;
+  if (lane == 31) S.wtot[cw] = incl;
+  consumer_bar();
+  double before = S.carry, total = S.carry;
+  for (int w = 0; w < kConsumerWarps; ++w) {
+    if (w < cw) before += S.wtot[w];
+    total += S.wtot[w];
+  }
+  const double E = before + exw;
+  const int found = S.found;
+  if (!found && E + (double)s4 > tl) atomicMin(&S.found_thread, tid);
+  consumer_bar();
+  if (!found && tid == S.found_thread) {
+    double C = E, Cp = E;
+    int z = -1;
+    for (int vv = 4 * tid; vv < nvec && z < 0; ++vv) {
+      float w[N];
+      wfun(vv, w);
+      for (int k = 0; k < N; ++k) {
+        Cp = C;
+        C += (double)w[k];
+        if (C > tl) { z = elem0 + vv * N + k; break; }
+      }
+    }
+    if (z >= 0) { S.z = z; S.cprev = Cp; S.cat = C; S.found = 1; }
+  }
+  consumer_bar();
+  if (tid == 0) {
+    if (!S.found) S.carry = total;
+    S.found_thread = INT_MAX;
+  }
+}
+
+template <int DT, bool GREEDY>
+__device__ void consumer_role(const Params& P, VSmem& S, int cw, int lane) {
+  constexpr int N = VecT<DT>::N;
+  const int tid = cw * 32 + lane;
+  int stage = 0;
+  uint32_t phase = 0;
+  int seq = 0;
+  RunState r;
+  run_reset(r);
+  bool ent = false;
+  float c = 0.f, xy = qnan(), wacc = 0.f;
+  double tl = 0.0;
+  auto advance = [&]() {
+    if (++stage == kStages) { stage = 0; phase ^= 1u; }
+  };
+  auto release = [&](int st) {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&S.empty[st]);
+  };
+  // hand one finished item to the epilogue warps
+  auto to_epilogue = [&](auto write_fields) -> bool {
+    const int eslot = seq % kEpiSlots;
+    const uint32_t epar = ((uint32_t)(seq / kEpiSlots) & 1u) ^ 1u;
+    if (!wait_bar(S, &S.epi_empty[eslot], epar)) { set_abort(P, S); return false; }
+    write_fields(S.slot[eslot]);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&S.epi_full[eslot]);
+    ++seq;
+    return true;
+  };
+  while (true) {
+    if (!wait_bar(S, &S.full[stage], phase)) { set_abort(P, S); return; }
+    const StageDesc d = S.desc[stage];
+    if (d.flags & F_TERM) {
+      // every epilogue warp must see the end: mark consecutive slots
+      for (int e = 0; e < kEpiWarps; ++e) {
+        if (!to_epilogue([&](EpiSlot& E) { if (tid == 0) E.term = 1; })) return;
+      }
+      return;
+    }
+    if (d.flags & F_DIRECT) fill_direct<DT>(P, S, stage, d, tid);
+    const uint4* vec = reinterpret_cast<const uint4*>(S.ring[stage]);
+
+    if (d.type == IT_STATS) {
+      if (d.flags & F_FIRST) {
+        run_reset(r);
+        ent = !GREEDY && d.kind == KIND_DRAFT && P.signals_on;
+        c = d.c;
+        xy = qnan();
+      }
+      uint4 w[kVecPerThread];
+      load_stage<DT>(vec, d.nvec, tid, w);
+      // the logit at the draft token, if this stage holds it (one shared load)
+      if (!GREEDY && tid == 0) {
+        const int off = d.y - d.elem0;
+        if (off >= 0 && off < d.nvec * N)
+          xy = DT == SPEC_BF16 ? __uint_as_float((uint32_t)reinterpret_cast<const unsigned short*>(vec)[off] << 16)
+                               : reinterpret_cast<const float*>(vec)[off];
+      }
+      if (GREEDY) stage_argmax<DT>(r, w, d.elem0, tid);
+      else if (ent) stage_softmax<DT, true>(r, w, c);
+      else stage_softmax<DT, false>(r, w, c);
+      release(stage);
+      advance();
+      if (d.flags & F_LAST) {
+        if (tid == 0 && (d.nhead > 0 || d.ntail > 0)) {
+          const unsigned char* tens = d.kind == KIND_TARGET ? P.target : P.draft;
+          const long long row0 = row_elem_offset(d.kind, d.b, d.i, P.G, P.V);
+          for (int k = 0; k < d.nhead; ++k) {
+            const float x = load_logit(tens, DT, row0 + d.head0 + k);
+            if (d.head0 + k == d.y) xy = x;
+            run_scalar<GREEDY>(r, x, d.head0 + k, c, ent);
+          }
+          for (int k = 0; k < d.ntail; ++k) {
+            const float x = load_logit(tens, DT, row0 + d.tail0 + k);
+            if (d.tail0 + k == d.y) xy = x;
+            run_scalar<GREEDY>(r, x, d.tail0 + k, c, ent);
+          }
+        }
+        Part p;
+        if (GREEDY) {
+          p = to_part(r);
+#pragma unroll
+          for (int off = 16; off >= 1; off >>= 1) p = merge_argmax(p, shfl_part(p, off));
+        } else {
+          p = warp_softmax_part(r, c, ent);
+        }
+        if (!to_epilogue([&](EpiSlot& E) {
+              if (lane == 0) E.part[cw] = p;
+              if (tid == 0) {
+                E.type = IT_STATS; E.row_id = d.row_id; E.b = d.b; E.i = d.i; E.kind = d.kind;
+                E.chunk = d.chunk; E.xy = xy;
+              }
+            }))
+          return;
+      }
+      continue;
+    }
+
+    if (d.type == IT_RSUM) {
+      // a pair of stages: slice of row k of the target, then the same slice of
+      // the draft.  Weights [p - q]_+; fp32 sums per group of 8 consecutive
+      // vectors are stored for the search, their fp64 total is the partial.
+      const int st1 = stage;
+      advance();
+      if (!wait_bar(S, &S.full[stage], phase)) { set_abort(P, S); return; }
+      const StageDesc d2 = S.desc[stage];
+      if (d2.flags & F_DIRECT) fill_direct<DT>(P, S, stage, d2, tid);
+      const uint4* vec2 = reinterpret_cast<const uint4*>(S.ring[stage]);
+      ResidW R;
+      R.c = d.c; R.mpc = d.m1 * d.c; R.mqc = d.m2 * d.c; R.rp = 1.f / d.s1; R.rq = 1.f / d.s2;
+      uint4 wt[kVecPerThread], wd[kVecPerThread];
+      load_stage<DT>(vec, d.nvec, tid, wt);
+      load_stage<DT>(vec2, d.nvec, tid, wd);
+      float* gs_out = P.rsum_gs + ((size_t)d.b * P.nres + d.chunk) * kGroupsPerStage;
+      double dsum = 0.0;
+#pragma unroll
+      for (int q = 0; q < kVecPerThread; ++q) {
+        float xt[N], xd[N], e[N];
+        VecT<DT>::unpack(wt[q], xt);
+        VecT<DT>::unpack(wd[q], xd);
+#pragma unroll
+        for (int k = 0; k < N; ++k) e[k] = R(xt[k], xd[k]);
+        float g;
+        if (N == 8) g = ((e[0] + e[1]) + (e[2] + e[3])) + ((e[4] + e[5]) + (e[6] + e[7]));
+        else g = (e[0] + e[1]) + (e[2] + e[3]);
+        // vectors tid + 256 q of 8 consecutive threads form one group
+        g += __shfl_xor_sync(0xffffffffu, g, 1);
+        g += __shfl_xor_sync(0xffffffffu, g, 2);
+        g += __shfl_xor_sync(0xffffffffu, g, 4);
+        const int v = tid + q * kConsumerThreads;
+        if ((lane & (kGroupVecs - 1)) == 0) {
+          if (v < d.nvec) __stcg(gs_out + v / kGroupVecs, g);
+          dsum += (double)g;
+        }
+      }
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, off);
+      release(st1);
+      release(stage);
+      advance();
+      if (!to_epilogue([&](EpiSlot& E) {
+            if (lane == 0) E.dsum[cw] = dsum;
+            if (tid == 0) { E.type = IT_RSUM; E.b = d.b; E.chunk = d.chunk; E.i = d.i; }
+          }))
+        return;
+      continue;
+    }
+
+    // IT_PSUM and IT_SEARCH over p: single stages of one chunk of the target row
+    const float mc = d.m1 * d.c;
+    const int excl = d.y;
+    auto pw = [&](int v, float* w) {
+      float x[N];
+      VecT<DT>::unpack(vec[v], x);
+#pragma unroll
+      for (int k = 0; k < N; ++k) w[k] = (d.elem0 + v * N + k == excl) ? 0.f : ex2(fmaf(x[k], d.c, -mc));
+    };
+    if (d.type == IT_PSUM) {
+      if (d.flags & F_FIRST) wacc = 0.f;
+      float sv[kVecPerThread];
+#pragma unroll
+      for (int q = 0; q < kVecPerThread; ++q) {
+        const int v = tid + q * kConsumerThreads;
+        float w[N];
+        if (v < d.nvec) pw(v, w);
+        else
+#pragma unroll
+          for (int k = 0; k < N; ++k) w[k] = 0.f;
+        if (N == 8) sv[q] = ((w[0] + w[1]) + (w[2] + w[3])) + ((w[4] + w[5]) + (w[6] + w[7]));
+        else sv[q] = (w[0] + w[1]) + (w[2] + w[3]);
+      }
+      wacc += (sv[0] + sv[1]) + (sv[2] + sv[3]);
+      release(stage);
+      advance();
+      if (d.flags & F_LAST) {
+        float s = wacc;
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+        if (!to_epilogue([&](EpiSlot& E) {
+              if (lane == 0) E.wsum[cw] = s;
+              if (tid == 0) { E.type = IT_PSUM; E.b = d.b; E.chunk = d.chunk; E.i = d.i; }
+            }))
+          return;
+      }
+      continue;
+    }
+    // IT_SEARCH over p
+    if (d.flags & F_FIRST) {
+      if (tid == 0) {
+        S.carry = 0.0; S.found = 0; S.z = -1; S.last_elem = -1; S.found_thread = INT_MAX;
+      }
+      tl = __ldcg(&P.search[d.b].tl);
+      consumer_bar();
+    }
+    if (!S.found) search_step<DT>(S, tid, lane, cw, d.nvec, d.elem0, tl, pw);
+    consumer_bar();
+    const int found = S.found;
+    release(stage);
+    advance();
+    if (d.flags & F_LAST) {
+      const int z = found ? S.z : S.last_elem;
+      const float margin = found ? (float)fmin(tl - S.cprev, S.cat - tl) : 0.f;
+      if (!to_epilogue([&](EpiSlot& E) {
+            if (tid == 0) { E.type = IT_SEARCH; E.b = d.b; E.z = z; E.margin = margin; }
+          }))
+        return;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// epilogue: request bookkeeping
+
+// Acceptance test of position i of request b, both rows complete (tutorial
+// page, sections 3.1-3.3), in fp32 on the fp32 row statistics:
+//   p(y) = 2^{(x_y - m_p) c} / s_p,  q(y) likewise (1 for one-hot q),
+//   accept <=> u q(y) < p(y),  a = min(1, p(y)/q(y)).
+// A test closer than 1e-5 (relative) to its threshold is counted and does not
+// stop the reading of later rows.  Returns the position code.
+template <bool GREEDY>
+__device__ int evaluate_position(const Params& P, int b, int i) {
+  const int G = P.G, V = P.V;
+  const int tid_t = target_row_id(b, i, G);
+  const RowStats tr = ldcg_stats(P.row_stats + tid_t);
+  const int y = P.draft_tokens[(size_t)b * G + i];
+  int code;
+  float a = qnan();
+  if (GREEDY) {
+    if (!row_ok(tr, true)) code = PC_NONFINITE;
+    else if (y < 0 || y >= V) code = PC_BAD_TOKEN;
+    else code = (y == (tr.idx & ~kIdxNaN)) ? PC_ACCEPT : PC_REJECT;
+  } else {
+    const bool sample = P.mode == MODE_SAMPLE;
+    const int did = draft_row_id(b, i, P.B, G);
+    const float u = P.uniforms[(size_t)b * (G + 1) + i];
+    const float c = scale_of(P.temperature[b]);
+    const float xt = __ldcg(P.row_xy + tid_t);
+    RowStats dr{};
+    float xd = 0.f;
+    if (sample) {
+      dr = ldcg_stats(P.row_stats + did);
+      xd = __ldcg(P.row_xy + did);
+    }
+    if (!row_ok(tr, false) || (sample && !row_ok(dr, false))) code = PC_NONFINITE;
+    else if (y < 0 || y >= V) code = PC_BAD_TOKEN;
+    else if (!(u >= 0.f && u < 1.f)) code = PC_BAD_UNIFORM;
+    else {
+      const float py = ex2((xt - tr.m) * c) / tr.s;
+      const float qy = sample ? ex2((xd - dr.m) * c) / dr.s : 1.f;
+      const float uq = u * qy;
+      code = uq < py ? PC_ACCEPT : PC_REJECT;
+      a = qy > 0.f ? fminf(1.f, py / qy) : (py > 0.f ? 1.f : 0.f);
+      if (fabsf(uq - py) <= 1e-5f * fmaxf(uq, py)) {
+        code |= PC_UNCERTAIN;
+        atomicAdd(&HDR_UNCERTAIN(P.hdr), 1u);
+      }
+    }
+  }
+  __stcg(P.pair_res + (size_t)b * (G + 1) + i, code);
+  __stcg(P.pair_a + (size_t)b * (G + 1) + i, a);
+  if (code != PC_ACCEPT && !(code & PC_UNCERTAIN)) atomicMin(P.known_reject + b, i);
+  return code & 15;
+}
+
+// Is the first reject k of a request known from its state word?  Positions
+// 0..k-1 evaluated and accepted, and k evaluated and not accepted; or all
+// gamma positions accepted and the bonus row complete.
+__device__ __forceinline__ bool k_known(unsigned long long s, int gam) {
+  const unsigned E = (unsigned)s & 0x7fffffffu;
+  const unsigned A = (unsigned)(s >> 32) & 0x7fffffffu;
+  const int j = __ffs(~(E & A)) - 1;
+  if (j < gam) return (E >> j) & 1u;
+  return (s & kBonusBit) != 0ull;
+}
+
+__device__ __forceinline__ int status_of_code(int code) {
+  return code == PC_NONFINITE ? SPEC_ST_NONFINITE
+       : code == PC_BAD_TOKEN ? SPEC_ST_BAD_TOKEN
+       : code == PC_BAD_UNIFORM ? SPEC_ST_BAD_UNIFORM : SPEC_ST_TIMEOUT;
+}
+
+__device__ __forceinline__ void finish_request(const Params& P, int b, int st, int lane) {
+  __syncwarp();
+  if (lane == 0) {
+    __stcg(P.req_status + b, st | kFinished);
+    atomicAdd(&P.hdr->done.v, 1u);
+  }
+}
+
+// Outputs of a settled request (warp-wide): committed tokens y_0..y_{k-1}
+// then z, accept_prob for positions <= k, the SpecKV signals from the draft
+// rows' statistics (H = log2 s - t/s bits, c = 1/s; tutorial-independent,
+// SpecKV page), status.
+__device__ void write_outputs(const Params& P, int b, int st, int k, int z, int lane) {
+  const int G = P.G, gam = gamma_of(P, b);
+  if (st & kVoidMask) {
+    write_void_outputs(P, b, st, lane, 32);
+    finish_request(P, b, st, lane);
+    return;
+  }
+  if (P.mode != MODE_SIGNALS) {
+    for (int j = lane; j <= G; j += 32)
+      P.tokens[(size_t)b * (G + 1) + j] = j < k ? P.draft_tokens[(size_t)b * G + j] : (j == k ? z : -1);
+    if (P.accept_prob)
+      for (int j = lane; j < G; j += 32)
+        P.accept_prob[(size_t)b * G + j] = (j < gam && j <= k) ? __ldcg(P.pair_a + (size_t)b * (G + 1) + j) : qnan();
+    if (lane == 0) P.accept_len[b] = k;
+  }
+  if (P.signals_on && (P.signals || P.row_signals)) {
+    double H = 0.0, cf = 0.0;
+    const bool in = lane < gam;
+    if (in) {
+      const RowStats r = ldcg_stats(P.row_stats + draft_row_id(b, lane, P.B, G));
+      const double s = (double)r.s;
+      H = (double)log2f(r.s) - (double)r.t / s;
+      cf = 1.0 / s;
+    }
+    if (P.row_signals && lane < G) {
+      float* rs = P.row_signals + ((size_t)b * G + lane) * 2;
+      rs[0] = in ? (float)H : qnan();
+      rs[1] = in ? (float)cf : qnan();
+    }
+    double hs = H, cs = cf, hm = in ? H : -INFINITY, cm = in ? cf : INFINITY;
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+      hs += __shfl_xor_sync(0xffffffffu, hs, off);
+      cs += __shfl_xor_sync(0xffffffffu, cs, off);
+      hm = fmax(hm, __shfl_xor_sync(0xffffffffu, hm, off));
+      cm = fmin(cm, __shfl_xor_sync(0xffffffffu, cm, off));
+    }
+    if (lane == 0 && P.signals) {
+      float* sg = P.signals + (size_t)b * 4;
+      if (gam > 0) {
+        sg[0] = (float)(hs / gam); sg[1] = (float)hm; sg[2] = (float)(cs / gam); sg[3] = (float)cm;
+      } else {
+        sg[0] = sg[1] = sg[2] = sg[3] = qnan();
+      }
+    }
+  }
+  if (lane == 0 && P.status) P.status[b] = st;
+  finish_request(P, b, st, lane);
+}
+
+// The output of a request is written once two things are known: the result
+// of its draw (first reject k, committed token z, or an error found on the
+// way) and, when signals are requested, every draft row's statistics.  A
+// counter per request counts the conditions met; whoever meets the last one
+// writes the outputs.
+__device__ __forceinline__ unsigned conditions_needed(const Params& P) {
+  return (P.mode == MODE_SIGNALS ? 0u : 1u) + (P.signals_on ? 1u : 0u);
+}
+
+// All conditions met: the outputs of request b (warp-wide).  The signal rows
+// are checked first, as the method reads them before the positions.
+__device__ void finalize_outputs(const Params& P, int b, int lane) {
+  const int G = P.G, gam = gamma_of(P, b);
+  if (P.signals_on) {
+    bool bad = false;
+    if (lane < gam) bad = !row_ok(ldcg_stats(P.row_stats + draft_row_id(b, lane, P.B, G)), false);
+    if (__ballot_sync(0xffffffffu, bad)) { write_outputs(P, b, SPEC_ST_NONFINITE, 0, -1, lane); return; }
+  }
+  if (P.mode == MODE_SIGNALS) { write_outputs(P, b, 0, 0, -1, lane); return; }
+  write_outputs(P, b, __ldcg(P.req_status + b), __ldcg(P.req_k + b), __ldcg(P.req_z + b), lane);
+}
+
+// One condition of request b is met (lane 0 decides; warp-wide call).
+__device__ __forceinline__ void condition_met(const Params& P, int b, int lane) {
+  bool last = false;
+  if (lane == 0) {
+    const unsigned o = atom_add_acqrel(P.req_cnt + 2 * b + 1, 1u);
+    last = o + 1u == conditions_needed(P);
+  }
+  if (__shfl_sync(0xffffffffu, last, 0)) finalize_outputs(P, b, lane);
+}
+
+// The draw of request b is settled: error bits st (0 if none), first reject
+// k, committed token z.  Warp-wide.
+__device__ void draw_done(const Params& P, int b, int st, int k, int z, int lane) {
+  if (lane == 0) {
+    __stcg(P.req_status + b, st);
+    __stcg(P.req_k + b, k);
+    __stcg(P.req_z + b, z);
+  }
+  __syncwarp();
+  condition_met(P, b, lane);
+}
+
+// Warp-wide: among n non-negative weights get(0..n-1) in order, the first j
+// whose prefix (fp64, fixed association) plus weight exceeds t, with the
+// prefix before it; when none does, the last j of positive weight (-1 if
+// none).  *total = the sum of all weights.
+template <class Get>
+__device__ int warp_locate(int n, Get get, double t, double* before, double* total, int lane) {
+  double carry = 0.0, fb = 0.0, lb = 0.0;
+  int found = -1, lastpos = -1;
+  for (int base = 0; base < n; base += 32) {
+    const int j = base + lane;
+    const double v = j < n ? get(j) : 0.0;
+    double incl = v;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const double o = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += o;
+    }
+    double ex = __shfl_up_sync(0xffffffffu, incl, 1);
+    if (lane == 0) ex = 0.0;
+    ex += carry;
+    const unsigned cross = __ballot_sync(0xffffffffu, j < n && ex + v > t);
+    const unsigned pos = __ballot_sync(0xffffffffu, j < n && v > 0.0);
+    if (found < 0 && cross) {
+      const int f = __ffs(cross) - 1;
+      found = base + f;
+      fb = __shfl_sync(0xffffffffu, ex, f);
+    }
+    if (pos) {
+      const int l = 31 - __clz(pos);
+      lastpos = base + l;
+      lb = __shfl_sync(0xffffffffu, ex, l);
+    }
+    carry += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  *total = carry;
+  if (found >= 0) { *before = fb; return found; }
+  *before = lb;
+  return lastpos;
+}
+
+// Locate the chunk of the draw from p_k (target row k of request b): chunk
+// weights from the statistics partials (unnormalised p), the chunk holding
+// the excluded token (one-hot residual) replaced by its fresh sum sy; then
+// create the search item.  Warp-wide.
+template <int DT>
+__device__ void locate_p(const Params& P, int b, int k, int excl, int cy, double sy, int st, int lane) {
+  const int G = P.G, nch = P.nch, ce = chunk_elems(DT);
+  const int rid = target_row_id(b, k, G);
+  const RowStats rs = ldcg_stats(P.row_stats + rid);
+  const float c = scale_of(P.temperature[b]);
+  const Part* parts = P.parts + (size_t)rid * nch;
+  auto get = [&](int j) -> double {
+    if (j == cy) return sy;
+    const Part q = ldcg_part(parts + j);
+    if (!(q.s > 0.f)) return 0.0;
+    return (double)(q.s * ex2((q.m - rs.m) * c));
+  };
+  double before, W;
+  warp_locate(nch, get, INFINITY, &before, &W, lane);
+  if (!(W > 0.0)) {
+    if (excl >= 0) {        // rounding left no mass besides y: draw from p itself
+      locate_p<DT>(P, b, k, -1, -1, 0.0, st | SPEC_ST_ZERO_RESIDUAL, lane);
+      return;
+    }
+    draw_done(P, b, SPEC_ST_TIMEOUT, 0, -1, lane);   // a complete row always has mass
+    return;
+  }
+  const float ud = P.uniforms[(size_t)b * (G + 1) + G];
+  const double t = (double)ud * W;
+  double tot;
+  const int cs = warp_locate(nch, get, t, &before, &tot, lane);
+  if (lane == 0) {
+    SearchDesc* sd = P.search + b;
+    __stcg(&sd->tl, t - before);
+    __stcg(&sd->W, W);
+    __stcg(&sd->kind, (int)SK_P);
+    __stcg(&sd->e0, cs * ce);
+    __stcg(&sd->e1, min(cs * ce + ce, P.V));
+    __stcg(&sd->excl, excl);
+    __stcg(&sd->status, st);
+    __stcg(&sd->row_t, rid);
+    __stcg(&sd->row_d, -1);
+  }
+  enqueue_items(P, 1, IT_SEARCH, b, 0, 0, lane);
+}
+
+// All residual slices of request b are summed: the draw (warp-wide).  The
+// slice is located by the fp64 prefix of the slice sums, the 64-token group
+// inside it by the fp64 prefix of the stored group sums, and the token by an
+// fp64 walk over the group's recomputed weights (two 128-byte loads, from
+// L2).  If rounding leaves no crossing in the group, the last weighted token
+// of the group is taken (a margin of 0 is counted as a near tie).
+template <int DT>
+__device__ void locate_resid(const Params& P, int b, int lane) {
+  constexpr int N = VecT<DT>::N;
+  constexpr int GE = kGroupVecs * N;                 // tokens per group (64 bf16 / 32 fp32)
+  const int G = P.G, V = P.V, nres = P.nres, se = stage_elems(DT);
+  const int k = __ldcg(P.req_k + b);
+  const double* parts = P.rsum_parts + (size_t)b * nres;
+  auto get = [&](int j) -> double { return __ldcg(parts + j); };
+  double before, W;
+  warp_locate(nres, get, INFINITY, &before, &W, lane);
+  if (!(W > 0.0)) {         // residual mass rounded to zero: draw from p_k
+    locate_p<DT>(P, b, k, -1, -1, 0.0, SPEC_ST_ZERO_RESIDUAL, lane);
+    return;
+  }
+  const float ud = P.uniforms[(size_t)b * (G + 1) + G];
+  const double t = (double)ud * W;
+  double tot;
+  const int cs = warp_locate(nres, get, t, &before, &tot, lane);
+  const int e0 = cs * se, e1 = min(e0 + se, V);
+  const int ngroups = (e1 - e0 + GE - 1) / GE;
+  const float* gsum = P.rsum_gs + ((size_t)b * nres + cs) * kGroupsPerStage;
+  auto gget = [&](int j) -> double { return (double)__ldcg(gsum + j); };
+  double gbefore;
+  const int g = warp_locate(ngroups, gget, t - before, &gbefore, &tot, lane);
+  const double tl = t - before - gbefore;
+  // the group's tokens: lane l takes tokens 2l, 2l+1 (bf16) or l (fp32)
+  const RowStats tr = ldcg_stats(P.row_stats + target_row_id(b, k, G));
+  const RowStats dr = ldcg_stats(P.row_stats + draft_row_id(b, k, P.B, G));
+  ResidW R;
+  R.c = scale_of(P.temperature[b]);
+  R.mpc = tr.m * R.c; R.mqc = dr.m * R.c; R.rp = 1.f / tr.s; R.rq = 1.f / dr.s;
+  const long long trow = row_elem_offset(KIND_TARGET, b, k, G, V), drow = row_elem_offset(KIND_DRAFT, b, k, G, V);
+  constexpr int PER = GE / 32;
+  float w[PER];
+  const int g0 = e0 + g * GE;
+  double mine = 0.0;
+#pragma unroll
+  for (int u = 0; u < PER; ++u) {
+    const int e = g0 + lane * PER + u;
+    w[u] = e < e1 ? R(load_logit(P.target, DT, trow + e), load_logit(P.draft, DT, drow + e)) : 0.f;
+    mine += (double)w[u];
+  }
+  double incl = mine;
+#pragma unroll
+  for (int dd = 1; dd < 32; dd <<= 1) {
+    const double o = __shfl_up_sync(0xffffffffu, incl, dd);
+    if (lane >= dd) incl += o;
+  }
+  const double ex = incl - mine;
+  const unsigned cross = __ballot_sync(0xffffffffu, ex + mine > tl);
+  int z = -1;
+  double margin = 0.0;
+  if (cross) {
+    const int f = __ffs(cross) - 1;
+    if (lane == f) {
+      double C = ex, Cp = ex;
+      for (int u = 0; u < PER; ++u) {
+        Cp = C;
+        C += (double)w[u];
+        if (C > tl) { z = g0 + lane * PER + u; break; }
+      }
+      if (z < 0) {         // rounding between the lane sum and its terms
+        for (int u = PER - 1; u >= 0; --u)
+          if (w[u] > 0.f) { z = g0 + lane * PER + u; break; }
+      } else {
+        margin = fmin(tl - Cp, C - tl);
+      }
+    }
+    z = __shfl_sync(0xffffffffu, z, f);
+    margin = __shfl_sync(0xffffffffu, margin, f);
+  } else {
+    const unsigned pos = __ballot_sync(0xffffffffu, mine > 0.0);
+    if (pos) {
+      const int l = 31 - __clz(pos);
+      int zz = -1;
+      if (lane == l)
+        for (int u = PER - 1; u >= 0; --u)
+          if (w[u] > 0.f) { zz = g0 + lane * PER + u; break; }
+      z = __shfl_sync(0xffffffffu, zz, l);
+    }
+  }
+  if (lane == 0 && !(margin >= (double)kDrawGuard * W)) atomicAdd(&HDR_UNCERTAIN(P.hdr), 1u);
+  draw_done(P, b, z >= 0 ? 0 : SPEC_ST_TIMEOUT, k, z, lane);
+}
+
+// The first reject k of request b is known: settle its draw, or create the
+// draw items.  Warp-wide.  Errors are taken in the method's order: positions
+// in order, then the bonus row, then the draw's uniform.
+template <int DT, bool GREEDY>
+__device__ void dispatch_draw(const Params& P, int b, int lane) {
+  const int G = P.G, gam = gamma_of(P, b);
+  const unsigned long long s = __ldcg(P.req_state + b);
+  const unsigned E = (unsigned)s & 0x7fffffffu, A = (unsigned)(s >> 32) & 0x7fffffffu;
+  const int j = __ffs(~(E & A)) - 1;
+  int k = gam;
+  bool rejected = false;
+  if (j < gam) {
+    const int code = __ldcg(P.pair_res + (size_t)b * (G + 1) + j) & 15;
+    if (code != PC_REJECT) { draw_done(P, b, status_of_code(code), 0, -1, lane); return; }
+    k = j;
+    rejected = true;
+  } else if (!row_ok(ldcg_stats(P.row_stats + target_row_id(b, gam, G)), GREEDY)) {
+    draw_done(P, b, SPEC_ST_NONFINITE, 0, -1, lane);
+    return;
+  }
+  if (GREEDY) {
+    const int z = ldcg_stats(P.row_stats + target_row_id(b, k, G)).idx & ~kIdxNaN;
+    draw_done(P, b, 0, k, z, lane);
+    return;
+  }
+  const float ud = P.uniforms[(size_t)b * (G + 1) + G];
+  if (!(ud >= 0.f && ud < 1.f)) { draw_done(P, b, SPEC_ST_BAD_UNIFORM, 0, -1, lane); return; }
+  if (lane == 0) __stcg(P.req_k + b, k);
+  __syncwarp();
+  if (rejected && P.mode == MODE_SAMPLE) {
+    enqueue_items(P, P.nres, IT_RSUM, b, 0, k, lane);
+  } else if (rejected) {
+    const int y = P.draft_tokens[(size_t)b * G + k];
+    enqueue_items(P, 1, IT_PSUM, b, y / chunk_elems(DT), k, lane);
+  } else {
+    locate_p<DT>(P, b, k, -1, -1, 0.0, 0, lane);
+  }
+}
+
+// A row of request b is complete (its statistics are published): record the
+// events it causes.  Warp-wide.
+template <int DT, bool GREEDY>
+__device__ void row_events(const Params& P, int b, int i, int kind, int lane) {
+  const int G = P.G, gam = gamma_of(P, b);
+  bool k_now = false, sig_now = false;
+  if (lane == 0) {
+    if (P.mode != MODE_SIGNALS) {
+      unsigned long long bits = 0ull;
+      if (i < gam) {
+        const unsigned pneed = P.mode == MODE_SAMPLE ? 2u : (kind == KIND_TARGET ? 1u : 0u);
+        if (pneed > 0u) {
+          const unsigned o2 = atom_add_acqrel(P.pair_arr + (size_t)b * (G + 1) + i, 1u);
+          if (o2 + 1u == pneed) {
+            const int code = evaluate_position<GREEDY>(P, b, i);
+            bits = (1ull << i) | (code == PC_ACCEPT ? (1ull << (32 + i)) : 0ull);
+          }
+        }
+      } else if (kind == KIND_TARGET && i == gam) {
+        bits = kBonusBit;
+      }
+      if (bits) {
+        const unsigned long long old = atom_or_acqrel_u64(P.req_state + b, bits);
+        k_now = !k_known(old, gam) && k_known(old | bits, gam);
+      }
+    }
+    if (kind == KIND_DRAFT && P.signals_on) {
+      const unsigned o = atom_add_acqrel(P.req_cnt + 2 * b, 1u);
+      sig_now = (int)o + 1 == gam;
+    }
+  }
+  if (__shfl_sync(0xffffffffu, k_now, 0)) dispatch_draw<DT, GREEDY>(P, b, lane);
+  if (__shfl_sync(0xffffffffu, sig_now, 0)) condition_met(P, b, lane);
+}
+
+// Epilogue warp e handles the items with sequence number = e (mod kEpiWarps).
+template <int DT, bool GREEDY>
+__device__ void epilogue_role(const Params& P, VSmem& S, int lane, int e) {
+  const int G = P.G, nch = P.nch;
+  for (int seq = e;; seq += kEpiWarps) {
+    const int eslot = seq % kEpiSlots;
+    const uint32_t epar = (uint32_t)(seq / kEpiSlots) & 1u;
+    if (!wait_bar(S, &S.epi_full[eslot], epar)) { set_abort(P, S); return; }
+    const EpiSlot& E = S.slot[eslot];
+    if (E.term) return;
+    const int type = E.type, rid = E.row_id, b = E.b, i = E.i, kind = E.kind, chunk = E.chunk;
+    const float xy = E.xy, margin = E.margin;
+    const int z = E.z;
+    Part p = lane < kConsumerWarps ? E.part[lane] : empty_part();
+    double ws = 0.0;
+    if (lane == 0) {
+      if (type == IT_RSUM)
+        for (int w = 0; w < kConsumerWarps; ++w) ws += E.dsum[w];
+      else
+        for (int w = 0; w < kConsumerWarps; ++w) ws += (double)E.wsum[w];
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&S.epi_empty[eslot]);
+
+    if (type == IT_RSUM) {
+      bool last = false;
+      if (lane == 0) {
+        __stcg(P.rsum_parts + (size_t)b * P.nres + chunk, ws);
+        __threadfence();   // the consumers' group sums, before the count
+        const unsigned o = atom_add_acqrel(P.rsum_arr + b, 1u);
+        last = o + 1u == (unsigned)P.nres;
+      }
+      if (__shfl_sync(0xffffffffu, last, 0)) locate_resid<DT>(P, b, lane);
+      continue;
+    }
+    if (type == IT_PSUM) {
+      ws = __shfl_sync(0xffffffffu, ws, 0);
+      const int k = __ldcg(P.req_k + b);
+      locate_p<DT>(P, b, k, P.draft_tokens[(size_t)b * G + k], chunk, ws, 0, lane);
+      continue;
+    }
+    if (type == IT_SEARCH) {
+      const SearchDesc* sd = P.search + b;
+      const double W = __ldcg(&sd->W);
+      const int st = __ldcg(&sd->status);
+      if (lane == 0 && !((double)margin >= kDrawGuard * W)) atomicAdd(&HDR_UNCERTAIN(P.hdr), 1u);
+      draw_done(P, b, z >= 0 ? st : SPEC_ST_TIMEOUT, __ldcg(P.req_k + b), z, lane);
+      continue;
+    }
+
+    // IT_STATS: publish the chunk partial; the CTA completing the row merges it
+    const bool ent = !GREEDY && kind == KIND_DRAFT && P.signals_on;
+    const float c = GREEDY ? 0.f : scale_of(P.temperature[b]);
+#pragma unroll
+    for (int off = 4; off >= 1; off >>= 1) {
+      const Part o = shfl_part(p, off);
+      p = GREEDY ? merge_argmax(p, o) : merge_parts(p, o, c, ent);
+    }
+    unsigned old = 0;
+    if (lane == 0) {
+      stcg_part(P.parts + (size_t)rid * nch + chunk, p);
+      if (!(xy != xy)) __stcg(P.row_xy + rid, xy);
+      old = atom_add_acqrel(P.row_arr + rid, 1u);   // release: the partial before the count
+    }
+    old = __shfl_sync(0xffffffffu, old, 0);
+    if (((old + 1u) & kCountMask) == (unsigned)nch && (old >> 20) == 0u) {
+      Part r = empty_part();
+      for (int k = lane; k < nch; k += 32) {
+        const Part q = ldcg_part(P.parts + (size_t)rid * nch + k);
+        r = GREEDY ? merge_argmax(r, q) : merge_parts(r, q, c, ent);
+      }
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) {
+        const Part o = shfl_part(r, off);
+        r = GREEDY ? merge_argmax(r, o) : merge_parts(r, o, c, ent);
+      }
+      if (lane == 0) {
+        stcg_part(reinterpret_cast<Part*>(P.row_stats + rid), r);
+        __stcg(P.row_done + rid, 1);
+      }
+      __syncwarp();
+      row_events<DT, GREEDY>(P, b, i, kind, lane);
+    }
+  }
+}
+
+}  // namespace
+
+template <int DT, bool GREEDY>
+__global__ void __launch_bounds__(kStatsThreads, 2) verify_kernel(Params P) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  VSmem& S = *reinterpret_cast<VSmem*>(smem_raw);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&S.full[s], 1);
+      mbar_init(&S.empty[s], kConsumerWarps);
+    }
+    for (int e = 0; e < kEpiSlots; ++e) {
+      mbar_init(&S.epi_full[e], kConsumerWarps);
+      mbar_init(&S.epi_empty[e], 1);
+      S.slot[e].term = 0;
+    }
+    S.abort = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  griddep_wait();   // the plan kernel's schedule and counters are ready
+  if (warp < kConsumerWarps) consumer_role<DT, GREEDY>(P, S, warp, lane);
+  else if (warp == kConsumerWarps) {
+    if (lane == 0) producer_role<DT, GREEDY>(P, S);
+  } else epilogue_role<DT, GREEDY>(P, S, lane, warp - kConsumerWarps - 1);
+  __syncthreads();
+  // the last CTA out voids any request an aborted wait left unfinished
+  if (threadIdx.x == 0) {
+    const unsigned ex = atomicAdd(&HDR_EXITED(P.hdr), 1u) + 1u;
+    if (ex == gridDim.x && ld_relaxed_u32(&P.hdr->error.v) != 0u) {
+      __threadfence();
+      for (int b = 0; b < P.B; ++b)
+        if (!(__ldcg(P.req_status + b) & kFinished)) write_void_outputs(P, b, SPEC_ST_TIMEOUT, 0, 1);
+    }
+  }
+}
+
+static size_t verify_smem_bytes() { return sizeof(VSmem); }
+
+cudaError_t configure_kernels() {
+  const int smem = (int)verify_smem_bytes();
+  cudaError_t e = cudaFuncSetAttribute(verify_kernel<SPEC_F32, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(verify_kernel<SPEC_F32, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(verify_kernel<SPEC_BF16, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(verify_kernel<SPEC_BF16, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  return e;
+}
+
+cudaError_t launch_plan(const Params& P, cudaStream_t s) {
+  return launch_ex(plan_kernel, dim3(1), dim3(1024), 0, s, false, P);
+}
+
+cudaError_t launch_verify(const Params& P, int grid, cudaStream_t s, bool pdl) {
+  const bool greedy = P.mode == MODE_GREEDY;
+  void (*k)(Params) = P.dtype == SPEC_BF16 ? (greedy ? verify_kernel<SPEC_BF16, true> : verify_kernel<SPEC_BF16, false>)
+                                           : (greedy ? verify_kernel<SPEC_F32, true> : verify_kernel<SPEC_F32, false>);
+  return launch_ex(k, dim3(grid), dim3(kStatsThreads), verify_smem_bytes(), s, pdl, P);
+}
+
+}  // namespace sv
