@@ -134,6 +134,8 @@ int run(const Call& c) {
   P.pair_arr = reinterpret_cast<unsigned*>(ws + L.pair_arr);
   P.pair_res = reinterpret_cast<int*>(ws + L.pair_res);
   P.pair_a = reinterpret_cast<float*>(ws + L.pair_a);
+  P.req_scale = reinterpret_cast<float*>(ws + L.req_scale);
+  P.req_gam = reinterpret_cast<int*>(ws + L.req_gam);
   P.req_state = reinterpret_cast<unsigned long long*>(ws + L.req_state);
   P.req_cnt = reinterpret_cast<unsigned*>(ws + L.req_cnt);
   P.req_k = reinterpret_cast<int*>(ws + L.req_k);
@@ -142,7 +144,7 @@ int run(const Call& c) {
   P.rsum_arr = reinterpret_cast<unsigned*>(ws + L.rsum_arr);
   P.rsum_parts = reinterpret_cast<double*>(ws + L.rsum_parts);
   P.rsum_gs = reinterpret_cast<float*>(ws + L.rsum_gs);
-  P.search = reinterpret_cast<SearchDesc*>(ws + L.search);
+  P.search = reinterpret_cast<DrawDesc*>(ws + L.search);
   P.dq = reinterpret_cast<DynItem*>(ws + L.dq);
   P.nrows = L.nrows; P.nch = L.nch; P.nres = L.nres; P.dq_cap = L.dq_cap;
   P.aligned_rows = ((size_t)c.V * es) % 16 == 0 && aligned(c.target, 16) && aligned(c.draft, 16);

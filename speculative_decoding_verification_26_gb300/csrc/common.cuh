@@ -30,13 +30,12 @@ constexpr int PC_UNCERTAIN = 16;   // or-ed in: |u - a| inside the guard band
 // work items of the persistent kernel
 enum ItemType : int {
   IT_STATS = 1,    // 64 KB chunk of one logit row: softmax statistics
-  IT_RSUM = 2,     // one stage of rows k of both models: sum of [p - q]_+
-  IT_PSUM = 3,     // one statistics chunk of the target row k: sum of p without y
-  IT_SEARCH = 4,   // inverse-CDF search inside one located chunk, then outputs
+  IT_DSUM = 2,     // one 16 KB slice of the draw's weights: group sums
 };
 
-// search kinds
-enum SearchKind : int { SK_P = 0, SK_RESID = 1 };
+// draw kinds: the residual [p_k - q_k]_+ (rows k of both models), or p of
+// target row k (bonus draw; one-hot residual with the draft token removed)
+enum DrawKind : int { DK_RESID = 1, DK_P = 2 };
 
 // state word bits of a request: bit i (< 31) position i evaluated, bit 32+i
 // position i accepted, bit 63 the bonus row complete
@@ -47,12 +46,12 @@ constexpr unsigned long long kBonusBit = 1ull << 63;
 
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
-constexpr int kEpiWarps = 2;                           // epilogue warps (items alternate)
+constexpr int kEpiWarps = 3;                           // epilogue warps (items alternate)
 constexpr int kStatsThreads = kConsumerThreads + 32 * (1 + kEpiWarps);   // + producer + epilogue warps
 constexpr int kStageBytes = 16384;                      // one bulk copy
 constexpr int kStages = 6;                              // ring depth per CTA
 constexpr int kChunkBytes = 4 * kStageBytes;            // one work item of a row
-constexpr int kEpiSlots = 8;                            // consumer -> epilogue ring
+constexpr int kEpiSlots = 12;                           // consumer -> epilogue ring (multiple of kEpiWarps)
 constexpr int kGroupVecs = 8;                           // residual group: 8 vectors (64 bf16 / 32 fp32 tokens)
 constexpr int kGroupsPerStage = kStageBytes / 16 / kGroupVecs;   // 128
 constexpr uint32_t kSkipInc = 1u << 20;                 // arrival mark of a skipped chunk
@@ -80,7 +79,7 @@ struct alignas(16) RowStats {
 
 struct Layout {
   size_t hdr, req_flags, known_reject, row_list, row_arr, row_done, row_stats, row_xy, parts, pair_arr,
-      pair_res, pair_a, req_state, req_cnt, req_k, req_status, req_z, rsum_arr, rsum_parts, rsum_gs, search, dq,
+      pair_res, pair_a, req_scale, req_gam, req_state, req_cnt, req_k, req_status, req_z, rsum_arr, rsum_parts, rsum_gs, search, dq,
       total;
   int nrows;      // B*(G+1) + B*G row ids
   int nch;        // statistics chunks per row
@@ -113,16 +112,12 @@ struct alignas(16) DynItem {
   int type, b, c, aux;
 };
 
-// where the final draw of a request searches (written before its IT_SEARCH item)
-struct alignas(16) SearchDesc {
-  double tl;       // target cumulative weight, relative to the chunk start
-  double W;        // total weight of the draw
-  int kind;        // SK_P or SK_RESID
-  int e0, e1;      // element range of the located chunk
+// the draw of a request (written before its IT_DSUM items)
+struct alignas(16) DrawDesc {
+  int kind;        // DK_RESID or DK_P
+  int k;           // position of the draw (first reject, or gamma_b)
   int excl;        // token left out (one-hot residual), or -1
-  int status;      // informational status bits gathered so far
-  int row_t, row_d;
-  int pad;
+  int status;      // informational status bits (SPEC_ST_ZERO_RESIDUAL)
 };
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -137,7 +132,7 @@ __host__ inline Layout make_layout(int B, int G, int V, int dtype) {
   L.nrows = nrows;
   L.nch = (V + ce - 1) / ce;
   L.nres = (V + se - 1) / se;
-  L.dq_cap = B * (L.nres + 2);
+  L.dq_cap = B * (2 * L.nres + 2);   // a draw restarted once after zero mass
   size_t o = 0;
   L.hdr = o;          o = align256(o + sizeof(Header));
   L.req_flags = o;    o = align256(o + sizeof(int) * B);
@@ -151,6 +146,8 @@ __host__ inline Layout make_layout(int B, int G, int V, int dtype) {
   L.pair_arr = o;     o = align256(o + sizeof(unsigned) * B * (G + 1));
   L.pair_res = o;     o = align256(o + sizeof(int) * B * (G + 1));
   L.pair_a = o;       o = align256(o + sizeof(float) * B * (G + 1));
+  L.req_scale = o;    o = align256(o + sizeof(float) * B);
+  L.req_gam = o;      o = align256(o + sizeof(int) * B);
   L.req_state = o;    o = align256(o + sizeof(unsigned long long) * B);
   L.req_cnt = o;      o = align256(o + sizeof(unsigned) * 2 * B);
   L.req_k = o;        o = align256(o + sizeof(int) * B);
@@ -159,7 +156,7 @@ __host__ inline Layout make_layout(int B, int G, int V, int dtype) {
   L.rsum_arr = o;     o = align256(o + sizeof(unsigned) * B);
   L.rsum_parts = o;   o = align256(o + sizeof(double) * (size_t)B * L.nres);
   L.rsum_gs = o;      o = align256(o + sizeof(float) * (size_t)B * L.nres * kGroupsPerStage);
-  L.search = o;       o = align256(o + sizeof(SearchDesc) * B);
+  L.search = o;       o = align256(o + sizeof(DrawDesc) * B);
   L.dq = o;           o = align256(o + sizeof(DynItem) * (size_t)L.dq_cap);
   L.total = o;
   return L;
@@ -196,6 +193,8 @@ struct Params {
   unsigned* pair_arr;
   int* pair_res;
   float* pair_a;
+  float* req_scale;              // log2(e) / T_b (plan kernel)
+  int* req_gam;                  // gamma_b (plan kernel)
   unsigned long long* req_state;
   unsigned* req_cnt;             // [B][2]: draft rows complete, conditions met
   int* req_k;
@@ -204,7 +203,7 @@ struct Params {
   unsigned* rsum_arr;
   double* rsum_parts;
   float* rsum_gs;                // residual sums per group of kGroupVecs vectors
-  SearchDesc* search;
+  DrawDesc* search;
   DynItem* dq;
   int nrows, nch, nres, dq_cap;
 };

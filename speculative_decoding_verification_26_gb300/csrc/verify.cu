@@ -11,10 +11,13 @@
 //   IT_STATS   softmax statistics of one chunk of a row (max m, s = sum
 //              2^{(x-m)c}, for signal rows t = sum (x-m)c 2^{(x-m)c}, greedy
 //              rows the max and its lowest index);
-//   IT_RSUM    sum of the residual [p_k - q_k]_+ over one 16 KB slice of
-//              rows k of both models (after a reject at k);
-//   IT_PSUM    sum of p_k without y_k over one chunk (one-hot reject);
-//   IT_SEARCH  the inverse-CDF search inside the located chunk.
+//   IT_DSUM    the weights of the final draw over one 16 KB slice of row k:
+//              the residual [p_k - q_k]_+ (reject, full q: rows k of both
+//              models) or p_k (bonus draw; one-hot reject with y_k removed);
+//              fp32 sums per 64-token group are kept, their fp64 total is
+//              the slice sum.  The CTA completing the last slice locates the
+//              slice, the group and the token (tutorial page, sections 3.2,
+//              3.3 and 5.2).
 // Roles inside a CTA:
 //   producer warp   claims items (dynamic queue first), skips rows that an
 //                   earlier reject has voided, stages the bytes into a 6-deep
@@ -146,6 +149,8 @@ __global__ void __launch_bounds__(1024) plan_kernel(Params P) {
     if (gam < 0 || gam > G) st |= SPEC_ST_BAD_GAMMA;
     if (P.mode != MODE_GREEDY && !temperature_ok(P.temperature[b])) st |= SPEC_ST_BAD_TEMPERATURE;
     P.req_flags[b] = st;
+    P.req_gam[b] = gam;
+    P.req_scale[b] = (P.mode != MODE_GREEDY && st == 0) ? scale_of(P.temperature[b]) : 0.f;
     // a request with no signal rows has its signal condition met already
     P.req_cnt[2 * b] = 0u;
     P.req_cnt[2 * b + 1] = (P.signals_on && st == 0 && gam == 0) ? 1u : 0u;
@@ -246,10 +251,9 @@ struct StageDesc {
 struct EpiSlot {
   int type, row_id, b, i;
   int kind, chunk, term, z;
-  float xy, margin;
-  int pad[2];
-  float wsum[kConsumerWarps];       // p sums per consumer warp (IT_PSUM)
-  double dsum[kConsumerWarps];      // residual sums per consumer warp (IT_RSUM)
+  float xy;
+  int pad[3];
+  double dsum[kConsumerWarps];      // draw-weight sums per consumer warp (IT_DSUM)
   Part part[kConsumerWarps];        // statistics per consumer warp
 };
 
@@ -263,11 +267,6 @@ struct __align__(128) VSmem {
   uint64_t epi_empty[kEpiSlots];
   StageDesc desc[kStages];
   EpiSlot slot[kEpiSlots];
-  // search scratch (consumer warps only)
-  float vs[kVecPerStage];
-  double wtot[kConsumerWarps];
-  double carry, cprev, cat;
-  int found_thread, z, last_elem, found;
   int abort;
 };
 
@@ -615,30 +614,43 @@ __device__ __forceinline__ int item_row(const Params& P, unsigned q, unsigned n_
   return q < n_items ? __ldg(P.row_list + q / (unsigned)P.nch) : 0;
 }
 
+// Raw per-request values of an item; finish_meta turns them into the
+// staging metadata once they have arrived (the producer stages an earlier
+// item in between, so the loads are not waited for).
+struct RawMeta {
+  unsigned q;
+  int rid, b, i, kind, kr, gam, tok;
+  float c;
+};
+
 template <bool GREEDY>
-__device__ __forceinline__ ItemMeta item_meta(const Params& P, unsigned q, int rid, unsigned n_items) {
-  ItemMeta m;
+__device__ __forceinline__ RawMeta item_meta_raw(const Params& P, unsigned q, int rid, unsigned n_items) {
+  RawMeta m;
   m.q = q;
-  m.valid = q < n_items;
-  m.skip = false;
-  m.y = -1;
-  m.c = 0.f;
   m.rid = rid;
   m.b = m.i = m.kind = 0;
-  m.chunk = (int)(q % (unsigned)P.nch);
-  if (!m.valid) return m;
+  m.kr = kNoReject; m.gam = 0; m.tok = -1; m.c = 0.f;
+  if (q >= n_items) return m;
   const int G = P.G;
   decode_row(rid, P.B, G, m.kind, m.b, m.i);
   const int b = m.b, i = m.i;
-  const int kr = (m.kind == KIND_TARGET || !P.signals_on) ? ld_relaxed(P.known_reject + b) : kNoReject;
-  const float T = GREEDY ? 1.f : P.temperature[b];
-  const int gam = gamma_of(P, b);
-  int y = -1;
+  if (m.kind == KIND_TARGET || !P.signals_on) m.kr = ld_relaxed(P.known_reject + b);
+  if (!GREEDY) m.c = __ldg(P.req_scale + b);
+  m.gam = __ldg(P.req_gam + b);
   // the draft token (sample / one-hot only: signals-only calls have no tokens)
-  if (!GREEDY && P.mode != MODE_SIGNALS && i < gam) y = P.draft_tokens[(size_t)b * G + i];
-  m.skip = kr < i;             // a reject at an earlier position voids this row
-  m.c = GREEDY ? 0.f : scale_of(T);
-  m.y = y;
+  if (!GREEDY && P.mode != MODE_SIGNALS && i < G) m.tok = __ldg(P.draft_tokens + (size_t)b * G + i);
+  return m;
+}
+
+__device__ __forceinline__ ItemMeta finish_meta(const Params& P, const RawMeta& r, unsigned n_items) {
+  ItemMeta m;
+  m.q = r.q;
+  m.valid = r.q < n_items;
+  m.rid = r.rid; m.b = r.b; m.i = r.i; m.kind = r.kind;
+  m.chunk = (int)(r.q % (unsigned)P.nch);
+  m.skip = r.kr < r.i;          // a reject at an earlier position voids this row
+  m.c = r.c;
+  m.y = r.i < r.gam ? r.tok : -1;
   return m;
 }
 
@@ -725,57 +737,33 @@ __device__ __forceinline__ bool put_row_range(const Params& P, VSmem& S, int& st
   return put_stage(S, stage, phase, d, 0, 0u);
 }
 
+// A draw slice: item c = slice index, aux = position k | kind << 8 | excl flag << 9.
 template <int DT>
 __device__ bool stage_dyn_item(const Params& P, VSmem& S, int& stage, uint32_t& phase, const DynItem& it) {
-  const int G = P.G, V = P.V, se = stage_elems(DT), ce = chunk_elems(DT);
-  const int b = it.b;
-  const float c = scale_of(P.temperature[b]);
+  const int G = P.G, V = P.V, se = stage_elems(DT);
+  const int b = it.b, k = it.aux & 0xff, kind = (it.aux >> 8) & 1 ? DK_P : DK_RESID, ch = it.c;
+  const bool has_excl = (it.aux >> 9) & 1;
   StageDesc d{};
-  d.type = it.type;
+  d.type = IT_DSUM;
   d.b = b;
-  d.c = c;
-  d.y = -1;
-  if (it.type == IT_RSUM) {
-    const int k = it.aux, ch = it.c;
-    const RowStats tr = ldcg_stats(P.row_stats + target_row_id(b, k, G));
+  d.i = k;
+  d.chunk = ch;
+  d.aux = kind;
+  d.c = __ldg(P.req_scale + b);
+  const RowStats tr = ldcg_stats(P.row_stats + target_row_id(b, k, G));
+  d.m1 = tr.m; d.s1 = tr.s;
+  d.y = has_excl ? P.draft_tokens[(size_t)b * G + k] : -1;
+  const int e0 = ch * se, e1 = min(e0 + se, V);
+  if (kind == DK_RESID) {
     const RowStats dr = ldcg_stats(P.row_stats + draft_row_id(b, k, P.B, G));
-    d.chunk = ch; d.i = k;
-    d.m1 = tr.m; d.s1 = tr.s; d.m2 = dr.m; d.s2 = dr.s;
-    const int e0 = ch * se, e1 = min(e0 + se, V);
-    d.flags = F_FIRST; d.aux = 0;
+    d.m2 = dr.m; d.s2 = dr.s;
+    d.flags = F_FIRST;
     if (!put_row_range<DT>(P, S, stage, phase, d, KIND_TARGET, b, k, e0, e1)) return false;
-    d.flags = F_LAST; d.aux = 1;
+    d.flags = F_LAST;
     return put_row_range<DT>(P, S, stage, phase, d, KIND_DRAFT, b, k, e0, e1);
   }
-  if (it.type == IT_PSUM) {
-    const int k = it.aux, cy = it.c;
-    const RowStats tr = ldcg_stats(P.row_stats + target_row_id(b, k, G));
-    d.chunk = cy; d.i = k;
-    d.m1 = tr.m; d.s1 = tr.s;
-    d.y = P.draft_tokens[(size_t)b * G + k];
-    const int e0 = cy * ce, e1 = min(e0 + ce, V);
-    for (int s0 = e0; s0 < e1; s0 += se) {
-      d.flags = (s0 == e0 ? F_FIRST : 0) | (s0 + se >= e1 ? F_LAST : 0);
-      if (!put_row_range<DT>(P, S, stage, phase, d, KIND_TARGET, b, k, s0, min(s0 + se, e1))) return false;
-    }
-    return true;
-  }
-  // IT_SEARCH: the located chunk of the draw
-  const SearchDesc* sd = P.search + b;
-  const int kind = __ldcg(&sd->kind), e0 = __ldcg(&sd->e0), e1 = __ldcg(&sd->e1);
-  const int rt = __ldcg(&sd->row_t);
-  int tk, tb, ti;
-  decode_row(rt, P.B, G, tk, tb, ti);
-  const RowStats tr = ldcg_stats(P.row_stats + rt);
-  d.m1 = tr.m; d.s1 = tr.s;
-  d.y = __ldcg(&sd->excl);
-  d.aux = kind;
-  d.i = ti;
-  for (int s0 = e0; s0 < e1; s0 += se) {
-    d.flags = (s0 == e0 ? F_FIRST : 0) | (s0 + se >= e1 ? F_LAST : 0);
-    if (!put_row_range<DT>(P, S, stage, phase, d, KIND_TARGET, b, ti, s0, min(s0 + se, e1))) return false;
-  }
-  return true;
+  d.flags = F_FIRST | F_LAST;
+  return put_row_range<DT>(P, S, stage, phase, d, KIND_TARGET, b, k, e0, e1);
 }
 
 template <int DT, bool GREEDY>
@@ -792,7 +780,7 @@ __device__ void producer_role(const Params& P, VSmem& S) {
   const unsigned q0 = atomicAdd(&P.hdr->queue.v, 1u);
   const unsigned q1 = atomicAdd(&P.hdr->queue.v, 1u);
   unsigned q2 = atomicAdd(&P.hdr->queue.v, 1u);
-  ItemMeta cur = item_meta<GREEDY>(P, q0, item_row(P, q0, n_items), n_items);
+  ItemMeta cur = finish_meta(P, item_meta_raw<GREEDY>(P, q0, item_row(P, q0, n_items), n_items), n_items);
   unsigned q_next = q1;
   int rid_next = item_row(P, q1, n_items);
   unsigned long long idle_since = 0;
@@ -805,12 +793,12 @@ __device__ void producer_role(const Params& P, VSmem& S) {
     const int peek = dyn ? ticket_peek(P, ticket) : 0;     // in flight while staging
     if (cur.valid) {
       // loads for the next items, issued before the (blocking) staging
-      const ItemMeta nxt = item_meta<GREEDY>(P, q_next, rid_next, n_items);
+      const RawMeta nxt = item_meta_raw<GREEDY>(P, q_next, rid_next, n_items);
       const int rid2 = item_row(P, q2, n_items);
       const unsigned q3 = q2 < n_items ? atomicAdd(&P.hdr->queue.v, 1u) : q2;
       if (cur.skip) red_add_release(P.row_arr + cur.rid, 1u + kSkipInc);
       else ok = stage_stats_item<DT, GREEDY>(P, S, stage, phase, cur);
-      cur = nxt;
+      cur = finish_meta(P, nxt, n_items);
       q_next = q2;
       rid_next = rid2;
       q2 = q3;
@@ -885,73 +873,6 @@ struct ResidW {
   }
 };
 
-// One search step over a staged piece of the located chunk (see the file
-// comment of the epilogue for the protocol): vector sums, an fp64 scan over
-// contiguous 4-vector groups of the 256 consumer threads, and an fp64 walk by
-// the thread whose group crosses the target.  wfun(v, w) gives the N weights
-// of vector v of the piece.
-template <int DT, class WF>
-__device__ void search_step(VSmem& S, int tid, int lane, int cw, int nvec, int elem0, double tl, WF wfun) {
-  constexpr int N = VecT<DT>::N;
-  int lastpos = -1;
-#pragma unroll
-  for (int q = 0; q < kVecPerThread; ++q) {
-    const int v = tid + q * kConsumerThreads;
-    float vsum = 0.f;
-    if (v < nvec) {
-      float w[N];
-      wfun(v, w);
-#pragma unroll
-      for (int k = 0; k < N; ++k) {
-        vsum += w[k];
-        if (w[k] > 0.f) lastpos = elem0 + v * N + k;
-      }
-    }
-    S.vs[v] = vsum;
-  }
-  if (lastpos >= 0) atomicMax(&S.last_elem, lastpos);
-  consumer_bar();
-  const float s4 = (S.vs[4 * tid] + S.vs[4 * tid + 1]) + (S.vs[4 * tid + 2] + S.vs[4 * tid + 3]);
-  double incl = (double)s4;
-#pragma unroll
-  for (int d = 1; d < 32; d <<= 1) {
-    const double o = __shfl_up_sync(0xffffffffu, incl, d);
-    if (lane >= d) incl += o;
-  }
-  double exw = __shfl_up_sync(0xffffffffu, incl, 1);
-  if (lane == 0) exw = 0.0;
-  if (lane == 31) S.wtot[cw] = incl;
-  consumer_bar();
-  double before = S.carry, total = S.carry;
-  for (int w = 0; w < kConsumerWarps; ++w) {
-    if (w < cw) before += S.wtot[w];
-    total += S.wtot[w];
-  }
-  const double E = before + exw;
-  const int found = S.found;
-  if (!found && E + (double)s4 > tl) atomicMin(&S.found_thread, tid);
-  consumer_bar();
-  if (!found && tid == S.found_thread) {
-    double C = E, Cp = E;
-    int z = -1;
-    for (int vv = 4 * tid; vv < nvec && z < 0; ++vv) {
-      float w[N];
-      wfun(vv, w);
-      for (int k = 0; k < N; ++k) {
-        Cp = C;
-        C += (double)w[k];
-        if (C > tl) { z = elem0 + vv * N + k; break; }
-      }
-    }
-    if (z >= 0) { S.z = z; S.cprev = Cp; S.cat = C; S.found = 1; }
-  }
-  consumer_bar();
-  if (tid == 0) {
-    if (!S.found) S.carry = total;
-    S.found_thread = INT_MAX;
-  }
-}
-
 template <int DT, bool GREEDY>
 __device__ void consumer_role(const Params& P, VSmem& S, int cw, int lane) {
   constexpr int N = VecT<DT>::N;
@@ -962,8 +883,7 @@ __device__ void consumer_role(const Params& P, VSmem& S, int cw, int lane) {
   RunState r;
   run_reset(r);
   bool ent = false;
-  float c = 0.f, xy = qnan(), wacc = 0.f;
-  double tl = 0.0;
+  float c = 0.f, xy = qnan();
   auto advance = [&]() {
     if (++stage == kStages) { stage = 0; phase ^= 1u; }
   };
@@ -1051,115 +971,68 @@ __device__ void consumer_role(const Params& P, VSmem& S, int cw, int lane) {
       continue;
     }
 
-    if (d.type == IT_RSUM) {
-      // a pair of stages: slice of row k of the target, then the same slice of
-      // the draft.  Weights [p - q]_+; fp32 sums per group of 8 consecutive
-      // vectors are stored for the search, their fp64 total is the partial.
-      const int st1 = stage;
+    // IT_DSUM: one slice of the draw's weights (a stage pair for the residual)
+    const bool resid = d.aux == DK_RESID;
+    const int st1 = stage;
+    const uint4* vec2 = vec;
+    if (resid) {
       advance();
       if (!wait_bar(S, &S.full[stage], phase)) { set_abort(P, S); return; }
       const StageDesc d2 = S.desc[stage];
       if (d2.flags & F_DIRECT) fill_direct<DT>(P, S, stage, d2, tid);
-      const uint4* vec2 = reinterpret_cast<const uint4*>(S.ring[stage]);
-      ResidW R;
-      R.c = d.c; R.mpc = d.m1 * d.c; R.mqc = d.m2 * d.c; R.rp = 1.f / d.s1; R.rq = 1.f / d.s2;
-      uint4 wt[kVecPerThread], wd[kVecPerThread];
-      load_stage<DT>(vec, d.nvec, tid, wt);
-      load_stage<DT>(vec2, d.nvec, tid, wd);
-      float* gs_out = P.rsum_gs + ((size_t)d.b * P.nres + d.chunk) * kGroupsPerStage;
-      double dsum = 0.0;
+      vec2 = reinterpret_cast<const uint4*>(S.ring[stage]);
+    }
+    uint4 wt[kVecPerThread], wd[kVecPerThread];
+    load_stage<DT>(vec, d.nvec, tid, wt);
+    if (resid) load_stage<DT>(vec2, d.nvec, tid, wd);
+    ResidW R;
+    R.c = d.c; R.mpc = d.m1 * d.c; R.mqc = d.m2 * d.c; R.rp = 1.f / d.s1; R.rq = 1.f / d.s2;
+    const float mc = d.m1 * d.c;
+    float* gs_out = P.rsum_gs + ((size_t)d.b * P.nres + d.chunk) * kGroupsPerStage;
+    double dsum = 0.0;
 #pragma unroll
-      for (int q = 0; q < kVecPerThread; ++q) {
-        float xt[N], xd[N], e[N];
-        VecT<DT>::unpack(wt[q], xt);
+    for (int q = 0; q < kVecPerThread; ++q) {
+      const int v = tid + q * kConsumerThreads;
+      float xt[N], e[N];
+      VecT<DT>::unpack(wt[q], xt);
+      if (resid) {
+        float xd[N];
         VecT<DT>::unpack(wd[q], xd);
 #pragma unroll
         for (int k = 0; k < N; ++k) e[k] = R(xt[k], xd[k]);
-        float g;
-        if (N == 8) g = ((e[0] + e[1]) + (e[2] + e[3])) + ((e[4] + e[5]) + (e[6] + e[7]));
-        else g = (e[0] + e[1]) + (e[2] + e[3]);
-        // vectors tid + 256 q of 8 consecutive threads form one group
-        g += __shfl_xor_sync(0xffffffffu, g, 1);
-        g += __shfl_xor_sync(0xffffffffu, g, 2);
-        g += __shfl_xor_sync(0xffffffffu, g, 4);
-        const int v = tid + q * kConsumerThreads;
-        if ((lane & (kGroupVecs - 1)) == 0) {
-          if (v < d.nvec) __stcg(gs_out + v / kGroupVecs, g);
-          dsum += (double)g;
+      } else {
+#pragma unroll
+        for (int k = 0; k < N; ++k) e[k] = ex2(fmaf(xt[k], d.c, -mc));
+        if (d.y >= 0) {
+          const int off = d.y - (d.elem0 + v * N);
+          if (off >= 0 && off < N)
+#pragma unroll
+            for (int k = 0; k < N; ++k)
+              if (k == off) e[k] = 0.f;
         }
       }
-#pragma unroll
-      for (int off = 16; off >= 1; off >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, off);
-      release(st1);
-      release(stage);
-      advance();
-      if (!to_epilogue([&](EpiSlot& E) {
-            if (lane == 0) E.dsum[cw] = dsum;
-            if (tid == 0) { E.type = IT_RSUM; E.b = d.b; E.chunk = d.chunk; E.i = d.i; }
-          }))
-        return;
-      continue;
-    }
-
-    // IT_PSUM and IT_SEARCH over p: single stages of one chunk of the target row
-    const float mc = d.m1 * d.c;
-    const int excl = d.y;
-    auto pw = [&](int v, float* w) {
-      float x[N];
-      VecT<DT>::unpack(vec[v], x);
-#pragma unroll
-      for (int k = 0; k < N; ++k) w[k] = (d.elem0 + v * N + k == excl) ? 0.f : ex2(fmaf(x[k], d.c, -mc));
-    };
-    if (d.type == IT_PSUM) {
-      if (d.flags & F_FIRST) wacc = 0.f;
-      float sv[kVecPerThread];
-#pragma unroll
-      for (int q = 0; q < kVecPerThread; ++q) {
-        const int v = tid + q * kConsumerThreads;
-        float w[N];
-        if (v < d.nvec) pw(v, w);
-        else
-#pragma unroll
-          for (int k = 0; k < N; ++k) w[k] = 0.f;
-        if (N == 8) sv[q] = ((w[0] + w[1]) + (w[2] + w[3])) + ((w[4] + w[5]) + (w[6] + w[7]));
-        else sv[q] = (w[0] + w[1]) + (w[2] + w[3]);
+      float g;
+      if (N == 8) g = ((e[0] + e[1]) + (e[2] + e[3])) + ((e[4] + e[5]) + (e[6] + e[7]));
+      else g = (e[0] + e[1]) + (e[2] + e[3]);
+      // vectors tid + 256 q of 8 consecutive threads form one group
+      g += __shfl_xor_sync(0xffffffffu, g, 1);
+      g += __shfl_xor_sync(0xffffffffu, g, 2);
+      g += __shfl_xor_sync(0xffffffffu, g, 4);
+      if ((lane & (kGroupVecs - 1)) == 0) {
+        if (v < d.nvec) __stcg(gs_out + v / kGroupVecs, g);
+        dsum += (double)g;
       }
-      wacc += (sv[0] + sv[1]) + (sv[2] + sv[3]);
-      release(stage);
-      advance();
-      if (d.flags & F_LAST) {
-        float s = wacc;
+    }
 #pragma unroll
-        for (int off = 16; off >= 1; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-        if (!to_epilogue([&](EpiSlot& E) {
-              if (lane == 0) E.wsum[cw] = s;
-              if (tid == 0) { E.type = IT_PSUM; E.b = d.b; E.chunk = d.chunk; E.i = d.i; }
-            }))
-          return;
-      }
-      continue;
-    }
-    // IT_SEARCH over p
-    if (d.flags & F_FIRST) {
-      if (tid == 0) {
-        S.carry = 0.0; S.found = 0; S.z = -1; S.last_elem = -1; S.found_thread = INT_MAX;
-      }
-      tl = __ldcg(&P.search[d.b].tl);
-      consumer_bar();
-    }
-    if (!S.found) search_step<DT>(S, tid, lane, cw, d.nvec, d.elem0, tl, pw);
-    consumer_bar();
-    const int found = S.found;
-    release(stage);
+    for (int off = 16; off >= 1; off >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, off);
+    release(st1);
+    if (resid) release(stage);
     advance();
-    if (d.flags & F_LAST) {
-      const int z = found ? S.z : S.last_elem;
-      const float margin = found ? (float)fmin(tl - S.cprev, S.cat - tl) : 0.f;
-      if (!to_epilogue([&](EpiSlot& E) {
-            if (tid == 0) { E.type = IT_SEARCH; E.b = d.b; E.z = z; E.margin = margin; }
-          }))
-        return;
-    }
+    if (!to_epilogue([&](EpiSlot& E) {
+          if (lane == 0) E.dsum[cw] = dsum;
+          if (tid == 0) { E.type = IT_DSUM; E.b = d.b; E.chunk = d.chunk; E.i = d.i; }
+        }))
+      return;
   }
 }
 
@@ -1188,7 +1061,7 @@ __device__ int evaluate_position(const Params& P, int b, int i) {
     const bool sample = P.mode == MODE_SAMPLE;
     const int did = draft_row_id(b, i, P.B, G);
     const float u = P.uniforms[(size_t)b * (G + 1) + i];
-    const float c = scale_of(P.temperature[b]);
+    const float c = __ldg(P.req_scale + b);
     const float xt = __ldcg(P.row_xy + tid_t);
     RowStats dr{};
     float xd = 0.f;
@@ -1262,31 +1135,31 @@ __device__ void write_outputs(const Params& P, int b, int st, int k, int z, int 
     if (lane == 0) P.accept_len[b] = k;
   }
   if (P.signals_on && (P.signals || P.row_signals)) {
-    double H = 0.0, cf = 0.0;
+    // H_i = log2 s_i - t_i / s_i bits and c_i = 1 / s_i (fp32; fixed xor tree)
+    float H = 0.f, cf = 0.f;
     const bool in = lane < gam;
     if (in) {
       const RowStats r = ldcg_stats(P.row_stats + draft_row_id(b, lane, P.B, G));
-      const double s = (double)r.s;
-      H = (double)log2f(r.s) - (double)r.t / s;
-      cf = 1.0 / s;
+      H = log2f(r.s) - r.t / r.s;
+      cf = 1.f / r.s;
     }
     if (P.row_signals && lane < G) {
       float* rs = P.row_signals + ((size_t)b * G + lane) * 2;
-      rs[0] = in ? (float)H : qnan();
-      rs[1] = in ? (float)cf : qnan();
+      rs[0] = in ? H : qnan();
+      rs[1] = in ? cf : qnan();
     }
-    double hs = H, cs = cf, hm = in ? H : -INFINITY, cm = in ? cf : INFINITY;
+    float hs = H, cs = cf, hm = in ? H : -INFINITY, cm = in ? cf : INFINITY;
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) {
       hs += __shfl_xor_sync(0xffffffffu, hs, off);
       cs += __shfl_xor_sync(0xffffffffu, cs, off);
-      hm = fmax(hm, __shfl_xor_sync(0xffffffffu, hm, off));
-      cm = fmin(cm, __shfl_xor_sync(0xffffffffu, cm, off));
+      hm = fmaxf(hm, __shfl_xor_sync(0xffffffffu, hm, off));
+      cm = fminf(cm, __shfl_xor_sync(0xffffffffu, cm, off));
     }
     if (lane == 0 && P.signals) {
       float* sg = P.signals + (size_t)b * 4;
       if (gam > 0) {
-        sg[0] = (float)(hs / gam); sg[1] = (float)hm; sg[2] = (float)(cs / gam); sg[3] = (float)cm;
+        sg[0] = hs / (float)gam; sg[1] = hm; sg[2] = cs / (float)gam; sg[3] = cm;
       } else {
         sg[0] = sg[1] = sg[2] = sg[3] = qnan();
       }
@@ -1380,108 +1253,147 @@ __device__ int warp_locate(int n, Get get, double t, double* before, double* tot
   return lastpos;
 }
 
-// Locate the chunk of the draw from p_k (target row k of request b): chunk
-// weights from the statistics partials (unnormalised p), the chunk holding
-// the excluded token (one-hot residual) replaced by its fresh sum sy; then
-// create the search item.  Warp-wide.
-template <int DT>
-__device__ void locate_p(const Params& P, int b, int k, int excl, int cy, double sy, int st, int lane) {
-  const int G = P.G, nch = P.nch, ce = chunk_elems(DT);
-  const int rid = target_row_id(b, k, G);
-  const RowStats rs = ldcg_stats(P.row_stats + rid);
-  const float c = scale_of(P.temperature[b]);
-  const Part* parts = P.parts + (size_t)rid * nch;
-  auto get = [&](int j) -> double {
-    if (j == cy) return sy;
-    const Part q = ldcg_part(parts + j);
-    if (!(q.s > 0.f)) return 0.0;
-    return (double)(q.s * ex2((q.m - rs.m) * c));
-  };
-  double before, W;
-  warp_locate(nch, get, INFINITY, &before, &W, lane);
-  if (!(W > 0.0)) {
-    if (excl >= 0) {        // rounding left no mass besides y: draw from p itself
-      locate_p<DT>(P, b, k, -1, -1, 0.0, st | SPEC_ST_ZERO_RESIDUAL, lane);
-      return;
-    }
-    draw_done(P, b, SPEC_ST_TIMEOUT, 0, -1, lane);   // a complete row always has mass
-    return;
-  }
-  const float ud = P.uniforms[(size_t)b * (G + 1) + G];
-  const double t = (double)ud * W;
-  double tot;
-  const int cs = warp_locate(nch, get, t, &before, &tot, lane);
+// Start (or restart) the draw of request b: record it, then create one
+// IT_DSUM item per slice of row k.  Warp-wide.
+__device__ void start_draw(const Params& P, int b, int kind, int k, bool has_excl, int status, int lane) {
   if (lane == 0) {
-    SearchDesc* sd = P.search + b;
-    __stcg(&sd->tl, t - before);
-    __stcg(&sd->W, W);
-    __stcg(&sd->kind, (int)SK_P);
-    __stcg(&sd->e0, cs * ce);
-    __stcg(&sd->e1, min(cs * ce + ce, P.V));
-    __stcg(&sd->excl, excl);
-    __stcg(&sd->status, st);
-    __stcg(&sd->row_t, rid);
-    __stcg(&sd->row_d, -1);
+    DrawDesc* dd = P.search + b;
+    __stcg(&dd->kind, kind);
+    __stcg(&dd->k, k);
+    __stcg(&dd->excl, has_excl ? 1 : 0);
+    __stcg(&dd->status, status);
+    __stcg(P.rsum_arr + b, 0u);
+    __stcg(P.req_k + b, k);
   }
-  enqueue_items(P, 1, IT_SEARCH, b, 0, 0, lane);
+  __syncwarp();
+  const int aux = k | (kind == DK_P ? 1 << 8 : 0) | (has_excl ? 1 << 9 : 0);
+  enqueue_items(P, P.nres, IT_DSUM, b, 0, aux, lane);
 }
 
-// All residual slices of request b are summed: the draw (warp-wide).  The
-// slice is located by the fp64 prefix of the slice sums, the 64-token group
-// inside it by the fp64 prefix of the stored group sums, and the token by an
-// fp64 walk over the group's recomputed weights (two 128-byte loads, from
-// L2).  If rounding leaves no crossing in the group, the last weighted token
-// of the group is taken (a margin of 0 is counted as a near tie).
+// Warp inclusive scan of one fp64 value per lane (fixed association).
+__device__ __forceinline__ double warp_incl_scan(double v, int lane) {
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const double o = __shfl_up_sync(0xffffffffu, v, d);
+    if (lane >= d) v += o;
+  }
+  return v;
+}
+
+// All slices of the draw of request b are summed (warp-wide).  The slice is
+// located by the fp64 prefix of the slice sums, the 64-token group inside it
+// by the fp64 prefix of the stored group sums, and the token by an fp64 walk
+// over the group's recomputed weights (one or two 128-byte loads, from L2).
+// If rounding leaves no crossing in the group, its last weighted token is
+// taken (counted as a near tie).  Zero total mass restarts the draw from p_k
+// with SPEC_ST_ZERO_RESIDUAL.
 template <int DT>
-__device__ void locate_resid(const Params& P, int b, int lane) {
+__device__ void locate_draw(const Params& P, int b, int lane) {
   constexpr int N = VecT<DT>::N;
   constexpr int GE = kGroupVecs * N;                 // tokens per group (64 bf16 / 32 fp32)
+  constexpr int PER = GE / 32;                       // tokens per lane in the final walk
+  constexpr int GPL = kGroupsPerStage / 32;          // groups per lane (4)
   const int G = P.G, V = P.V, nres = P.nres, se = stage_elems(DT);
-  const int k = __ldcg(P.req_k + b);
+  const DrawDesc* dd = P.search + b;
+  const int kind = __ldcg(&dd->kind), k = __ldcg(&dd->k), dstat = __ldcg(&dd->status);
+  const bool has_excl = __ldcg(&dd->excl) != 0;
+  const bool resid = kind == DK_RESID;
+  // independent loads first
+  const RowStats tr = ldcg_stats(P.row_stats + target_row_id(b, k, G));
+  const RowStats dr = resid ? ldcg_stats(P.row_stats + draft_row_id(b, k, P.B, G)) : RowStats{};
+  const float c = __ldg(P.req_scale + b);
+  const float ud = P.uniforms[(size_t)b * (G + 1) + G];
+  const int excl = has_excl ? P.draft_tokens[(size_t)b * G + k] : -1;
   const double* parts = P.rsum_parts + (size_t)b * nres;
-  auto get = [&](int j) -> double { return __ldcg(parts + j); };
-  double before, W;
-  warp_locate(nres, get, INFINITY, &before, &W, lane);
-  if (!(W > 0.0)) {         // residual mass rounded to zero: draw from p_k
-    locate_p<DT>(P, b, k, -1, -1, 0.0, SPEC_ST_ZERO_RESIDUAL, lane);
+  // 1. the slice: prefix of the slice sums
+  double W, before;
+  int cs;
+  if (nres <= 32) {
+    const double v = lane < nres ? __ldcg(parts + lane) : 0.0;
+    const double incl = warp_incl_scan(v, lane);
+    W = __shfl_sync(0xffffffffu, incl, 31);
+    const double t = (double)ud * W;
+    const unsigned cross = __ballot_sync(0xffffffffu, lane < nres && incl > t);
+    const unsigned pos = __ballot_sync(0xffffffffu, v > 0.0);
+    cs = cross ? __ffs(cross) - 1 : (pos ? 31 - __clz(pos) : -1);
+    before = cs >= 0 ? __shfl_sync(0xffffffffu, incl - v, cs) : 0.0;
+  } else {
+    auto get = [&](int j) -> double { return __ldcg(parts + j); };
+    warp_locate(nres, get, INFINITY, &before, &W, lane);
+    double tot;
+    cs = warp_locate(nres, get, (double)ud * W, &before, &tot, lane);
+  }
+  if (!(W > 0.0)) {
+    if (resid || has_excl) {   // residual mass rounded to zero: draw from p_k itself
+      start_draw(P, b, DK_P, k, false, dstat | SPEC_ST_ZERO_RESIDUAL, lane);
+      return;
+    }
+    draw_done(P, b, SPEC_ST_TIMEOUT, 0, -1, lane);      // a complete row always has mass
     return;
   }
-  const float ud = P.uniforms[(size_t)b * (G + 1) + G];
   const double t = (double)ud * W;
-  double tot;
-  const int cs = warp_locate(nres, get, t, &before, &tot, lane);
   const int e0 = cs * se, e1 = min(e0 + se, V);
   const int ngroups = (e1 - e0 + GE - 1) / GE;
+  // 2. the group: lane l holds groups GPL*l .. GPL*l + GPL-1
   const float* gsum = P.rsum_gs + ((size_t)b * nres + cs) * kGroupsPerStage;
-  auto gget = [&](int j) -> double { return (double)__ldcg(gsum + j); };
-  double gbefore;
-  const int g = warp_locate(ngroups, gget, t - before, &gbefore, &tot, lane);
-  const double tl = t - before - gbefore;
-  // the group's tokens: lane l takes tokens 2l, 2l+1 (bf16) or l (fp32)
-  const RowStats tr = ldcg_stats(P.row_stats + target_row_id(b, k, G));
-  const RowStats dr = ldcg_stats(P.row_stats + draft_row_id(b, k, P.B, G));
+  float gv[GPL];
+  double lsum = 0.0;
+#pragma unroll
+  for (int u = 0; u < GPL; ++u) {
+    const int j = lane * GPL + u;
+    gv[u] = j < ngroups ? __ldcg(gsum + j) : 0.f;
+    lsum += (double)gv[u];
+  }
+  const double tl = t - before;
+  const double gincl = warp_incl_scan(lsum, lane);
+  const unsigned gcross = __ballot_sync(0xffffffffu, gincl > tl);
+  const unsigned gpos = __ballot_sync(0xffffffffu, lsum > 0.0);
+  const int gl = gcross ? __ffs(gcross) - 1 : (gpos ? 31 - __clz(gpos) : 0);
+  int g = gl * GPL;
+  double gbefore = __shfl_sync(0xffffffffu, gincl - lsum, gl);
+  {
+    // walk the crossing lane's groups (every lane computes the same from shuffles)
+    double acc = gbefore;
+    int gsel = -1;
+    double gsel_before = gbefore;
+    int last_pos = -1;
+    double last_before = gbefore;
+#pragma unroll
+    for (int u = 0; u < GPL; ++u) {
+      const double w = (double)__shfl_sync(0xffffffffu, gv[u], gl);
+      if (w > 0.0) { last_pos = gl * GPL + u; last_before = acc; }
+      if (gsel < 0 && acc + w > tl) { gsel = gl * GPL + u; gsel_before = acc; }
+      acc += w;
+    }
+    if (gsel < 0) { gsel = last_pos >= 0 ? last_pos : gl * GPL; gsel_before = last_before; }
+    g = gsel;
+    gbefore = gsel_before;
+  }
+  const double tl2 = tl - gbefore;
+  // 3. the token: lane l takes PER consecutive tokens of the group
   ResidW R;
-  R.c = scale_of(P.temperature[b]);
-  R.mpc = tr.m * R.c; R.mqc = dr.m * R.c; R.rp = 1.f / tr.s; R.rq = 1.f / dr.s;
-  const long long trow = row_elem_offset(KIND_TARGET, b, k, G, V), drow = row_elem_offset(KIND_DRAFT, b, k, G, V);
-  constexpr int PER = GE / 32;
+  R.c = c; R.mpc = tr.m * c; R.mqc = dr.m * c; R.rp = 1.f / tr.s; R.rq = 1.f / dr.s;
+  const float mc = tr.m * c;
+  const long long trow = row_elem_offset(KIND_TARGET, b, k, G, V);
+  const long long drow = resid ? row_elem_offset(KIND_DRAFT, b, k, G, V) : 0;
   float w[PER];
   const int g0 = e0 + g * GE;
   double mine = 0.0;
 #pragma unroll
   for (int u = 0; u < PER; ++u) {
     const int e = g0 + lane * PER + u;
-    w[u] = e < e1 ? R(load_logit(P.target, DT, trow + e), load_logit(P.draft, DT, drow + e)) : 0.f;
-    mine += (double)w[u];
+    float wu = 0.f;
+    if (e < e1) {
+      const float xt = load_logit(P.target, DT, trow + e);
+      if (resid) wu = R(xt, load_logit(P.draft, DT, drow + e));
+      else wu = e == excl ? 0.f : ex2(fmaf(xt, c, -mc));
+    }
+    w[u] = wu;
+    mine += (double)wu;
   }
-  double incl = mine;
-#pragma unroll
-  for (int dd = 1; dd < 32; dd <<= 1) {
-    const double o = __shfl_up_sync(0xffffffffu, incl, dd);
-    if (lane >= dd) incl += o;
-  }
+  const double incl = warp_incl_scan(mine, lane);
   const double ex = incl - mine;
-  const unsigned cross = __ballot_sync(0xffffffffu, ex + mine > tl);
+  const unsigned cross = __ballot_sync(0xffffffffu, incl > tl2);
   int z = -1;
   double margin = 0.0;
   if (cross) {
@@ -1491,13 +1403,13 @@ __device__ void locate_resid(const Params& P, int b, int lane) {
       for (int u = 0; u < PER; ++u) {
         Cp = C;
         C += (double)w[u];
-        if (C > tl) { z = g0 + lane * PER + u; break; }
+        if (C > tl2) { z = g0 + lane * PER + u; break; }
       }
       if (z < 0) {         // rounding between the lane sum and its terms
         for (int u = PER - 1; u >= 0; --u)
           if (w[u] > 0.f) { z = g0 + lane * PER + u; break; }
       } else {
-        margin = fmin(tl - Cp, C - tl);
+        margin = fmin(tl2 - Cp, C - tl2);
       }
     }
     z = __shfl_sync(0xffffffffu, z, f);
@@ -1514,7 +1426,7 @@ __device__ void locate_resid(const Params& P, int b, int lane) {
     }
   }
   if (lane == 0 && !(margin >= (double)kDrawGuard * W)) atomicAdd(&HDR_UNCERTAIN(P.hdr), 1u);
-  draw_done(P, b, z >= 0 ? 0 : SPEC_ST_TIMEOUT, k, z, lane);
+  draw_done(P, b, z >= 0 ? dstat : SPEC_ST_TIMEOUT, k, z, lane);
 }
 
 // The first reject k of request b is known: settle its draw, or create the
@@ -1544,16 +1456,8 @@ __device__ void dispatch_draw(const Params& P, int b, int lane) {
   }
   const float ud = P.uniforms[(size_t)b * (G + 1) + G];
   if (!(ud >= 0.f && ud < 1.f)) { draw_done(P, b, SPEC_ST_BAD_UNIFORM, 0, -1, lane); return; }
-  if (lane == 0) __stcg(P.req_k + b, k);
-  __syncwarp();
-  if (rejected && P.mode == MODE_SAMPLE) {
-    enqueue_items(P, P.nres, IT_RSUM, b, 0, k, lane);
-  } else if (rejected) {
-    const int y = P.draft_tokens[(size_t)b * G + k];
-    enqueue_items(P, 1, IT_PSUM, b, y / chunk_elems(DT), k, lane);
-  } else {
-    locate_p<DT>(P, b, k, -1, -1, 0.0, 0, lane);
-  }
+  if (rejected && P.mode == MODE_SAMPLE) start_draw(P, b, DK_RESID, k, false, 0, lane);
+  else start_draw(P, b, DK_P, k, rejected, 0, lane);    // one-hot residual: p without y_k
 }
 
 // A row of request b is complete (its statistics are published): record the
@@ -1602,20 +1506,15 @@ __device__ void epilogue_role(const Params& P, VSmem& S, int lane, int e) {
     const EpiSlot& E = S.slot[eslot];
     if (E.term) return;
     const int type = E.type, rid = E.row_id, b = E.b, i = E.i, kind = E.kind, chunk = E.chunk;
-    const float xy = E.xy, margin = E.margin;
-    const int z = E.z;
+    const float xy = E.xy;
     Part p = lane < kConsumerWarps ? E.part[lane] : empty_part();
     double ws = 0.0;
-    if (lane == 0) {
-      if (type == IT_RSUM)
-        for (int w = 0; w < kConsumerWarps; ++w) ws += E.dsum[w];
-      else
-        for (int w = 0; w < kConsumerWarps; ++w) ws += (double)E.wsum[w];
-    }
+    if (lane == 0 && type == IT_DSUM)
+      for (int w = 0; w < kConsumerWarps; ++w) ws += E.dsum[w];
     __syncwarp();
     if (lane == 0) mbar_arrive(&S.epi_empty[eslot]);
 
-    if (type == IT_RSUM) {
+    if (type == IT_DSUM) {
       bool last = false;
       if (lane == 0) {
         __stcg(P.rsum_parts + (size_t)b * P.nres + chunk, ws);
@@ -1623,27 +1522,13 @@ __device__ void epilogue_role(const Params& P, VSmem& S, int lane, int e) {
         const unsigned o = atom_add_acqrel(P.rsum_arr + b, 1u);
         last = o + 1u == (unsigned)P.nres;
       }
-      if (__shfl_sync(0xffffffffu, last, 0)) locate_resid<DT>(P, b, lane);
-      continue;
-    }
-    if (type == IT_PSUM) {
-      ws = __shfl_sync(0xffffffffu, ws, 0);
-      const int k = __ldcg(P.req_k + b);
-      locate_p<DT>(P, b, k, P.draft_tokens[(size_t)b * G + k], chunk, ws, 0, lane);
-      continue;
-    }
-    if (type == IT_SEARCH) {
-      const SearchDesc* sd = P.search + b;
-      const double W = __ldcg(&sd->W);
-      const int st = __ldcg(&sd->status);
-      if (lane == 0 && !((double)margin >= kDrawGuard * W)) atomicAdd(&HDR_UNCERTAIN(P.hdr), 1u);
-      draw_done(P, b, z >= 0 ? st : SPEC_ST_TIMEOUT, __ldcg(P.req_k + b), z, lane);
+      if (__shfl_sync(0xffffffffu, last, 0)) locate_draw<DT>(P, b, lane);
       continue;
     }
 
     // IT_STATS: publish the chunk partial; the CTA completing the row merges it
     const bool ent = !GREEDY && kind == KIND_DRAFT && P.signals_on;
-    const float c = GREEDY ? 0.f : scale_of(P.temperature[b]);
+    const float c = GREEDY ? 0.f : __ldg(P.req_scale + b);
 #pragma unroll
     for (int off = 4; off >= 1; off >>= 1) {
       const Part o = shfl_part(p, off);
