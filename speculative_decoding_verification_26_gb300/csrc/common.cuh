@@ -57,7 +57,11 @@ constexpr int kGroupsPerStage = kStageBytes / 16 / kGroupVecs;   // 128
 constexpr uint32_t kSkipInc = 1u << 20;                 // arrival mark of a skipped chunk
 constexpr uint32_t kCountMask = kSkipInc - 1;
 constexpr int kNoReject = 0x7fffffff;
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s per wait
+// Every bounded wait counts SM clock cycles (clock64 is a register of the SM
+// and costs a few cycles to read; the global timer is read from outside the
+// SM and delays the reading warp by about a microsecond under load).
+// 4e9 cycles: about 2 s at the maximum clock, longer when clocked down.
+constexpr long long kWaitLimitCycles = 4000000000ll;
 
 // ---------------------------------------------------------------------------
 // partial statistics of a run of logits, relative to its own max m:
@@ -269,13 +273,26 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait for phase `parity` of `bar` to complete; gives up after kWaitLimitNs.
+// As mbar_try_wait, but the thread may sleep in hardware until the phase
+// completes or `hint_ns` pass (instead of returning at once): a waiting warp
+// then takes no issue slots and no shared-memory bandwidth from the others.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for phase `parity` of `bar` to complete; gives up after kWaitLimitCycles.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
-  const unsigned long long t0 = globaltimer();
+  const long long c0 = clock64();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (globaltimer() - t0 > kWaitLimitNs) return false;
+    if (clock64() - c0 > kWaitLimitCycles) return false;
   }
 }
 

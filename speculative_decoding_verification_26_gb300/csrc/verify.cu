@@ -284,13 +284,15 @@ __device__ __forceinline__ void set_abort(const Params& P, VSmem& S) {
 }
 
 // Bounded wait that also gives up when another role of the CTA aborted.
+// The wait sleeps in hardware between checks (at most kSleepHintNs each).
+constexpr uint32_t kSleepHintNs = 100000;
 __device__ __forceinline__ bool wait_bar(VSmem& S, uint64_t* bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
-  const unsigned long long t0 = globaltimer();
+  const long long c0 = clock64();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_sleep(bar, parity, kSleepHintNs)) return true;
     if (aborted(S)) return false;
-    if (globaltimer() - t0 > kWaitLimitNs) return false;
+    if (clock64() - c0 > kWaitLimitCycles) return false;
   }
 }
 
@@ -783,7 +785,7 @@ __device__ void producer_role(const Params& P, VSmem& S) {
   ItemMeta cur = finish_meta(P, item_meta_raw<GREEDY>(P, q0, item_row(P, q0, n_items), n_items), n_items);
   unsigned q_next = q1;
   int rid_next = item_row(P, q1, n_items);
-  unsigned long long idle_since = 0;
+  long long idle_since = -1;      // clock64 at the start of the current idle spell
   unsigned sleep_ns = 64;
   while (ok) {
     // one static item and one ready draw item per round: neither kind can
@@ -812,16 +814,16 @@ __device__ void producer_role(const Params& P, VSmem& S) {
       did = true;
     }
     if (did) {
-      idle_since = 0;
+      idle_since = -1;
       sleep_ns = 64;
       continue;
     }
     // nothing to stage right now: finished, or draw items are still to come
     if (ld_relaxed_u32(&P.hdr->done.v) >= n_valid) break;
     if (ld_relaxed_u32(&P.hdr->error.v) != 0u) break;
-    const unsigned long long now = globaltimer();
-    if (idle_since == 0) idle_since = now;
-    else if (now - idle_since > kWaitLimitNs) { ok = false; break; }
+    const long long now = clock64();
+    if (idle_since < 0) idle_since = now;
+    else if (now - idle_since > kWaitLimitCycles) { ok = false; break; }
     __nanosleep(sleep_ns);
     if (sleep_ns < 1024) sleep_ns *= 2;
   }
@@ -834,8 +836,8 @@ __device__ void producer_role(const Params& P, VSmem& S) {
   set_abort(P, S);
   for (int s = 0; s < kStages; ++s) {
     const uint32_t par = s < stage ? phase : phase ^ 1u;
-    const unsigned long long t0 = globaltimer();
-    while (!mbar_try_wait(&S.full[s], par) && globaltimer() - t0 < kWaitLimitNs) {
+    const long long c0 = clock64();
+    while (!mbar_try_wait(&S.full[s], par) && clock64() - c0 < kWaitLimitCycles) {
     }
   }
 }
