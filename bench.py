@@ -1,11 +1,11 @@
 #!/usr/bin/env python3
 """Throughput of batched speculative-sampling verification on GB300.
 
-One step = one spec_verify_sample call (plan + stats + finalize kernels) over
+One step = one spec_verify_sample call (plan kernel + persistent verify kernel) over
 one synthetic round of the headline workload: B = 64 requests, gamma = 7,
 V = 151936 bf16 logits, full-q verification with the SpecKV draft signals.
 The metric is verify rounds/s (whole job, all ranks); the roofline is the HBM
-bandwidth of the statistics kernel on the bytes the method must read.
+bandwidth of the verify kernel on the bytes the method must read.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -134,7 +134,7 @@ class ClockSampler:
 
 def source_sha() -> str:
     h = hashlib.sha256()
-    for rel in ("speculative_decoding_verification_26_gb300/csrc/stats.cu",
+    for rel in ("speculative_decoding_verification_26_gb300/csrc/verify.cu",
                 "speculative_decoding_verification_26_gb300/csrc/common.cuh"):
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
@@ -142,9 +142,9 @@ def source_sha() -> str:
 
 
 def profiled_traffic():
-    """Per-launch DRAM bytes of the statistics kernel from the committed ncu
+    """Per-launch DRAM bytes of the verify kernel from the committed ncu
     summary, if it was taken on the current kernel source; else None."""
-    path = os.path.join(ROOT, "profiles", "stats_kernel_m_traffic.txt")
+    path = os.path.join(ROOT, "profiles", "verify_kernel_b64_g7_v151936_traffic.txt")
     try:
         with open(path) as f:
             d = json.loads(f.read().split("\n---\n")[0])
@@ -285,7 +285,7 @@ def run_ours(args):
     rounds_all = sum_over_ranks(float(K), world, dev)
     value = job_rate(rounds_all, t_max)
 
-    # statistics-kernel duration, live, with events around that kernel only
+    # verify-kernel duration, live, with events around that kernel only
     nprof = min(K, 200)
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nprof)]
     for a, b in evs:
@@ -296,11 +296,11 @@ def run_ours(args):
         sv.profile_next_call(*evs[k])
         step(k)
     torch.cuda.synchronize()
-    t_stats = statistics.mean(a.elapsed_time(b) for a, b in evs) / 1e3
+    t_kern = statistics.mean(a.elapsed_time(b) for a, b in evs) / 1e3
     nsets = len(sets)
     N_bytes = statistics.mean(rows_needed[k % nsets] for k in range(nprof)) * V * es
     hbm_peak, peak_kind = peaks()
-    achieved = N_bytes / t_stats / 1e9
+    achieved = N_bytes / t_kern / 1e9
     traffic = profiled_traffic()
 
     # end to end: pinned host inputs -> device, call, results -> host, every step
@@ -357,10 +357,10 @@ def run_ours(args):
                        "l2": f"{nsets} rotating input sets of {F_bytes/1e6:.0f} MB "
                              f"({nsets*F_bytes/1e9:.2f} GB > 4x L2)",
                        "parallelism": f"{world} independent request shards, no collective"},
-            "roofline": {"bound": "hbm", "kernel": "stats_kernel", "achieved": achieved, "peak": hbm_peak,
+            "roofline": {"bound": "hbm", "kernel": "verify_kernel", "achieved": achieved, "peak": hbm_peak,
                          "unit": "GB/s", "frac": achieved / hbm_peak, "peak_kind": peak_kind,
                          "traffic": traffic, "algorithmic_bytes_per_launch": N_bytes,
-                         "kernel_ms": t_stats * 1e3},
+                         "kernel_ms": t_kern * 1e3},
             "gpu_launches": int(launches),
             "clocks": clocks,
             "tokens_per_s": value * mean_committed,

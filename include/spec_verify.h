@@ -116,8 +116,9 @@ const char* spec_request_status_string(int bit);
 uint64_t spec_launch_count(void);
 
 /* Profiling aid.  The next verification call made by this host thread records
- * `begin_event` on its stream just before its statistics kernel (the kernel
- * that streams the logits) and `end_event` just after it; the hook then
+ * `begin_event` on its stream just before its verify kernel (the persistent
+ * kernel that streams the logits and settles every request) and `end_event`
+ * just after it; the hook then
  * clears itself.  Both are cudaEvent_t handles owned by the caller; NULL
  * clears the hook.  The event records sit between two launches of the call,
  * so that call's start-up overlap with the kernel before is lost. */

@@ -82,7 +82,7 @@ def launch_count() -> int:
 
 
 def profile_next_call(begin, end) -> None:
-    """Record torch.cuda.Event `begin`/`end` around the statistics kernel of
+    """Record torch.cuda.Event `begin`/`end` around the verify kernel of
     the next call made by this thread (see spec_profile_next_call)."""
     rc = lib().spec_profile_next_call(ctypes.c_void_p(begin.cuda_event), ctypes.c_void_p(end.cuda_event))
     if rc != OK:
