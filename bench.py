@@ -422,29 +422,23 @@ def run_reference(args):
         return dict(target=wl.target[idx], draft=wl.draft[idx], tok=wl.draft_tokens[idx], gamma=wl.gamma[idx],
                     T=wl.temperature[idx], u=wl.uniforms[idx])
 
-    # size each step (a sample of n_req requests) so the whole run stays within ~2 minutes
-    one = sub(np.arange(1))
+    # A step is one request of the round (a bounded sample of the workload:
+    # about 25 ms of fp64 work on one core).  The K timed steps run `cores` at a
+    # time, one request per OpenMP thread, so K = 20000 steps take ~30 s.
+    def run_steps(k0, n):
+        for j in range(0, n, cores):
+            idx = (np.arange(min(cores, n - j)) + k0 + j) % B
+            s = sub(idx)
+            o.verify_sample(s["target"], s["draft"], s["tok"], s["gamma"], s["T"], s["u"], want_signals=True,
+                            nthreads=min(cores, len(idx)))
+    run_steps(0, args.warmup)
     t0 = time.perf_counter()
-    o.verify_sample(one["target"], one["draft"], one["tok"], one["gamma"], one["T"], one["u"], want_signals=True,
-                    nthreads=1)
-    t_req = time.perf_counter() - t0                      # one request on one core
-    budget = 120.0 / max(1, args.steps + args.warmup)     # seconds per step
-    n_req = int(max(1, min(B, budget * cores / max(t_req, 1e-6))))
-    threads = min(cores, n_req)
-
-    def step(k):
-        idx = (np.arange(n_req) + k * n_req) % B
-        s = sub(idx)
-        o.verify_sample(s["target"], s["draft"], s["tok"], s["gamma"], s["T"], s["u"], want_signals=True,
-                        nthreads=threads)
-    for k in range(args.warmup):
-        step(k)
-    t0 = time.perf_counter()
-    for k in range(args.steps):
-        step(k)
+    run_steps(args.warmup, args.steps)
     dt = time.perf_counter() - t0
-    value = args.steps * n_req / B / dt
-    sample = f"each step: {n_req} of the {B} requests of one round (fp64, OpenMP over requests, {threads} threads)"
+    value = args.steps / B / dt
+    threads = min(cores, args.steps)
+    sample = (f"each step: 1 of the {B} requests of one round (fp64); the {args.steps} timed steps run "
+              f"{threads} at a time, OpenMP over requests")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
