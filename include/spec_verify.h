@@ -168,6 +168,46 @@ int spec_draft_signals(const void* draft_logits, int dtype, int B, int G, int V,
                        float* signals, float* row_signals, int32_t* status,
                        void* workspace, size_t workspace_bytes, spec_stream_t stream);
 
+/* Size of the library-owned scratch used by spec_verify_sample_static: 8 MiB.
+ * It holds the workspace of spec_workspace_bytes(B, G, V) <= this value, e.g.
+ * B <= 342 at G = 8, V = 151936, or B <= 348 at G = 7, V = 151936. */
+#define SPEC_STATIC_WORKSPACE_BYTES (8u << 20)
+
+/* spec_verify_sample without a caller workspace.  The pages have no
+ * counterpart: this is a convenience of the library, not part of the method.
+ *
+ * Arguments, outputs and results are those of spec_verify_sample (same
+ * meaning, layout and ownership); the call uses a file-scope device buffer
+ * of SPEC_STATIC_WORKSPACE_BYTES inside the library instead.  The call
+ * itself allocates nothing: no cudaMalloc, no cudaFree, no other allocating
+ * routine.  It is meant for callers that cannot allocate: a C caller with no
+ * device allocator of its own; a serving loop whose device memory is all
+ * held by a pool allocator, so that no free bytes are left for a workspace;
+ * a per-step decode path that must not pay cudaMalloc/cudaFree, which can
+ * synchronise the device and stall every other stream.
+ *
+ * Setup: the first call on each device (with that device current) looks up
+ * the buffer's device address once (cudaGetSymbolAddress; a failure returns
+ * SPEC_ERR_CUDA and the next call tries again) and configures the kernels,
+ * as the first call of any entry point does.  Make that first call before
+ * any stream capture begins.
+ * Contents: nothing in the buffer has to start at zero; every call's first
+ * kernel resets each counter and flag it reads.
+ * Sharing: every call of this entry point on one device uses the same
+ * buffer.  Two calls whose executions overlap on the device (different
+ * streams, or different host threads without ordering between them) race on
+ * it and corrupt each other's results.  Calls on one stream run one after
+ * the other and are safe.
+ * Errors: as spec_verify_sample, and SPEC_ERR_WORKSPACE (before any CUDA
+ * call) when spec_workspace_bytes(B, G, V) > SPEC_STATIC_WORKSPACE_BYTES. */
+int spec_verify_sample_static(const void* target_logits, const void* draft_logits, int dtype,
+                              int B, int G, int V,
+                              const int32_t* draft_tokens, const int32_t* gamma,
+                              const float* temperature, const float* uniforms,
+                              int32_t* accept_len, int32_t* tokens,
+                              float* signals, float* accept_prob, int32_t* status,
+                              spec_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

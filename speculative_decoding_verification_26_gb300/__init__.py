@@ -12,3 +12,4 @@ from ._lib import (  # noqa: F401
     status_string,
     verify_greedy, verify_onehot, verify_sample, workspace, workspace_bytes,
 )
+from ._lib import STATIC_WORKSPACE_BYTES, verify_sample_static  # noqa: F401

@@ -255,3 +255,46 @@ def draft_signals(draft, gamma, temperature, *, row_signals=False, ws=None, out=
     if rs is not None:
         r["row_signals"] = rs
     return r
+
+
+STATIC_WORKSPACE_BYTES = 8 << 20
+
+
+def verify_sample_static(target, draft, draft_tokens, gamma, temperature, uniforms, *, signals=True,
+                         accept_prob=False, out=None):
+    """verify_sample on the library's own static scratch (spec_verify_sample_static).
+
+    The C call allocates nothing; this wrapper allocates outputs only when
+    `out` does not supply them.  Calls on one device must not overlap."""
+    torch = _torch()
+    L = lib()
+    f = L.spec_verify_sample_static
+    if f.argtypes is None:
+        P, I = ctypes.c_void_p, ctypes.c_int
+        f.argtypes = [P, P, I, I, I, I, P, P, P, P, P, P, P, P, P, P]
+        f.restype = I
+    B, Gp1, V = target.shape
+    G = Gp1 - 1
+    dev = target.device
+    _check(target, "target", device=dev)
+    _check(draft, "draft", target.dtype, (B, G, V), dev)
+    _check(draft_tokens, "draft_tokens", torch.int32, (B, G), dev)
+    _check(gamma, "gamma", torch.int32, (B,), dev)
+    _check(temperature, "temperature", torch.float32, (B,), dev)
+    _check(uniforms, "uniforms", torch.float32, (B, G + 1), dev)
+    o = out or {}
+    acc = _out(o, "accept_len", lambda: torch.empty(B, dtype=torch.int32, device=dev))
+    tok = _out(o, "tokens", lambda: torch.empty(B, G + 1, dtype=torch.int32, device=dev))
+    st = _out(o, "status", lambda: torch.empty(B, dtype=torch.int32, device=dev))
+    sig = (_out(o, "signals", lambda: torch.empty(B, 4, dtype=torch.float32, device=dev))) if signals else None
+    ap = (_out(o, "accept_prob", lambda: torch.empty(B, G, dtype=torch.float32, device=dev))) if accept_prob else None
+    rc = f(_ptr(target), _ptr(draft), _dtype_code(target), B, G, V, _ptr(draft_tokens), _ptr(gamma),
+           _ptr(temperature), _ptr(uniforms), _ptr(acc), _ptr(tok), _ptr(sig), _ptr(ap), _ptr(st), _stream(dev))
+    if rc != OK:
+        raise SpecVerifyError(rc, "spec_verify_sample_static")
+    r = {"accept_len": acc, "tokens": tok, "status": st}
+    if sig is not None:
+        r["signals"] = sig
+    if ap is not None:
+        r["accept_prob"] = ap
+    return r

@@ -167,6 +167,28 @@ int run(const Call& c) {
   return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 
+// Library-owned scratch of spec_verify_sample_static (one per device: a
+// __device__ variable lives in each context that loads the module).
+static __device__ __align__(256) unsigned char g_static_ws[SPEC_STATIC_WORKSPACE_BYTES];
+
+// Device address of g_static_ws on the current device, looked up once per
+// device with that device current.
+void* g_static_addr[kMaxDevices] = {};
+
+int static_workspace(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SPEC_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return SPEC_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_static_addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_ws) != cudaSuccess || p == nullptr) return SPEC_ERR_CUDA;
+    g_static_addr[dev] = p;
+  }
+  *out = g_static_addr[dev];
+  return SPEC_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -229,6 +251,23 @@ int spec_verify_sample(const void* target_logits, const void* draft_logits, int 
                        spec_stream_t stream) {
   Call c{MODE_SAMPLE, target_logits, draft_logits, dtype, B, G, V, draft_tokens, gamma, temperature, uniforms,
          accept_len, tokens, status, signals, nullptr, accept_prob, workspace, workspace_bytes,
+         reinterpret_cast<cudaStream_t>(stream)};
+  return run(c);
+}
+
+int spec_verify_sample_static(const void* target_logits, const void* draft_logits, int dtype, int B, int G,
+                              int V, const int32_t* draft_tokens, const int32_t* gamma, const float* temperature,
+                              const float* uniforms, int32_t* accept_len, int32_t* tokens, float* signals,
+                              float* accept_prob, int32_t* status, spec_stream_t stream) {
+  // size checks first: nothing touches the device when they fail
+  const size_t need = spec_workspace_bytes(B, G, V);
+  if (need == 0) return SPEC_ERR_INVALID_ARG;
+  if (need > (size_t)SPEC_STATIC_WORKSPACE_BYTES) return SPEC_ERR_WORKSPACE;
+  void* ws = nullptr;
+  const int rc = static_workspace(&ws);
+  if (rc != SPEC_OK) return rc;
+  Call c{MODE_SAMPLE, target_logits, draft_logits, dtype, B, G, V, draft_tokens, gamma, temperature, uniforms,
+         accept_len, tokens, status, signals, nullptr, accept_prob, ws, (size_t)SPEC_STATIC_WORKSPACE_BYTES,
          reinterpret_cast<cudaStream_t>(stream)};
   return run(c);
 }
