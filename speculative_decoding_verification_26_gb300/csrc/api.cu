@@ -126,26 +126,15 @@ int run(const Call& c) {
   P.req_flags = reinterpret_cast<int*>(ws + L.req_flags);
   P.known_reject = reinterpret_cast<int*>(ws + L.known_reject);
   P.row_list = reinterpret_cast<int*>(ws + L.row_list);
-  P.row_arr = reinterpret_cast<unsigned*>(ws + L.row_arr);
-  P.row_done = reinterpret_cast<int*>(ws + L.row_done);
-  P.row_stats = reinterpret_cast<RowStats*>(ws + L.row_stats);
-  P.row_xy = reinterpret_cast<float*>(ws + L.row_xy);
-  P.parts = reinterpret_cast<Part*>(ws + L.parts);
-  P.pair_arr = reinterpret_cast<unsigned*>(ws + L.pair_arr);
-  P.pair_res = reinterpret_cast<int*>(ws + L.pair_res);
-  P.pair_a = reinterpret_cast<float*>(ws + L.pair_a);
   P.req_scale = reinterpret_cast<float*>(ws + L.req_scale);
   P.req_gam = reinterpret_cast<int*>(ws + L.req_gam);
-  P.req_state = reinterpret_cast<unsigned long long*>(ws + L.req_state);
-  P.req_cnt = reinterpret_cast<unsigned*>(ws + L.req_cnt);
-  P.req_k = reinterpret_cast<int*>(ws + L.req_k);
   P.req_status = reinterpret_cast<int*>(ws + L.req_status);
-  P.req_z = reinterpret_cast<int*>(ws + L.req_z);
-  P.rsum_arr = reinterpret_cast<unsigned*>(ws + L.rsum_arr);
-  P.rsum_parts = reinterpret_cast<double*>(ws + L.rsum_parts);
-  P.rsum_gs = reinterpret_cast<float*>(ws + L.rsum_gs);
-  P.search = reinterpret_cast<DrawDesc*>(ws + L.search);
-  P.dq = reinterpret_cast<DynItem*>(ws + L.dq);
+  P.req_fin = reinterpret_cast<unsigned*>(ws + L.req_fin);
+  P.cparts = reinterpret_cast<tword*>(ws + L.cparts);
+  P.dsum = reinterpret_cast<tword*>(ws + L.dsum);
+  P.gsum = reinterpret_cast<tword*>(ws + L.gsum);
+  P.dd = reinterpret_cast<tword*>(ws + L.dd);
+  P.dq = reinterpret_cast<tword*>(ws + L.dq);
   P.nrows = L.nrows; P.nch = L.nch; P.nres = L.nres; P.dq_cap = L.dq_cap;
   P.aligned_rows = ((size_t)c.V * es) % 16 == 0 && aligned(c.target, 16) && aligned(c.draft, 16);
 

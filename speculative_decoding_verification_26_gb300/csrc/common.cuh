@@ -37,26 +37,25 @@ enum ItemType : int {
 // target row k (bonus draw; one-hot residual with the draft token removed)
 enum DrawKind : int { DK_RESID = 1, DK_P = 2 };
 
-// state word bits of a request: bit i (< 31) position i evaluated, bit 32+i
-// position i accepted, bit 63 the bonus row complete
-constexpr unsigned long long kBonusBit = 1ull << 63;
 
 // ---------------------------------------------------------------------------
 // geometry
 
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
-constexpr int kEpiWarps = 3;                           // epilogue warps (items alternate)
-constexpr int kStatsThreads = kConsumerThreads + 32 * (1 + kEpiWarps);   // + producer + epilogue warps
+constexpr int kEpiWarps = 2;                           // epilogue warps (items alternate)
+constexpr int kStatsThreads = kConsumerThreads + 32 * (2 + kEpiWarps);   // + producer, epilogue, owner warps
 constexpr int kStageBytes = 16384;                      // one bulk copy
 constexpr int kStages = 6;                              // ring depth per CTA
 constexpr int kChunkBytes = 4 * kStageBytes;            // one work item of a row
 constexpr int kEpiSlots = 12;                           // consumer -> epilogue ring (multiple of kEpiWarps)
-constexpr int kGroupVecs = 8;                           // residual group: 8 vectors (64 bf16 / 32 fp32 tokens)
-constexpr int kGroupsPerStage = kStageBytes / 16 / kGroupVecs;   // 128
-constexpr uint32_t kSkipInc = 1u << 20;                 // arrival mark of a skipped chunk
-constexpr uint32_t kCountMask = kSkipInc - 1;
+constexpr int kGroupVecs = 32;                          // draw group: one warp's 32 vectors (256 bf16 / 128 fp32 tokens)
+constexpr int kGroupsPerStage = kStageBytes / 16 / kGroupVecs;   // 32
+constexpr int kPartWords = 5;                           // tagged words of a chunk partial: m, s, t, idx, x_y
+constexpr int kDrawWords = 8;                           // tagged words of a draw descriptor
 constexpr int kNoReject = 0x7fffffff;
+constexpr unsigned kEpochMax = 0x3ffffff0u;             // tags are 4 * epoch + kind (kind < 4)
+constexpr unsigned long long kWorkspaceMagic = 0x5356455246595631ull;
 // Every bounded wait counts SM clock cycles (clock64 is a register of the SM
 // and costs a few cycles to read; the global timer is read from outside the
 // SM and delays the reading warp by about a microsecond under load).
@@ -82,12 +81,11 @@ struct alignas(16) RowStats {
 // workspace layout (offsets in bytes, 256-aligned)
 
 struct Layout {
-  size_t hdr, req_flags, known_reject, row_list, row_arr, row_done, row_stats, row_xy, parts, pair_arr,
-      pair_res, pair_a, req_scale, req_gam, req_state, req_cnt, req_k, req_status, req_z, rsum_arr, rsum_parts, rsum_gs, search, dq,
+  size_t hdr, req_flags, known_reject, row_list, req_scale, req_gam, req_status, req_fin, cparts, dsum, gsum, dd, dq,
       total;
   int nrows;      // B*(G+1) + B*G row ids
   int nch;        // statistics chunks per row
-  int nres;       // residual chunks per row (one stage each)
+  int nres;       // draw slices per row (one stage each)
   int dq_cap;     // dynamic queue capacity
 };
 
@@ -104,25 +102,25 @@ struct Header {
   Counter dq_tail;      // dynamic items reserved
   Counter done;         // requests whose outputs are written
   Counter error;        // SPEC_ST_TIMEOUT when any wait gave up
-  Counter misc;         // n_items, n_valid, exited, n_uncertain (rarely written)
+  Counter misc;         // n_items, n_valid, exited, n_uncertain, epoch, magic (rarely written)
 };
 #define HDR_N_ITEMS(h) ((h)->misc.pad[0])
 #define HDR_N_VALID(h) ((h)->misc.pad[1])
 #define HDR_EXITED(h) ((h)->misc.pad[2])
 #define HDR_UNCERTAIN(h) ((h)->misc.pad[3])
+#define HDR_EPOCH(h) ((h)->misc.pad[4])
+#define HDR_MAGIC(h) (*reinterpret_cast<unsigned long long*>(&(h)->misc.pad[7]))   // byte offset 32: 8-aligned
 
-// a dynamically created work item (type 0 = slot reserved, not yet written)
-struct alignas(16) DynItem {
-  int type, b, c, aux;
-};
-
-// the draw of a request (written before its IT_DSUM items)
-struct alignas(16) DrawDesc {
-  int kind;        // DK_RESID or DK_P
-  int k;           // position of the draw (first reject, or gamma_b)
-  int excl;        // token left out (one-hot residual), or -1
-  int status;      // informational status bits (SPEC_ST_ZERO_RESIDUAL)
-};
+// Data that crosses CTAs travels in tagged 64-bit words: payload in the high
+// 32 bits, the tag in the low 32 bits: 4 * epoch for chunk partials and
+// queue entries, 4 * epoch + 1 + round for the words of a draw round (one
+// tag space per kind of word, so that a word left by an earlier call in an
+// array laid out differently can never carry a tag of this call).  An aligned 64-bit relaxed access is
+// single-copy atomic, so a reader that sees the current tag has the payload
+// written in this call, whatever the order in which words become visible:
+// no fence and no counter is needed to publish them.  Every call has a new
+// epoch, so words left by earlier calls are never mistaken for new ones.
+typedef unsigned long long tword;
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
@@ -142,26 +140,15 @@ __host__ inline Layout make_layout(int B, int G, int V, int dtype) {
   L.req_flags = o;    o = align256(o + sizeof(int) * B);
   L.known_reject = o; o = align256(o + sizeof(int) * B);
   L.row_list = o;     o = align256(o + sizeof(int) * nrows);
-  L.row_arr = o;      o = align256(o + sizeof(unsigned) * nrows);
-  L.row_done = o;     o = align256(o + sizeof(int) * nrows);
-  L.row_stats = o;    o = align256(o + sizeof(RowStats) * nrows);
-  L.row_xy = o;       o = align256(o + sizeof(float) * nrows);
-  L.parts = o;        o = align256(o + sizeof(Part) * (size_t)nrows * L.nch);
-  L.pair_arr = o;     o = align256(o + sizeof(unsigned) * B * (G + 1));
-  L.pair_res = o;     o = align256(o + sizeof(int) * B * (G + 1));
-  L.pair_a = o;       o = align256(o + sizeof(float) * B * (G + 1));
   L.req_scale = o;    o = align256(o + sizeof(float) * B);
   L.req_gam = o;      o = align256(o + sizeof(int) * B);
-  L.req_state = o;    o = align256(o + sizeof(unsigned long long) * B);
-  L.req_cnt = o;      o = align256(o + sizeof(unsigned) * 2 * B);
-  L.req_k = o;        o = align256(o + sizeof(int) * B);
   L.req_status = o;   o = align256(o + sizeof(int) * B);
-  L.req_z = o;        o = align256(o + sizeof(int) * B);
-  L.rsum_arr = o;     o = align256(o + sizeof(unsigned) * B);
-  L.rsum_parts = o;   o = align256(o + sizeof(double) * (size_t)B * L.nres);
-  L.rsum_gs = o;      o = align256(o + sizeof(float) * (size_t)B * L.nres * kGroupsPerStage);
-  L.search = o;       o = align256(o + sizeof(DrawDesc) * B);
-  L.dq = o;           o = align256(o + sizeof(DynItem) * (size_t)L.dq_cap);
+  L.req_fin = o;      o = align256(o + sizeof(unsigned) * B);
+  L.cparts = o;       o = align256(o + sizeof(tword) * (size_t)nrows * L.nch * kPartWords);
+  L.dsum = o;         o = align256(o + sizeof(tword) * 2 * (size_t)B * L.nres);
+  L.gsum = o;         o = align256(o + sizeof(tword) * (size_t)B * L.nres * kGroupsPerStage);
+  L.dd = o;           o = align256(o + sizeof(tword) * kDrawWords * (size_t)B);
+  L.dq = o;           o = align256(o + sizeof(tword) * 2 * (size_t)L.dq_cap);
   L.total = o;
   return L;
 }
@@ -186,29 +173,18 @@ struct Params {
   float* accept_prob;
   // workspace views
   Header* hdr;
-  int* req_flags;
-  int* known_reject;
-  int* row_list;
-  unsigned* row_arr;
-  int* row_done;
-  RowStats* row_stats;
-  float* row_xy;                 // logit of the row at its draft token (rows i < gamma_b)
-  Part* parts;
-  unsigned* pair_arr;
-  int* pair_res;
-  float* pair_a;
+  int* req_flags;                // error bits found by the plan kernel
+  int* known_reject;             // earliest decided reject (early exit), relaxed
+  int* row_list;                 // position-major row schedule
   float* req_scale;              // log2(e) / T_b (plan kernel)
   int* req_gam;                  // gamma_b (plan kernel)
-  unsigned long long* req_state;
-  unsigned* req_cnt;             // [B][2]: draft rows complete, conditions met
-  int* req_k;
-  int* req_status;
-  int* req_z;
-  unsigned* rsum_arr;
-  double* rsum_parts;
-  float* rsum_gs;                // residual sums per group of kGroupVecs vectors
-  DrawDesc* search;
-  DynItem* dq;
+  int* req_status;               // kFinished: settled by the plan kernel
+  unsigned* req_fin;             // epoch of the call whose outputs were written
+  tword* cparts;                 // [nrows][nch][kPartWords] chunk partials
+  tword* dsum;                   // [B][nres][2] draw slice sums (fp64 as hi, lo)
+  tword* gsum;                   // [B][nres][kGroupsPerStage] draw group sums (fp32)
+  tword* dd;                     // [B][kDrawWords] draw descriptors
+  tword* dq;                     // [dq_cap][2] dynamic work queue
   int nrows, nch, nres, dq_cap;
 };
 
@@ -306,20 +282,28 @@ __device__ __forceinline__ void bulk_load(void* smem_dst, const void* gmem_src, 
       : "memory");
 }
 
-__device__ __forceinline__ unsigned atom_add_acqrel(unsigned* p, unsigned v) {
-  unsigned old;
-  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-  return old;
-}
 
-__device__ __forceinline__ void red_add_release(unsigned* p, unsigned v) {
-  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
 
 __device__ __forceinline__ int ld_relaxed(const int* p) {
   int v;
   asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
+}
+
+// tagged words (see tword)
+__device__ __forceinline__ tword tw_make(unsigned payload, unsigned tag) {
+  return ((tword)payload << 32) | (tword)tag;
+}
+__device__ __forceinline__ bool tw_ok(tword w, unsigned tag) { return (unsigned)w == tag; }
+__device__ __forceinline__ unsigned tw_u32(tword w) { return (unsigned)(w >> 32); }
+__device__ __forceinline__ float tw_f32(tword w) { return __uint_as_float((unsigned)(w >> 32)); }
+__device__ __forceinline__ tword ld_tw(const tword* p) {
+  tword v;
+  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_tw(tword* p, tword v) {
+  asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }

@@ -117,6 +117,18 @@ __device__ inline int rows_for(const Block& bl, int gam) {
 
 }  // namespace
 
+// Words of the tagged arrays, for the one-time clear of a new workspace.
+__device__ inline void clear_tagged(const Params& P, int tid, int nth) {
+  const size_t n_parts = (size_t)P.nrows * P.nch * kPartWords;
+  const size_t n_dsum = 2 * (size_t)P.B * P.nres;
+  const size_t n_gsum = (size_t)P.B * P.nres * kGroupsPerStage;
+  for (size_t j = tid; j < n_parts; j += nth) P.cparts[j] = 0ull;
+  for (size_t j = tid; j < n_dsum; j += nth) P.dsum[j] = 0ull;
+  for (size_t j = tid; j < n_gsum; j += nth) P.gsum[j] = 0ull;
+  for (size_t j = tid; j < (size_t)kDrawWords * P.B; j += nth) P.dd[j] = 0ull;
+  for (size_t j = tid; j < 2 * (size_t)P.dq_cap; j += nth) P.dq[j] = 0ull;
+}
+
 __global__ void __launch_bounds__(1024) plan_kernel(Params P) {
   griddep_launch();
   const int B = P.B, G = P.G, tid = threadIdx.x, nth = blockDim.x;
@@ -126,24 +138,25 @@ __global__ void __launch_bounds__(1024) plan_kernel(Params P) {
   __shared__ Block s_blk[64];
   __shared__ int s_nb;
   __shared__ unsigned s_settled;
+  __shared__ unsigned s_epoch;
+  __shared__ int s_clear;
 
-  if (tid == 0) s_settled = 0u;
-  for (int j = tid; j < P.nrows; j += nth) {
-    P.row_arr[j] = 0u;
-    P.row_done[j] = 0;
+  // The epoch of this call: one more than the last call's on this workspace.
+  // A workspace without the magic word (first use) or at the end of the
+  // epoch range has its tagged arrays cleared, so that no old word carries
+  // a tag this call will use (tag 0 is never used).
+  if (tid == 0) {
+    s_settled = 0u;
+    const bool known = HDR_MAGIC(P.hdr) == kWorkspaceMagic;
+    unsigned e = known ? HDR_EPOCH(P.hdr) + 1u : 1u;
+    s_clear = !known || e >= kEpochMax || e == 0u;
+    if (s_clear) e = 1u;
+    s_epoch = e;
   }
-  for (int j = tid; j < B * (G + 1); j += nth) {
-    P.pair_arr[j] = 0u;
-    P.pair_res[j] = PC_NONE;
-    P.pair_a[j] = qnan();
-  }
-  for (int j = tid; j < P.dq_cap; j += nth) P.dq[j].type = 0;
   __syncthreads();
+  if (s_clear) clear_tagged(P, tid, nth);
   for (int b = tid; b < B; b += nth) {
     P.known_reject[b] = kNoReject;
-    P.req_state[b] = 0ull;
-    P.rsum_arr[b] = 0u;
-    P.req_k[b] = 0;
     int st = 0;
     const int gam = gamma_of(P, b);
     if (gam < 0 || gam > G) st |= SPEC_ST_BAD_GAMMA;
@@ -151,9 +164,6 @@ __global__ void __launch_bounds__(1024) plan_kernel(Params P) {
     P.req_flags[b] = st;
     P.req_gam[b] = gam;
     P.req_scale[b] = (P.mode != MODE_GREEDY && st == 0) ? scale_of(P.temperature[b]) : 0.f;
-    // a request with no signal rows has its signal condition met already
-    P.req_cnt[2 * b] = 0u;
-    P.req_cnt[2 * b + 1] = (P.signals_on && st == 0 && gam == 0) ? 1u : 0u;
     if (st != 0) {
       write_void_outputs(P, b, st, 0, 1);
       P.req_status[b] = st | kFinished;
@@ -188,6 +198,8 @@ __global__ void __launch_bounds__(1024) plan_kernel(Params P) {
     for (int k = 0; k < nb; ++k) { s_off[k] = acc; acc += s_count[k]; }
     s_off[nb] = acc;
     P.hdr->queue.v = 0u;
+    HDR_EPOCH(P.hdr) = s_epoch;
+    HDR_MAGIC(P.hdr) = kWorkspaceMagic;
     HDR_N_ITEMS(P.hdr) = (unsigned)acc * (unsigned)P.nch;
     P.hdr->error.v = 0u;
     HDR_UNCERTAIN(P.hdr) = 0u;
@@ -242,8 +254,9 @@ struct StageDesc {
   int flags, head0, nhead, tail0;
   int ntail, y, aux, n_elems;       // n_elems: direct stages
   long long src_elem;               // direct stages: flat element offset of the source
-  float c, m1, s1, m2;              // scale; row statistics of the rows used
-  float s2, tl;                     // search: target weight within the chunk (fp32 view)
+  float c, m1, s1, m2;              // scale; row statistics of the rows used (draw)
+  float s2;
+  unsigned tag;                     // draw: tag of the draw's words
   int pad[2];
 };
 
@@ -252,12 +265,11 @@ struct EpiSlot {
   int type, row_id, b, i;
   int kind, chunk, term, z;
   float xy;
-  int pad[3];
+  unsigned tag;                     // draw: tag of the draw's words
+  int pad[2];
   double dsum[kConsumerWarps];      // draw-weight sums per consumer warp (IT_DSUM)
   Part part[kConsumerWarps];        // statistics per consumer warp
 };
-
-constexpr int kVecPerStage = kStageBytes / 16;     // 1024
 
 struct __align__(128) VSmem {
   unsigned char ring[kStages][kStageBytes];
@@ -539,28 +551,20 @@ __device__ __forceinline__ unsigned ld_relaxed_u32(const unsigned* p) {
   asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
-__device__ __forceinline__ int ld_acquire_i32(const int* p) {
-  int v;
-  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-__device__ __forceinline__ void st_release_i32(int* p, int v) {
-  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-__device__ __forceinline__ unsigned long long atom_or_acqrel_u64(unsigned long long* p, unsigned long long v) {
-  unsigned long long old;
-  asm volatile("atom.acq_rel.gpu.global.or.b64 %0, [%1], %2;" : "=l"(old) : "l"(p), "l"(v) : "memory");
-  return old;
-}
 __device__ __forceinline__ void consumer_bar() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumerThreads) : "memory"); }
 
 // ---------------------------------------------------------------------------
 // device work queue
 
-// Reserve n consecutive entries (chunk indices c0 .. c0+n-1); every lane of
-// the calling warp writes the entries j = lane, lane + 32, ... (payload
-// first, then the type with release, which publishes the entry).  Warp-wide.
-__device__ void enqueue_items(const Params& P, int n, int type, int b, int c0, int aux, int lane) {
+// Tags of this call's words (see tword).
+__device__ __forceinline__ unsigned draw_tag(unsigned epoch, int round) { return 4u * epoch + 1u + (unsigned)round; }
+__device__ __forceinline__ unsigned part_tag(unsigned epoch) { return 4u * epoch; }   // partials, queue entries
+
+// An entry is two tagged words: (b) and (slice | round << 30), both with the
+// call's partial tag.  The owner of request b reserves n consecutive entries
+// (slices 0 .. n-1) and every lane of its warp writes entries lane,
+// lane + 32, ...  Warp-wide.
+__device__ void enqueue_draw(const Params& P, int n, int b, int round, unsigned epoch, int lane) {
   unsigned base = 0;
   if (lane == 0) base = atomicAdd(&P.hdr->dq_tail.v, (unsigned)n);
   base = __shfl_sync(0xffffffffu, base, 0);
@@ -570,33 +574,25 @@ __device__ void enqueue_items(const Params& P, int n, int type, int b, int c0, i
       atomicOr(&P.hdr->error.v, (unsigned)SPEC_ST_TIMEOUT);
       continue;
     }
-    DynItem* e = P.dq + slot;
-    __stcg(&e->b, b);
-    __stcg(&e->c, c0 + j);
-    __stcg(&e->aux, aux);
-    st_release_i32(&e->type, type);
+    st_tw(P.dq + 2 * (size_t)slot, tw_make((unsigned)b, part_tag(epoch)));
+    st_tw(P.dq + 2 * (size_t)slot + 1, tw_make((unsigned)j | ((unsigned)round << 30), part_tag(epoch)));
   }
   __syncwarp();
 }
 
 // Dynamic items are handed out by ticket: a producer holds one ticket (an
 // index into the queue, from one atomicAdd) and takes the item stored there
-// once an enqueuer has published it.  Tickets past the last item are never
-// served; their holders leave when every request is done.
-__device__ __forceinline__ int ticket_peek(const Params& P, unsigned ticket) {   // relaxed, non-blocking
-  if (ticket >= (unsigned)P.dq_cap) return 0;
-  int v;
-  asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(&P.dq[ticket].type) : "memory");
-  return v;
-}
+// once both of its words carry this call's tag.  Tickets past the last item
+// are never served; their holders leave when every request is done.
+struct DynItem {
+  int b, slice, round;
+};
 
-__device__ __forceinline__ void ticket_take(const Params& P, unsigned ticket, DynItem& it) {
-  const DynItem* e = P.dq + ticket;
-  it.type = ld_acquire_i32(&e->type);          // orders the payload reads after the publish
-  it.b = __ldcg(&e->b);
-  it.c = __ldcg(&e->c);
-  it.aux = __ldcg(&e->aux);
-}
+
+// The draw descriptor of request b (owner -> producers), kDrawWords tagged
+// words: kind | k << 8, excluded token (one-hot), m_p, s_p, m_q, s_q, scale.
+enum DrawWord : int { DW_KIND = 0, DW_EXCL, DW_M1, DW_S1, DW_M2, DW_S2, DW_C, DW_PAD };
+
 
 // ---------------------------------------------------------------------------
 // producer
@@ -739,26 +735,43 @@ __device__ __forceinline__ bool put_row_range(const Params& P, VSmem& S, int& st
   return put_stage(S, stage, phase, d, 0, 0u);
 }
 
-// A draw slice: item c = slice index, aux = position k | kind << 8 | excl flag << 9.
+// A draw slice: rows k of the request (the descriptor, written by the owner
+// before the queue entries, is read until all its words carry the draw's
+// tag; bounded).
 template <int DT>
-__device__ bool stage_dyn_item(const Params& P, VSmem& S, int& stage, uint32_t& phase, const DynItem& it) {
-  const int G = P.G, V = P.V, se = stage_elems(DT);
-  const int b = it.b, k = it.aux & 0xff, kind = (it.aux >> 8) & 1 ? DK_P : DK_RESID, ch = it.c;
-  const bool has_excl = (it.aux >> 9) & 1;
+__device__ bool stage_dyn_item(const Params& P, VSmem& S, int& stage, uint32_t& phase, const DynItem& it,
+                               unsigned epoch) {
+  const int V = P.V, se = stage_elems(DT);
+  const int b = it.b, ch = it.slice;
+  const unsigned tag = draw_tag(epoch, it.round);
+  const tword* dd = P.dd + (size_t)b * kDrawWords;
+  tword w[DW_PAD];
+  const long long c0 = clock64();
+  while (true) {
+    bool ok = true;
+#pragma unroll
+    for (int j = 0; j < DW_PAD; ++j) {
+      w[j] = ld_tw(dd + j);
+      ok &= tw_ok(w[j], tag);
+    }
+    if (ok) break;
+    if (aborted(S) || clock64() - c0 > kWaitLimitCycles) return false;
+  }
+  const unsigned kk = tw_u32(w[DW_KIND]);
+  const int kind = (int)(kk & 0xffu), k = (int)(kk >> 8);
   StageDesc d{};
   d.type = IT_DSUM;
   d.b = b;
   d.i = k;
   d.chunk = ch;
   d.aux = kind;
-  d.c = __ldg(P.req_scale + b);
-  const RowStats tr = ldcg_stats(P.row_stats + target_row_id(b, k, G));
-  d.m1 = tr.m; d.s1 = tr.s;
-  d.y = has_excl ? P.draft_tokens[(size_t)b * G + k] : -1;
+  d.c = tw_f32(w[DW_C]);
+  d.m1 = tw_f32(w[DW_M1]); d.s1 = tw_f32(w[DW_S1]);
+  d.m2 = tw_f32(w[DW_M2]); d.s2 = tw_f32(w[DW_S2]);
+  d.y = (int)tw_u32(w[DW_EXCL]);
+  d.tag = tag;
   const int e0 = ch * se, e1 = min(e0 + se, V);
   if (kind == DK_RESID) {
-    const RowStats dr = ldcg_stats(P.row_stats + draft_row_id(b, k, P.B, G));
-    d.m2 = dr.m; d.s2 = dr.s;
     d.flags = F_FIRST;
     if (!put_row_range<DT>(P, S, stage, phase, d, KIND_TARGET, b, k, e0, e1)) return false;
     d.flags = F_LAST;
@@ -769,7 +782,7 @@ __device__ bool stage_dyn_item(const Params& P, VSmem& S, int& stage, uint32_t& 
 }
 
 template <int DT, bool GREEDY>
-__device__ void producer_role(const Params& P, VSmem& S) {
+__device__ void producer_role(const Params& P, VSmem& S, unsigned epoch) {
   const unsigned n_items = HDR_N_ITEMS(P.hdr);
   const unsigned n_valid = HDR_N_VALID(P.hdr);
   int stage = 0;
@@ -792,25 +805,31 @@ __device__ void producer_role(const Params& P, VSmem& S) {
     // starve the other (late target rows and early draws are both on the
     // critical path of some request)
     bool did = false;
-    const int peek = dyn ? ticket_peek(P, ticket) : 0;     // in flight while staging
+    // the ticket's entry words, in flight while the static item is staged
+    tword t0 = 0ull, t1 = 0ull;
+    if (dyn && ticket < (unsigned)P.dq_cap) {
+      t0 = ld_tw(P.dq + 2 * (size_t)ticket);
+      t1 = ld_tw(P.dq + 2 * (size_t)ticket + 1);
+    }
     if (cur.valid) {
       // loads for the next items, issued before the (blocking) staging
       const RawMeta nxt = item_meta_raw<GREEDY>(P, q_next, rid_next, n_items);
       const int rid2 = item_row(P, q2, n_items);
       const unsigned q3 = q2 < n_items ? atomicAdd(&P.hdr->queue.v, 1u) : q2;
-      if (cur.skip) red_add_release(P.row_arr + cur.rid, 1u + kSkipInc);
-      else ok = stage_stats_item<DT, GREEDY>(P, S, stage, phase, cur);
+      if (!cur.skip) ok = stage_stats_item<DT, GREEDY>(P, S, stage, phase, cur);   // a voided row is not read
       cur = finish_meta(P, nxt, n_items);
       q_next = q2;
       rid_next = rid2;
       q2 = q3;
       did = true;
     }
-    if (ok && peek != 0) {
+    if (ok && tw_ok(t0, part_tag(epoch)) && tw_ok(t1, part_tag(epoch))) {
       DynItem it;
-      ticket_take(P, ticket, it);
+      it.b = (int)tw_u32(t0);
+      it.slice = (int)(tw_u32(t1) & 0x3fffffffu);
+      it.round = (int)(tw_u32(t1) >> 30);
       ticket = atomicAdd(&P.hdr->dq_head.v, 1u);
-      ok = stage_dyn_item<DT>(P, S, stage, phase, it);
+      ok = stage_dyn_item<DT>(P, S, stage, phase, it, epoch);
       did = true;
     }
     if (did) {
@@ -819,7 +838,8 @@ __device__ void producer_role(const Params& P, VSmem& S) {
       continue;
     }
     // nothing to stage right now: finished, or draw items are still to come
-    if (ld_relaxed_u32(&P.hdr->done.v) >= n_valid) break;
+    // (calls without draws are finished when the static items are)
+    if (!dyn || ld_relaxed_u32(&P.hdr->done.v) >= n_valid) break;
     if (ld_relaxed_u32(&P.hdr->error.v) != 0u) break;
     const long long now = clock64();
     if (idle_since < 0) idle_since = now;
@@ -990,8 +1010,8 @@ __device__ void consumer_role(const Params& P, VSmem& S, int cw, int lane) {
     ResidW R;
     R.c = d.c; R.mpc = d.m1 * d.c; R.mqc = d.m2 * d.c; R.rp = 1.f / d.s1; R.rq = 1.f / d.s2;
     const float mc = d.m1 * d.c;
-    float* gs_out = P.rsum_gs + ((size_t)d.b * P.nres + d.chunk) * kGroupsPerStage;
-    double dsum = 0.0;
+    tword* gs_out = P.gsum + ((size_t)d.b * P.nres + d.chunk) * kGroupsPerStage;
+    double dsum = 0.0;                  // lane 0: this warp's groups, in q order
 #pragma unroll
     for (int q = 0; q < kVecPerThread; ++q) {
       const int v = tid + q * kConsumerThreads;
@@ -1016,91 +1036,148 @@ __device__ void consumer_role(const Params& P, VSmem& S, int cw, int lane) {
       float g;
       if (N == 8) g = ((e[0] + e[1]) + (e[2] + e[3])) + ((e[4] + e[5]) + (e[6] + e[7]));
       else g = (e[0] + e[1]) + (e[2] + e[3]);
-      // vectors tid + 256 q of 8 consecutive threads form one group
-      g += __shfl_xor_sync(0xffffffffu, g, 1);
-      g += __shfl_xor_sync(0xffffffffu, g, 2);
-      g += __shfl_xor_sync(0xffffffffu, g, 4);
-      if ((lane & (kGroupVecs - 1)) == 0) {
-        if (v < d.nvec) __stcg(gs_out + v / kGroupVecs, g);
+      // the vectors 32 cw + 256 q + lane of one warp form group cw + 8 q
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) g += __shfl_xor_sync(0xffffffffu, g, off);
+      const int gi = v / kGroupVecs;
+      if (lane == 0 && gi * kGroupVecs < d.nvec) {
+        st_tw(gs_out + gi, tw_make(__float_as_uint(g), d.tag));
         dsum += (double)g;
       }
     }
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, off);
     release(st1);
     if (resid) release(stage);
     advance();
     if (!to_epilogue([&](EpiSlot& E) {
           if (lane == 0) E.dsum[cw] = dsum;
-          if (tid == 0) { E.type = IT_DSUM; E.b = d.b; E.chunk = d.chunk; E.i = d.i; }
+          if (tid == 0) { E.type = IT_DSUM; E.b = d.b; E.chunk = d.chunk; E.i = d.i; E.tag = d.tag; }
         }))
       return;
   }
 }
 
 // ---------------------------------------------------------------------------
-// epilogue: request bookkeeping
+// epilogue: publish chunk partials and draw slice sums as tagged words
 
-// Acceptance test of position i of request b, both rows complete (tutorial
-// page, sections 3.1-3.3), in fp32 on the fp32 row statistics:
-//   p(y) = 2^{(x_y - m_p) c} / s_p,  q(y) likewise (1 for one-hot q),
-//   accept <=> u q(y) < p(y),  a = min(1, p(y)/q(y)).
-// A test closer than 1e-5 (relative) to its threshold is counted and does not
-// stop the reading of later rows.  Returns the position code.
-template <bool GREEDY>
-__device__ int evaluate_position(const Params& P, int b, int i) {
-  const int G = P.G, V = P.V;
-  const int tid_t = target_row_id(b, i, G);
-  const RowStats tr = ldcg_stats(P.row_stats + tid_t);
-  const int y = P.draft_tokens[(size_t)b * G + i];
-  int code;
-  float a = qnan();
-  if (GREEDY) {
-    if (!row_ok(tr, true)) code = PC_NONFINITE;
-    else if (y < 0 || y >= V) code = PC_BAD_TOKEN;
-    else code = (y == (tr.idx & ~kIdxNaN)) ? PC_ACCEPT : PC_REJECT;
-  } else {
-    const bool sample = P.mode == MODE_SAMPLE;
-    const int did = draft_row_id(b, i, P.B, G);
-    const float u = P.uniforms[(size_t)b * (G + 1) + i];
-    const float c = __ldg(P.req_scale + b);
-    const float xt = __ldcg(P.row_xy + tid_t);
-    RowStats dr{};
-    float xd = 0.f;
-    if (sample) {
-      dr = ldcg_stats(P.row_stats + did);
-      xd = __ldcg(P.row_xy + did);
-    }
-    if (!row_ok(tr, false) || (sample && !row_ok(dr, false))) code = PC_NONFINITE;
-    else if (y < 0 || y >= V) code = PC_BAD_TOKEN;
-    else if (!(u >= 0.f && u < 1.f)) code = PC_BAD_UNIFORM;
-    else {
-      const float py = ex2((xt - tr.m) * c) / tr.s;
-      const float qy = sample ? ex2((xd - dr.m) * c) / dr.s : 1.f;
-      const float uq = u * qy;
-      code = uq < py ? PC_ACCEPT : PC_REJECT;
-      a = qy > 0.f ? fminf(1.f, py / qy) : (py > 0.f ? 1.f : 0.f);
-      if (fabsf(uq - py) <= 1e-5f * fmaxf(uq, py)) {
-        code |= PC_UNCERTAIN;
-        atomicAdd(&HDR_UNCERTAIN(P.hdr), 1u);
+template <int DT, bool GREEDY>
+__device__ void epilogue_role(const Params& P, VSmem& S, int lane, int e, unsigned epoch) {
+  const int nch = P.nch;
+  for (int seq = e;; seq += kEpiWarps) {
+    const int eslot = seq % kEpiSlots;
+    const uint32_t epar = (uint32_t)(seq / kEpiSlots) & 1u;
+    if (!wait_bar(S, &S.epi_full[eslot], epar)) { set_abort(P, S); return; }
+    const EpiSlot& E = S.slot[eslot];
+    if (E.term) return;
+    const int type = E.type, rid = E.row_id, b = E.b, kind = E.kind, chunk = E.chunk;
+    const float xy = E.xy;
+    const unsigned dtag = E.tag;
+    Part p = lane < kConsumerWarps ? E.part[lane] : empty_part();
+    double ws = 0.0;
+    if (lane == 0 && type == IT_DSUM)
+      for (int w = 0; w < kConsumerWarps; ++w) ws += E.dsum[w];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&S.epi_empty[eslot]);
+
+    if (type == IT_DSUM) {
+      // the slice sum, fp64 as two tagged halves
+      if (lane == 0) {
+        tword* o = P.dsum + 2 * ((size_t)b * P.nres + chunk);
+        const unsigned long long bits = (unsigned long long)__double_as_longlong(ws);
+        st_tw(o, tw_make((unsigned)(bits >> 32), dtag));
+        st_tw(o + 1, tw_make((unsigned)bits, dtag));
       }
+      continue;
+    }
+    // IT_STATS: merge the consumer warps' partials (fixed tree), publish
+    const bool ent = !GREEDY && kind == KIND_DRAFT && P.signals_on;
+    const float c = GREEDY ? 0.f : __ldg(P.req_scale + b);
+#pragma unroll
+    for (int off = 4; off >= 1; off >>= 1) {
+      const Part o = shfl_part(p, off);
+      p = GREEDY ? merge_argmax(p, o) : merge_parts(p, o, c, ent);
+    }
+    if (lane == 0) {
+      tword* o = P.cparts + ((size_t)rid * nch + chunk) * kPartWords;
+      const unsigned ptag = part_tag(epoch);
+      st_tw(o + 0, tw_make(__float_as_uint(p.m), ptag));
+      st_tw(o + 1, tw_make(__float_as_uint(p.s), ptag));
+      st_tw(o + 2, tw_make(__float_as_uint(p.t), ptag));
+      st_tw(o + 3, tw_make((unsigned)p.idx, ptag));
+      st_tw(o + 4, tw_make(__float_as_uint(xy), ptag));
     }
   }
-  __stcg(P.pair_res + (size_t)b * (G + 1) + i, code);
-  __stcg(P.pair_a + (size_t)b * (G + 1) + i, a);
-  if (code != PC_ACCEPT && !(code & PC_UNCERTAIN)) atomicMin(P.known_reject + b, i);
-  return code & 15;
 }
 
-// Is the first reject k of a request known from its state word?  Positions
-// 0..k-1 evaluated and accepted, and k evaluated and not accepted; or all
-// gamma positions accepted and the bonus row complete.
-__device__ __forceinline__ bool k_known(unsigned long long s, int gam) {
-  const unsigned E = (unsigned)s & 0x7fffffffu;
-  const unsigned A = (unsigned)(s >> 32) & 0x7fffffffu;
-  const int j = __ffs(~(E & A)) - 1;
-  if (j < gam) return (E >> j) & 1u;
-  return (s & kBonusBit) != 0ull;
+// ---------------------------------------------------------------------------
+// owner: one warp per CTA takes each of its requests (b = CTA, CTA + grid,
+// ...) from the row partials to the outputs: merges the rows in the order
+// the schedule streams them, tests the positions in order, publishes the
+// first reject (early exit), runs the draw and writes the outputs.  All of a
+// request's decisions are taken in one warp, so they need no atomics.
+
+// A wait of the owner gives up after kWaitLimitCycles, or at once when any
+// role of any CTA has given up (the header error word).
+struct OwnerClock {
+  long long c0;
+  __device__ __forceinline__ void start() { c0 = clock64(); }
+  __device__ __forceinline__ bool expired(const Params& P) const {
+    const bool mine = __any_sync(0xffffffffu, clock64() - c0 > kWaitLimitCycles);
+    if (mine) {   // this wait gave up: every other role gives up too
+      if ((threadIdx.x & 31) == 0) atomicOr(&P.hdr->error.v, (unsigned)SPEC_ST_TIMEOUT);
+      return true;
+    }
+    return __any_sync(0xffffffffu, ld_relaxed_u32(&P.hdr->error.v) != 0u);
+  }
+};
+
+struct RowRes {
+  RowStats st;   // merged statistics (every lane)
+  float xy;      // logit at the requested element (NaN if not requested)
+};
+
+// Merged statistics of row rid (warp-wide).  Waits until every chunk
+// partial carries the call's tag, merges them in chunk order (lane l takes
+// chunks l, l+32, ...; then a fixed xor tree) and takes x_y from the chunk
+// that holds element y (y < 0: none).  False if the wait gave up.
+template <bool GREEDY>
+__device__ bool merge_row(const Params& P, int rid, int y, float c, bool ent, unsigned epoch, int lane, RowRes& out) {
+  const int nch = P.nch;
+  const tword* base = P.cparts + (size_t)rid * nch * kPartWords;
+  const int ychunk = y >= 0 ? y / chunk_elems(P.dtype) : -1;
+  Part r = empty_part();
+  float xy = qnan();
+  OwnerClock clk;
+  clk.start();
+  for (int k0 = 0; k0 < nch; k0 += 32) {
+    const int k = k0 + lane;
+    tword w[kPartWords];
+    while (true) {
+      bool ok = true;
+      if (k < nch) {
+#pragma unroll
+        for (int j = 0; j < kPartWords; ++j) {
+          w[j] = ld_tw(base + (size_t)k * kPartWords + j);
+          ok &= tw_ok(w[j], part_tag(epoch));
+        }
+      }
+      if (__all_sync(0xffffffffu, ok)) break;
+      if (clk.expired(P)) return false;
+    }
+    if (k < nch) {
+      Part q;
+      q.m = tw_f32(w[0]); q.s = tw_f32(w[1]); q.t = tw_f32(w[2]); q.idx = (int)tw_u32(w[3]);
+      r = GREEDY ? merge_argmax(r, q) : merge_parts(r, q, c, ent);
+      if (k == ychunk) xy = tw_f32(w[4]);
+    }
+  }
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) {
+    const Part o = shfl_part(r, off);
+    r = GREEDY ? merge_argmax(r, o) : merge_parts(r, o, c, ent);
+  }
+  out.st.m = r.m; out.st.s = r.s; out.st.t = r.t; out.st.idx = r.idx;
+  out.xy = (ychunk >= 0 && ychunk < nch) ? __shfl_sync(0xffffffffu, xy, ychunk & 31) : qnan();
+  return true;
 }
 
 __device__ __forceinline__ int status_of_code(int code) {
@@ -1109,110 +1186,41 @@ __device__ __forceinline__ int status_of_code(int code) {
        : code == PC_BAD_UNIFORM ? SPEC_ST_BAD_UNIFORM : SPEC_ST_TIMEOUT;
 }
 
-__device__ __forceinline__ void finish_request(const Params& P, int b, int st, int lane) {
-  __syncwarp();
-  if (lane == 0) {
-    __stcg(P.req_status + b, st | kFinished);
-    atomicAdd(&P.hdr->done.v, 1u);
-  }
-}
-
-// Outputs of a settled request (warp-wide): committed tokens y_0..y_{k-1}
-// then z, accept_prob for positions <= k, the SpecKV signals from the draft
-// rows' statistics (H = log2 s - t/s bits, c = 1/s; tutorial-independent,
-// SpecKV page), status.
-__device__ void write_outputs(const Params& P, int b, int st, int k, int z, int lane) {
-  const int G = P.G, gam = gamma_of(P, b);
-  if (st & kVoidMask) {
-    write_void_outputs(P, b, st, lane, 32);
-    finish_request(P, b, st, lane);
-    return;
-  }
-  if (P.mode != MODE_SIGNALS) {
-    for (int j = lane; j <= G; j += 32)
-      P.tokens[(size_t)b * (G + 1) + j] = j < k ? P.draft_tokens[(size_t)b * G + j] : (j == k ? z : -1);
-    if (P.accept_prob)
-      for (int j = lane; j < G; j += 32)
-        P.accept_prob[(size_t)b * G + j] = (j < gam && j <= k) ? __ldcg(P.pair_a + (size_t)b * (G + 1) + j) : qnan();
-    if (lane == 0) P.accept_len[b] = k;
-  }
-  if (P.signals_on && (P.signals || P.row_signals)) {
-    // H_i = log2 s_i - t_i / s_i bits and c_i = 1 / s_i (fp32; fixed xor tree)
-    float H = 0.f, cf = 0.f;
-    const bool in = lane < gam;
-    if (in) {
-      const RowStats r = ldcg_stats(P.row_stats + draft_row_id(b, lane, P.B, G));
-      H = log2f(r.s) - r.t / r.s;
-      cf = 1.f / r.s;
-    }
-    if (P.row_signals && lane < G) {
-      float* rs = P.row_signals + ((size_t)b * G + lane) * 2;
-      rs[0] = in ? H : qnan();
-      rs[1] = in ? cf : qnan();
-    }
-    float hs = H, cs = cf, hm = in ? H : -INFINITY, cm = in ? cf : INFINITY;
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) {
-      hs += __shfl_xor_sync(0xffffffffu, hs, off);
-      cs += __shfl_xor_sync(0xffffffffu, cs, off);
-      hm = fmaxf(hm, __shfl_xor_sync(0xffffffffu, hm, off));
-      cm = fminf(cm, __shfl_xor_sync(0xffffffffu, cm, off));
-    }
-    if (lane == 0 && P.signals) {
-      float* sg = P.signals + (size_t)b * 4;
-      if (gam > 0) {
-        sg[0] = hs / (float)gam; sg[1] = hm; sg[2] = cs / (float)gam; sg[3] = cm;
-      } else {
-        sg[0] = sg[1] = sg[2] = sg[3] = qnan();
-      }
+// Acceptance test of position i (tutorial page "5.1 投机解码核心原理",
+// sections 3.1-3.3), in fp32 on the merged row statistics:
+//   p(y) = 2^{(x_y - m_p) c} / s_p,  q(y) likewise (1 for one-hot q),
+//   accept <=> u q(y) < p(y),  a = min(1, p(y)/q(y)).
+// A test closer than 1e-5 (relative) to its threshold is counted; it is not
+// published as an early exit.  Returns the position code (with
+// PC_UNCERTAIN); *a = a_i (NaN when not computed).  Every lane computes the
+// same.
+template <bool GREEDY>
+__device__ int evaluate_pos(const Params& P, int b, int i, const RowRes& T, const RowRes& D, int y, float c,
+                            float* a_out) {
+  const int G = P.G, V = P.V;
+  int code;
+  float a = qnan();
+  if (GREEDY) {
+    if (!row_ok(T.st, true)) code = PC_NONFINITE;
+    else if (y < 0 || y >= V) code = PC_BAD_TOKEN;
+    else code = (y == (T.st.idx & ~kIdxNaN)) ? PC_ACCEPT : PC_REJECT;
+  } else {
+    const bool sample = P.mode == MODE_SAMPLE;
+    const float u = P.uniforms[(size_t)b * (G + 1) + i];
+    if (!row_ok(T.st, false) || (sample && !row_ok(D.st, false))) code = PC_NONFINITE;
+    else if (y < 0 || y >= V) code = PC_BAD_TOKEN;
+    else if (!(u >= 0.f && u < 1.f)) code = PC_BAD_UNIFORM;
+    else {
+      const float py = ex2((T.xy - T.st.m) * c) / T.st.s;
+      const float qy = sample ? ex2((D.xy - D.st.m) * c) / D.st.s : 1.f;
+      const float uq = u * qy;
+      code = uq < py ? PC_ACCEPT : PC_REJECT;
+      a = qy > 0.f ? fminf(1.f, py / qy) : (py > 0.f ? 1.f : 0.f);
+      if (fabsf(uq - py) <= 1e-5f * fmaxf(uq, py)) code |= PC_UNCERTAIN;
     }
   }
-  if (lane == 0 && P.status) P.status[b] = st;
-  finish_request(P, b, st, lane);
-}
-
-// The output of a request is written once two things are known: the result
-// of its draw (first reject k, committed token z, or an error found on the
-// way) and, when signals are requested, every draft row's statistics.  A
-// counter per request counts the conditions met; whoever meets the last one
-// writes the outputs.
-__device__ __forceinline__ unsigned conditions_needed(const Params& P) {
-  return (P.mode == MODE_SIGNALS ? 0u : 1u) + (P.signals_on ? 1u : 0u);
-}
-
-// All conditions met: the outputs of request b (warp-wide).  The signal rows
-// are checked first, as the method reads them before the positions.
-__device__ void finalize_outputs(const Params& P, int b, int lane) {
-  const int G = P.G, gam = gamma_of(P, b);
-  if (P.signals_on) {
-    bool bad = false;
-    if (lane < gam) bad = !row_ok(ldcg_stats(P.row_stats + draft_row_id(b, lane, P.B, G)), false);
-    if (__ballot_sync(0xffffffffu, bad)) { write_outputs(P, b, SPEC_ST_NONFINITE, 0, -1, lane); return; }
-  }
-  if (P.mode == MODE_SIGNALS) { write_outputs(P, b, 0, 0, -1, lane); return; }
-  write_outputs(P, b, __ldcg(P.req_status + b), __ldcg(P.req_k + b), __ldcg(P.req_z + b), lane);
-}
-
-// One condition of request b is met (lane 0 decides; warp-wide call).
-__device__ __forceinline__ void condition_met(const Params& P, int b, int lane) {
-  bool last = false;
-  if (lane == 0) {
-    const unsigned o = atom_add_acqrel(P.req_cnt + 2 * b + 1, 1u);
-    last = o + 1u == conditions_needed(P);
-  }
-  if (__shfl_sync(0xffffffffu, last, 0)) finalize_outputs(P, b, lane);
-}
-
-// The draw of request b is settled: error bits st (0 if none), first reject
-// k, committed token z.  Warp-wide.
-__device__ void draw_done(const Params& P, int b, int st, int k, int z, int lane) {
-  if (lane == 0) {
-    __stcg(P.req_status + b, st);
-    __stcg(P.req_k + b, k);
-    __stcg(P.req_z + b, z);
-  }
-  __syncwarp();
-  condition_met(P, b, lane);
+  *a_out = a;
+  return code;
 }
 
 // Warp-wide: among n non-negative weights get(0..n-1) in order, the first j
@@ -1255,23 +1263,6 @@ __device__ int warp_locate(int n, Get get, double t, double* before, double* tot
   return lastpos;
 }
 
-// Start (or restart) the draw of request b: record it, then create one
-// IT_DSUM item per slice of row k.  Warp-wide.
-__device__ void start_draw(const Params& P, int b, int kind, int k, bool has_excl, int status, int lane) {
-  if (lane == 0) {
-    DrawDesc* dd = P.search + b;
-    __stcg(&dd->kind, kind);
-    __stcg(&dd->k, k);
-    __stcg(&dd->excl, has_excl ? 1 : 0);
-    __stcg(&dd->status, status);
-    __stcg(P.rsum_arr + b, 0u);
-    __stcg(P.req_k + b, k);
-  }
-  __syncwarp();
-  const int aux = k | (kind == DK_P ? 1 << 8 : 0) | (has_excl ? 1 << 9 : 0);
-  enqueue_items(P, P.nres, IT_DSUM, b, 0, aux, lane);
-}
-
 // Warp inclusive scan of one fp64 value per lane (fixed association).
 __device__ __forceinline__ double warp_incl_scan(double v, int lane) {
 #pragma unroll
@@ -1282,36 +1273,66 @@ __device__ __forceinline__ double warp_incl_scan(double v, int lane) {
   return v;
 }
 
-// All slices of the draw of request b are summed (warp-wide).  The slice is
-// located by the fp64 prefix of the slice sums, the 64-token group inside it
-// by the fp64 prefix of the stored group sums, and the token by an fp64 walk
-// over the group's recomputed weights (one or two 128-byte loads, from L2).
-// If rounding leaves no crossing in the group, its last weighted token is
-// taken (counted as a near tie).  Zero total mass restarts the draw from p_k
-// with SPEC_ST_ZERO_RESIDUAL.
+// Start one round of the draw of request b: its descriptor (read by the
+// producers that stage the slices), then one queue entry per slice of row k.
+// Warp-wide.
+__device__ void start_draw(const Params& P, int b, int kind, int k, int excl, const RowStats& tr,
+                           const RowStats& dr, float c, int round, unsigned epoch, int lane) {
+  const unsigned tag = draw_tag(epoch, round);
+  tword* dd = P.dd + (size_t)b * kDrawWords;
+  unsigned v = 0u;
+  if (lane == DW_KIND) v = (unsigned)kind | ((unsigned)k << 8);
+  else if (lane == DW_EXCL) v = (unsigned)excl;
+  else if (lane == DW_M1) v = __float_as_uint(tr.m);
+  else if (lane == DW_S1) v = __float_as_uint(tr.s);
+  else if (lane == DW_M2) v = __float_as_uint(dr.m);
+  else if (lane == DW_S2) v = __float_as_uint(dr.s);
+  else if (lane == DW_C) v = __float_as_uint(c);
+  if (lane < DW_PAD) st_tw(dd + lane, tw_make(v, tag));
+  __syncwarp();
+  enqueue_draw(P, P.nres, b, round, epoch, lane);
+}
+
+enum DrawResult : int { DR_OK = 0, DR_ZERO = 1, DR_FAIL = 2 };
+
+__device__ __forceinline__ double slice_sum(const tword* o, int j) {
+  const unsigned long long hi = tw_u32(ld_tw(o + 2 * j)), lo = tw_u32(ld_tw(o + 2 * j + 1));
+  return __longlong_as_double((long long)((hi << 32) | lo));
+}
+
+// One round of the draw, once its slices are summed (warp-wide).  The slice
+// is located by the fp64 prefix of the slice sums, the group of one warp's
+// 32 vectors (256 bf16 / 128 fp32 tokens) inside it by the fp64 prefix of
+// the stored group sums, and the token by an fp64 walk over the group's
+// recomputed weights (one 16-byte load per lane and row, from L2).  If
+// rounding leaves no crossing in the group, its last weighted token is
+// taken (counted as a near tie).  DR_ZERO: the total mass is zero.
 template <int DT>
-__device__ void locate_draw(const Params& P, int b, int lane) {
+__device__ int draw_round(const Params& P, int b, int kind, int k, int excl, const RowStats& tr, const RowStats& dr,
+                          float c, float ud, unsigned tag, int lane, int* z_out) {
   constexpr int N = VecT<DT>::N;
-  constexpr int GE = kGroupVecs * N;                 // tokens per group (64 bf16 / 32 fp32)
-  constexpr int PER = GE / 32;                       // tokens per lane in the final walk
-  constexpr int GPL = kGroupsPerStage / 32;          // groups per lane (4)
+  constexpr int GE = kGroupVecs * N;                 // tokens per group
+  constexpr int PER = GE / 32;                       // tokens per lane in the final walk (= N)
   const int G = P.G, V = P.V, nres = P.nres, se = stage_elems(DT);
-  const DrawDesc* dd = P.search + b;
-  const int kind = __ldcg(&dd->kind), k = __ldcg(&dd->k), dstat = __ldcg(&dd->status);
-  const bool has_excl = __ldcg(&dd->excl) != 0;
   const bool resid = kind == DK_RESID;
-  // independent loads first
-  const RowStats tr = ldcg_stats(P.row_stats + target_row_id(b, k, G));
-  const RowStats dr = resid ? ldcg_stats(P.row_stats + draft_row_id(b, k, P.B, G)) : RowStats{};
-  const float c = __ldg(P.req_scale + b);
-  const float ud = P.uniforms[(size_t)b * (G + 1) + G];
-  const int excl = has_excl ? P.draft_tokens[(size_t)b * G + k] : -1;
-  const double* parts = P.rsum_parts + (size_t)b * nres;
+  const tword* sums = P.dsum + 2 * (size_t)b * nres;
+  // 0. every slice summed
+  OwnerClock clk;
+  clk.start();
+  for (int j0 = 0; j0 < nres; j0 += 32) {
+    const int j = j0 + lane;
+    while (true) {
+      bool ok = true;
+      if (j < nres) ok = tw_ok(ld_tw(sums + 2 * j), tag) && tw_ok(ld_tw(sums + 2 * j + 1), tag);
+      if (__all_sync(0xffffffffu, ok)) break;
+      if (clk.expired(P)) return DR_FAIL;
+    }
+  }
   // 1. the slice: prefix of the slice sums
   double W, before;
   int cs;
   if (nres <= 32) {
-    const double v = lane < nres ? __ldcg(parts + lane) : 0.0;
+    const double v = lane < nres ? slice_sum(sums, lane) : 0.0;
     const double incl = warp_incl_scan(v, lane);
     W = __shfl_sync(0xffffffffu, incl, 31);
     const double t = (double)ud * W;
@@ -1320,57 +1341,37 @@ __device__ void locate_draw(const Params& P, int b, int lane) {
     cs = cross ? __ffs(cross) - 1 : (pos ? 31 - __clz(pos) : -1);
     before = cs >= 0 ? __shfl_sync(0xffffffffu, incl - v, cs) : 0.0;
   } else {
-    auto get = [&](int j) -> double { return __ldcg(parts + j); };
+    auto get = [&](int j) -> double { return slice_sum(sums, j); };
     warp_locate(nres, get, INFINITY, &before, &W, lane);
     double tot;
     cs = warp_locate(nres, get, (double)ud * W, &before, &tot, lane);
   }
-  if (!(W > 0.0)) {
-    if (resid || has_excl) {   // residual mass rounded to zero: draw from p_k itself
-      start_draw(P, b, DK_P, k, false, dstat | SPEC_ST_ZERO_RESIDUAL, lane);
-      return;
-    }
-    draw_done(P, b, SPEC_ST_TIMEOUT, 0, -1, lane);      // a complete row always has mass
-    return;
-  }
+  if (!(W > 0.0)) return DR_ZERO;
+  if (cs < 0) return DR_FAIL;
   const double t = (double)ud * W;
   const int e0 = cs * se, e1 = min(e0 + se, V);
-  const int ngroups = (e1 - e0 + GE - 1) / GE;
-  // 2. the group: lane l holds groups GPL*l .. GPL*l + GPL-1
-  const float* gsum = P.rsum_gs + ((size_t)b * nres + cs) * kGroupsPerStage;
-  float gv[GPL];
-  double lsum = 0.0;
-#pragma unroll
-  for (int u = 0; u < GPL; ++u) {
-    const int j = lane * GPL + u;
-    gv[u] = j < ngroups ? __ldcg(gsum + j) : 0.f;
-    lsum += (double)gv[u];
+  const int ngroups = (e1 - e0 + GE - 1) / GE;       // <= kGroupsPerStage = 32
+  // 2. the group: lane l holds group l of the slice
+  const tword* gsum = P.gsum + ((size_t)b * nres + cs) * kGroupsPerStage;
+  float gv = 0.f;
+  clk.start();
+  while (true) {
+    bool ok = true;
+    if (lane < ngroups) {
+      const tword w = ld_tw(gsum + lane);
+      ok = tw_ok(w, tag);
+      gv = tw_f32(w);
+    }
+    if (__all_sync(0xffffffffu, ok)) break;
+    if (clk.expired(P)) return DR_FAIL;
   }
+  const double lsum = lane < ngroups ? (double)gv : 0.0;
   const double tl = t - before;
   const double gincl = warp_incl_scan(lsum, lane);
   const unsigned gcross = __ballot_sync(0xffffffffu, gincl > tl);
   const unsigned gpos = __ballot_sync(0xffffffffu, lsum > 0.0);
-  const int gl = gcross ? __ffs(gcross) - 1 : (gpos ? 31 - __clz(gpos) : 0);
-  int g = gl * GPL;
-  double gbefore = __shfl_sync(0xffffffffu, gincl - lsum, gl);
-  {
-    // walk the crossing lane's groups (every lane computes the same from shuffles)
-    double acc = gbefore;
-    int gsel = -1;
-    double gsel_before = gbefore;
-    int last_pos = -1;
-    double last_before = gbefore;
-#pragma unroll
-    for (int u = 0; u < GPL; ++u) {
-      const double w = (double)__shfl_sync(0xffffffffu, gv[u], gl);
-      if (w > 0.0) { last_pos = gl * GPL + u; last_before = acc; }
-      if (gsel < 0 && acc + w > tl) { gsel = gl * GPL + u; gsel_before = acc; }
-      acc += w;
-    }
-    if (gsel < 0) { gsel = last_pos >= 0 ? last_pos : gl * GPL; gsel_before = last_before; }
-    g = gsel;
-    gbefore = gsel_before;
-  }
+  const int g = gcross ? __ffs(gcross) - 1 : (gpos ? 31 - __clz(gpos) : 0);
+  const double gbefore = __shfl_sync(0xffffffffu, gincl - lsum, g);
   const double tl2 = tl - gbefore;
   // 3. the token: lane l takes PER consecutive tokens of the group
   ResidW R;
@@ -1428,139 +1429,167 @@ __device__ void locate_draw(const Params& P, int b, int lane) {
     }
   }
   if (lane == 0 && !(margin >= (double)kDrawGuard * W)) atomicAdd(&HDR_UNCERTAIN(P.hdr), 1u);
-  draw_done(P, b, z >= 0 ? dstat : SPEC_ST_TIMEOUT, k, z, lane);
+  *z_out = z;
+  return z >= 0 ? DR_OK : DR_FAIL;
 }
 
-// The first reject k of request b is known: settle its draw, or create the
-// draw items.  Warp-wide.  Errors are taken in the method's order: positions
-// in order, then the bonus row, then the draw's uniform.
-template <int DT, bool GREEDY>
-__device__ void dispatch_draw(const Params& P, int b, int lane) {
-  const int G = P.G, gam = gamma_of(P, b);
-  const unsigned long long s = __ldcg(P.req_state + b);
-  const unsigned E = (unsigned)s & 0x7fffffffu, A = (unsigned)(s >> 32) & 0x7fffffffu;
-  const int j = __ffs(~(E & A)) - 1;
-  int k = gam;
-  bool rejected = false;
-  if (j < gam) {
-    const int code = __ldcg(P.pair_res + (size_t)b * (G + 1) + j) & 15;
-    if (code != PC_REJECT) { draw_done(P, b, status_of_code(code), 0, -1, lane); return; }
-    k = j;
-    rejected = true;
-  } else if (!row_ok(ldcg_stats(P.row_stats + target_row_id(b, gam, G)), GREEDY)) {
-    draw_done(P, b, SPEC_ST_NONFINITE, 0, -1, lane);
-    return;
-  }
-  if (GREEDY) {
-    const int z = ldcg_stats(P.row_stats + target_row_id(b, k, G)).idx & ~kIdxNaN;
-    draw_done(P, b, 0, k, z, lane);
-    return;
-  }
-  const float ud = P.uniforms[(size_t)b * (G + 1) + G];
-  if (!(ud >= 0.f && ud < 1.f)) { draw_done(P, b, SPEC_ST_BAD_UNIFORM, 0, -1, lane); return; }
-  if (rejected && P.mode == MODE_SAMPLE) start_draw(P, b, DK_RESID, k, false, 0, lane);
-  else start_draw(P, b, DK_P, k, rejected, 0, lane);    // one-hot residual: p without y_k
-}
-
-// A row of request b is complete (its statistics are published): record the
-// events it causes.  Warp-wide.
-template <int DT, bool GREEDY>
-__device__ void row_events(const Params& P, int b, int i, int kind, int lane) {
-  const int G = P.G, gam = gamma_of(P, b);
-  bool k_now = false, sig_now = false;
-  if (lane == 0) {
+// Outputs of one request (warp-wide): committed tokens y_0..y_{k-1} then z,
+// accept_prob for positions <= k, the SpecKV signals (H_i = log2 s_i -
+// t_i / s_i bits and c_i = 1 / s_i, held by lane i), status; then the
+// request is counted as done.
+__device__ void owner_outputs(const Params& P, int b, int gam, int st, int k, int z, float a_lane, float H_lane,
+                              float cf_lane, unsigned epoch, int lane) {
+  const int G = P.G;
+  if (st & kVoidMask) {
+    write_void_outputs(P, b, st, lane, 32);
+  } else {
     if (P.mode != MODE_SIGNALS) {
-      unsigned long long bits = 0ull;
-      if (i < gam) {
-        const unsigned pneed = P.mode == MODE_SAMPLE ? 2u : (kind == KIND_TARGET ? 1u : 0u);
-        if (pneed > 0u) {
-          const unsigned o2 = atom_add_acqrel(P.pair_arr + (size_t)b * (G + 1) + i, 1u);
-          if (o2 + 1u == pneed) {
-            const int code = evaluate_position<GREEDY>(P, b, i);
-            bits = (1ull << i) | (code == PC_ACCEPT ? (1ull << (32 + i)) : 0ull);
-          }
-        }
-      } else if (kind == KIND_TARGET && i == gam) {
-        bits = kBonusBit;
+      for (int j = lane; j <= G; j += 32)
+        P.tokens[(size_t)b * (G + 1) + j] = j < k ? P.draft_tokens[(size_t)b * G + j] : (j == k ? z : -1);
+      if (P.accept_prob && lane < G)
+        P.accept_prob[(size_t)b * G + lane] = (lane < gam && lane <= k) ? a_lane : qnan();
+      if (lane == 0) P.accept_len[b] = k;
+    }
+    if (P.signals_on && (P.signals || P.row_signals)) {
+      const bool in = lane < gam;
+      const float H = in ? H_lane : 0.f, cf = in ? cf_lane : 0.f;
+      if (P.row_signals && lane < G) {
+        float* rs = P.row_signals + ((size_t)b * G + lane) * 2;
+        rs[0] = in ? H : qnan();
+        rs[1] = in ? cf : qnan();
       }
-      if (bits) {
-        const unsigned long long old = atom_or_acqrel_u64(P.req_state + b, bits);
-        k_now = !k_known(old, gam) && k_known(old | bits, gam);
-      }
-    }
-    if (kind == KIND_DRAFT && P.signals_on) {
-      const unsigned o = atom_add_acqrel(P.req_cnt + 2 * b, 1u);
-      sig_now = (int)o + 1 == gam;
-    }
-  }
-  if (__shfl_sync(0xffffffffu, k_now, 0)) dispatch_draw<DT, GREEDY>(P, b, lane);
-  if (__shfl_sync(0xffffffffu, sig_now, 0)) condition_met(P, b, lane);
-}
-
-// Epilogue warp e handles the items with sequence number = e (mod kEpiWarps).
-template <int DT, bool GREEDY>
-__device__ void epilogue_role(const Params& P, VSmem& S, int lane, int e) {
-  const int G = P.G, nch = P.nch;
-  for (int seq = e;; seq += kEpiWarps) {
-    const int eslot = seq % kEpiSlots;
-    const uint32_t epar = (uint32_t)(seq / kEpiSlots) & 1u;
-    if (!wait_bar(S, &S.epi_full[eslot], epar)) { set_abort(P, S); return; }
-    const EpiSlot& E = S.slot[eslot];
-    if (E.term) return;
-    const int type = E.type, rid = E.row_id, b = E.b, i = E.i, kind = E.kind, chunk = E.chunk;
-    const float xy = E.xy;
-    Part p = lane < kConsumerWarps ? E.part[lane] : empty_part();
-    double ws = 0.0;
-    if (lane == 0 && type == IT_DSUM)
-      for (int w = 0; w < kConsumerWarps; ++w) ws += E.dsum[w];
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&S.epi_empty[eslot]);
-
-    if (type == IT_DSUM) {
-      bool last = false;
-      if (lane == 0) {
-        __stcg(P.rsum_parts + (size_t)b * P.nres + chunk, ws);
-        __threadfence();   // the consumers' group sums, before the count
-        const unsigned o = atom_add_acqrel(P.rsum_arr + b, 1u);
-        last = o + 1u == (unsigned)P.nres;
-      }
-      if (__shfl_sync(0xffffffffu, last, 0)) locate_draw<DT>(P, b, lane);
-      continue;
-    }
-
-    // IT_STATS: publish the chunk partial; the CTA completing the row merges it
-    const bool ent = !GREEDY && kind == KIND_DRAFT && P.signals_on;
-    const float c = GREEDY ? 0.f : __ldg(P.req_scale + b);
-#pragma unroll
-    for (int off = 4; off >= 1; off >>= 1) {
-      const Part o = shfl_part(p, off);
-      p = GREEDY ? merge_argmax(p, o) : merge_parts(p, o, c, ent);
-    }
-    unsigned old = 0;
-    if (lane == 0) {
-      stcg_part(P.parts + (size_t)rid * nch + chunk, p);
-      if (!(xy != xy)) __stcg(P.row_xy + rid, xy);
-      old = atom_add_acqrel(P.row_arr + rid, 1u);   // release: the partial before the count
-    }
-    old = __shfl_sync(0xffffffffu, old, 0);
-    if (((old + 1u) & kCountMask) == (unsigned)nch && (old >> 20) == 0u) {
-      Part r = empty_part();
-      for (int k = lane; k < nch; k += 32) {
-        const Part q = ldcg_part(P.parts + (size_t)rid * nch + k);
-        r = GREEDY ? merge_argmax(r, q) : merge_parts(r, q, c, ent);
-      }
+      float hs = H, cs = cf, hm = in ? H : -INFINITY, cm = in ? cf : INFINITY;
 #pragma unroll
       for (int off = 16; off >= 1; off >>= 1) {
-        const Part o = shfl_part(r, off);
-        r = GREEDY ? merge_argmax(r, o) : merge_parts(r, o, c, ent);
+        hs += __shfl_xor_sync(0xffffffffu, hs, off);
+        cs += __shfl_xor_sync(0xffffffffu, cs, off);
+        hm = fmaxf(hm, __shfl_xor_sync(0xffffffffu, hm, off));
+        cm = fminf(cm, __shfl_xor_sync(0xffffffffu, cm, off));
       }
-      if (lane == 0) {
-        stcg_part(reinterpret_cast<Part*>(P.row_stats + rid), r);
-        __stcg(P.row_done + rid, 1);
+      if (lane == 0 && P.signals) {
+        float* sg = P.signals + (size_t)b * 4;
+        if (gam > 0) {
+          sg[0] = hs / (float)gam; sg[1] = hm; sg[2] = cs / (float)gam; sg[3] = cm;
+        } else {
+          sg[0] = sg[1] = sg[2] = sg[3] = qnan();
+        }
       }
-      __syncwarp();
-      row_events<DT, GREEDY>(P, b, i, kind, lane);
     }
+    if (lane == 0 && P.status) P.status[b] = st;
+  }
+  __syncwarp();
+  if (lane == 0) {
+    P.req_fin[b] = epoch;
+    atomicAdd(&P.hdr->done.v, 1u);
+  }
+}
+
+// Request b from its row partials to its outputs (warp-wide).  Errors are
+// taken in the method's order: positions in order, then the bonus row, then
+// the draw's uniform; with signals requested, a draft row that is not
+// usable voids the request (the signals are read before the positions).
+template <int DT, bool GREEDY>
+__device__ void serve_request(const Params& P, int b, unsigned epoch, int lane) {
+  const int B = P.B, G = P.G;
+  const int gam = __ldg(P.req_gam + b);
+  const float c = GREEDY ? 0.f : __ldg(P.req_scale + b);
+  const bool sample = P.mode == MODE_SAMPLE;
+  const bool sig = P.signals_on != 0;
+  float a_lane = qnan(), H_lane = qnan(), cf_lane = qnan();
+  bool sig_bad = false, failed = false, rejected = false;
+  int st = 0, k = gam, z = -1, ndraft = 0;   // ndraft: draft rows merged so far (0 .. ndraft-1)
+  RowRes rt{}, rd{};                          // rows k of the draw
+  rd.st.m = 0.f; rd.st.s = 1.f;
+  auto take_draft = [&](int i, const RowRes& D) {
+    if (sig) {
+      if (lane == i) {
+        H_lane = log2f(D.st.s) - D.st.t / D.st.s;
+        cf_lane = 1.f / D.st.s;
+      }
+      sig_bad |= !row_ok(D.st, false);
+    }
+  };
+
+  if (P.mode != MODE_SIGNALS) {
+    for (int i = 0; i < gam; ++i) {
+      const int y = P.draft_tokens[(size_t)b * G + i];
+      RowRes T, D{};
+      if (!merge_row<GREEDY>(P, target_row_id(b, i, G), GREEDY ? -1 : y, c, false, epoch, lane, T)) {
+        failed = true;
+        break;
+      }
+      if (sample) {
+        if (!merge_row<false>(P, draft_row_id(b, i, B, G), y, c, sig, epoch, lane, D)) { failed = true; break; }
+        take_draft(i, D);
+        ndraft = i + 1;
+      }
+      float a;
+      const int code = evaluate_pos<GREEDY>(P, b, i, T, D, y, c, &a);
+      if (lane == i) a_lane = a;
+      if (code & PC_UNCERTAIN) {
+        if (lane == 0) atomicAdd(&HDR_UNCERTAIN(P.hdr), 1u);
+      } else if (code != PC_ACCEPT && lane == 0) {
+        asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" ::"l"(P.known_reject + b), "r"(i) : "memory");  // early exit
+      }
+      if ((code & 15) != PC_ACCEPT) {
+        k = i;
+        if ((code & 15) == PC_REJECT) { rejected = true; rt = T; rd = D; }
+        else st = status_of_code(code & 15);
+        break;
+      }
+    }
+    if (!failed && st == 0 && !rejected) {      // every position accepted: the bonus row
+      if (!merge_row<GREEDY>(P, target_row_id(b, gam, G), -1, c, false, epoch, lane, rt)) failed = true;
+      else if (!row_ok(rt.st, GREEDY)) st = SPEC_ST_NONFINITE;
+    }
+  }
+  // the draw rounds are started before the remaining signal rows are merged
+  const bool draw = !GREEDY && P.mode != MODE_SIGNALS && !failed && st == 0;
+  int kind = DK_P, excl = -1;
+  float ud = 0.f;
+  if (draw) {
+    ud = P.uniforms[(size_t)b * (G + 1) + G];
+    if (!(ud >= 0.f && ud < 1.f)) {
+      st = SPEC_ST_BAD_UNIFORM;
+    } else {
+      if (rejected && sample) kind = DK_RESID;
+      else if (rejected) excl = P.draft_tokens[(size_t)b * G + k];    // one-hot residual: p without y_k
+      start_draw(P, b, kind, k, excl, rt.st, rd.st, c, 0, epoch, lane);
+    }
+  }
+  if (sig && !failed) {
+    for (int i = ndraft; i < gam; ++i) {
+      RowRes D;
+      if (!merge_row<false>(P, draft_row_id(b, i, B, G), -1, c, true, epoch, lane, D)) { failed = true; break; }
+      take_draft(i, D);
+    }
+  }
+  if (draw && st == 0 && !failed) {
+    int r = draw_round<DT>(P, b, kind, k, excl, rt.st, rd.st, c, ud, draw_tag(epoch, 0), lane, &z);
+    if (r == DR_ZERO && (kind == DK_RESID || excl >= 0)) {
+      // residual mass rounded to zero: draw from p_k itself
+      st |= SPEC_ST_ZERO_RESIDUAL;
+      kind = DK_P;
+      excl = -1;
+      start_draw(P, b, kind, k, excl, rt.st, rd.st, c, 1, epoch, lane);
+      r = draw_round<DT>(P, b, kind, k, excl, rt.st, rd.st, c, ud, draw_tag(epoch, 1), lane, &z);
+    }
+    if (r != DR_OK) {
+      failed = true;
+      z = -1;
+    }
+  }
+  if (GREEDY && !failed && st == 0) z = rt.st.idx & ~kIdxNaN;
+  if (failed) st = SPEC_ST_TIMEOUT;
+  else if (sig && __any_sync(0xffffffffu, sig_bad)) st = SPEC_ST_NONFINITE;
+  owner_outputs(P, b, gam, st, k, z, a_lane, H_lane, cf_lane, epoch, lane);
+}
+
+template <int DT, bool GREEDY>
+__device__ void owner_role(const Params& P, unsigned epoch, int lane) {
+  for (int b = blockIdx.x; b < P.B; b += gridDim.x) {
+    if (__ldg(P.req_status + b) & kFinished) continue;    // settled by the plan kernel
+    serve_request<DT, GREEDY>(P, b, epoch, lane);
   }
 }
 
@@ -1585,19 +1614,26 @@ __global__ void __launch_bounds__(kStatsThreads, 2) verify_kernel(Params P) {
     fence_mbar_init();
   }
   __syncthreads();
-  griddep_wait();   // the plan kernel's schedule and counters are ready
+  griddep_wait();   // the plan kernel's schedule, counters and epoch are ready
+  const unsigned epoch = HDR_EPOCH(P.hdr);   // partials and queue entries carry 4 * epoch
   if (warp < kConsumerWarps) consumer_role<DT, GREEDY>(P, S, warp, lane);
   else if (warp == kConsumerWarps) {
-    if (lane == 0) producer_role<DT, GREEDY>(P, S);
-  } else epilogue_role<DT, GREEDY>(P, S, lane, warp - kConsumerWarps - 1);
+    if (lane == 0) producer_role<DT, GREEDY>(P, S, epoch);
+  } else if (warp <= kConsumerWarps + kEpiWarps) {
+    epilogue_role<DT, GREEDY>(P, S, lane, warp - kConsumerWarps - 1, epoch);
+  } else {
+    owner_role<DT, GREEDY>(P, epoch, lane);
+  }
   __syncthreads();
   // the last CTA out voids any request an aborted wait left unfinished
   if (threadIdx.x == 0) {
+    __threadfence();
     const unsigned ex = atomicAdd(&HDR_EXITED(P.hdr), 1u) + 1u;
     if (ex == gridDim.x && ld_relaxed_u32(&P.hdr->error.v) != 0u) {
       __threadfence();
       for (int b = 0; b < P.B; ++b)
-        if (!(__ldcg(P.req_status + b) & kFinished)) write_void_outputs(P, b, SPEC_ST_TIMEOUT, 0, 1);
+        if (!(__ldcg(P.req_status + b) & kFinished) && __ldcg(P.req_fin + b) != epoch)
+          write_void_outputs(P, b, SPEC_ST_TIMEOUT, 0, 1);
     }
   }
 }
