@@ -27,14 +27,14 @@ thread_local cudaEvent_t g_prof_begin = nullptr, g_prof_end = nullptr;
 
 struct DevState {
   bool ready = false;
-  int sms = 0;
+  int ctas = 0;       // resident verify CTAs on the device (SMs x CTAs per SM, at most 2 per SM)
   int status = SPEC_OK;
 };
 constexpr int kMaxDevices = 64;
 DevState g_dev[kMaxDevices];
 std::mutex g_mu;
 
-int device_state(int* sms) {
+int device_state(int* ctas) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return SPEC_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return SPEC_ERR_UNSUPPORTED;
@@ -49,14 +49,21 @@ int device_state(int* sms) {
     if (major != 10 || minor != 3) {
       d.status = SPEC_ERR_UNSUPPORTED;   // the library carries sm_103a code only
     } else {
-      const cudaError_t e = configure_kernels();
+      cudaError_t e = configure_kernels();
+      int per_sm = 0;
+      if (e == cudaSuccess) e = verify_blocks_per_sm(&per_sm);
       if (e != cudaSuccess) return SPEC_ERR_CUDA;
-      d.status = SPEC_OK;
+      if (per_sm < 1) {
+        d.status = SPEC_ERR_UNSUPPORTED;
+      } else {
+        d.status = SPEC_OK;
+        n *= per_sm < 2 ? per_sm : 2;
+      }
     }
-    d.sms = n;
+    d.ctas = n;
     d.ready = true;
   }
-  *sms = d.sms;
+  *ctas = d.ctas;
   return d.status;
 }
 
@@ -109,8 +116,8 @@ int run(const Call& c) {
   const Layout L = make_layout(c.B, c.G, c.V, c.dtype);
   if (!c.workspace || c.workspace_bytes < L.total) return SPEC_ERR_WORKSPACE;
   if (!aligned(c.workspace, 256)) return SPEC_ERR_INVALID_ARG;
-  int sms = 0;
-  const int ds = device_state(&sms);
+  int ctas = 0;
+  const int ds = device_state(&ctas);
   if (ds != SPEC_OK) return ds;
 
   unsigned char* ws = static_cast<unsigned char*>(c.workspace);
@@ -138,9 +145,10 @@ int run(const Call& c) {
   P.nrows = L.nrows; P.nch = L.nch; P.nres = L.nres; P.dq_cap = L.dq_cap;
   P.aligned_rows = ((size_t)c.V * es) % 16 == 0 && aligned(c.target, 16) && aligned(c.draft, 16);
 
-  // persistent grid: two CTAs per SM, never more CTAs than work items
+  // persistent grid: every CTA resident at once (two per SM), never more
+  // CTAs than work items
   const long long max_items = (long long)c.B * (2 * c.G + 1) * L.nch;
-  const int grid1 = (int)(max_items < 2ll * sms ? max_items : 2ll * sms);
+  const int grid1 = (int)(max_items < (long long)ctas ? max_items : (long long)ctas);
   const cudaEvent_t pb = g_prof_begin, pe = g_prof_end;
   g_prof_begin = g_prof_end = nullptr;
   cudaError_t e = launch_plan(P, c.stream);

@@ -425,6 +425,7 @@ __device__ __forceinline__ Part empty_part() {
 cudaError_t launch_plan(const Params& P, cudaStream_t s);
 cudaError_t launch_verify(const Params& P, int grid, cudaStream_t s, bool pdl);
 cudaError_t configure_kernels();   // dynamic shared-memory limit, current device
+cudaError_t verify_blocks_per_sm(int* out);   // resident verify CTAs per SM, current device
 
 template <class K>
 inline cudaError_t launch_ex(K kern, dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl, const Params& P) {

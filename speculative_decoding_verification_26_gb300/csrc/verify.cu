@@ -245,19 +245,31 @@ __global__ void __launch_bounds__(1024) plan_kernel(Params P) {
 
 namespace {
 
-constexpr int F_FIRST = 1, F_LAST = 2, F_TERM = 4, F_DIRECT = 8;
+constexpr int F_FIRST = 1, F_LAST = 2, F_TERM = 4, F_DIRECT = 8, F_DRAW = 16;
+constexpr int kItemSlots = 8;       // > kStages (see ItemDesc)
 
-// One staged piece of an item (producer -> consumers).
-struct StageDesc {
-  int type, b, i, kind;
-  int row_id, chunk, elem0, nvec;
-  int flags, head0, nhead, tail0;
-  int ntail, y, aux, n_elems;       // n_elems: direct stages
-  long long src_elem;               // direct stages: flat element offset of the source
-  float c, m1, s1, m2;              // scale; row statistics of the rows used (draw)
-  float s2;
+// One work item (producer -> consumers), written once, before its first
+// stage is issued, into slot (item number mod kItemSlots).  The slot is
+// written again kItemSlots items later, after the ring slot of that item's
+// first stage came free, i.e. after every consumer warp released a stage at
+// least two past this item's last: every warp is then done with this item,
+// chunk-end work included.  So consumers read item fields in shared memory
+// when they need them and hold none in registers over a stage.
+struct ItemDesc {
+  int b, i, kind, row_id;
+  int chunk, y, aux, head0;
+  int nhead, tail0, ntail;
+  float c, m1, s1, m2, s2;
   unsigned tag;                     // draw: tag of the draw's words
-  int pad[2];
+  int pad[3];
+};
+
+// One staged piece of an item (producer -> consumers): 16 bytes.
+struct StageDesc {
+  int flags;                        // F_FIRST | F_LAST | F_TERM | F_DIRECT | F_DRAW
+  int nvec;                         // 16-byte vectors in the stage
+  int elem0;                        // row element of the stage's first element
+  int item;                         // item slot | row kind << 4 (draw slices: target, then draft)
 };
 
 // One finished item (consumers -> epilogue).
@@ -268,7 +280,7 @@ struct EpiSlot {
   unsigned tag;                     // draw: tag of the draw's words
   int pad[2];
   double dsum[kConsumerWarps];      // draw-weight sums per consumer warp (IT_DSUM)
-  Part part[kConsumerWarps];        // statistics per consumer warp
+  Part part[kConsumerWarps];        // statistics per consumer warp (IT_STATS)
 };
 
 struct __align__(128) VSmem {
@@ -278,6 +290,7 @@ struct __align__(128) VSmem {
   uint64_t epi_full[kEpiSlots];
   uint64_t epi_empty[kEpiSlots];
   StageDesc desc[kStages];
+  ItemDesc item[kItemSlots];
   EpiSlot slot[kEpiSlots];
   int abort;
 };
@@ -652,11 +665,13 @@ __device__ __forceinline__ ItemMeta finish_meta(const Params& P, const RawMeta& 
   return m;
 }
 
-// Stage one piece: wait for a free ring slot, write its descriptor, start the
-// bulk copy (bytes > 0) or just mark it full.
+// Stage one piece: wait for a free ring slot, write the item's descriptor
+// (first piece of an item) and the stage's, start the bulk copy (bytes > 0)
+// or just mark it full.
 __device__ __forceinline__ bool put_stage(VSmem& S, int& stage, uint32_t& phase, const StageDesc& d,
-                                          uintptr_t src, uint32_t bytes) {
+                                          const ItemDesc* it, uintptr_t src, uint32_t bytes) {
   if (!wait_bar(S, &S.empty[stage], phase ^ 1u)) return false;
+  if (it) S.item[d.item & (kItemSlots - 1)] = *it;
   S.desc[stage] = d;
   if (bytes > 0) {
     mbar_arrive_expect_tx(&S.full[stage], bytes);
@@ -669,7 +684,8 @@ __device__ __forceinline__ bool put_stage(VSmem& S, int& stage, uint32_t& phase,
 }
 
 template <int DT, bool GREEDY>
-__device__ bool stage_stats_item(const Params& P, VSmem& S, int& stage, uint32_t& phase, const ItemMeta& cur) {
+__device__ bool stage_stats_item(const Params& P, VSmem& S, int& stage, uint32_t& phase, const ItemMeta& cur,
+                                 int islot) {
   constexpr int ES = DT == SPEC_BF16 ? 2 : 4;
   const int G = P.G, V = P.V;
   const int ce = chunk_elems(DT);
@@ -693,21 +709,22 @@ __device__ bool stage_stats_item(const Params& P, VSmem& S, int& stage, uint32_t
   }
   const long long mid = (long long)(A1 - A0);
   const int npieces = mid > 0 ? (int)((mid + kStageBytes - 1) / kStageBytes) : 1;
-  StageDesc d{};
-  d.type = IT_STATS;
-  d.row_id = cur.rid; d.b = cur.b; d.i = cur.i; d.kind = cur.kind;
-  d.chunk = cur.chunk;
-  d.head0 = e_begin; d.nhead = nhead;
-  d.tail0 = e_end - ntail; d.ntail = ntail;
-  d.c = cur.c;
-  d.y = cur.y;
+  ItemDesc it{};
+  it.row_id = cur.rid; it.b = cur.b; it.i = cur.i; it.kind = cur.kind;
+  it.chunk = cur.chunk;
+  it.head0 = e_begin; it.nhead = nhead;
+  it.tail0 = e_end - ntail; it.ntail = ntail;
+  it.c = cur.c;
+  it.y = cur.y;
+  StageDesc d;
+  d.item = islot;
   for (int p = 0; p < npieces; ++p) {
     const long long off = (long long)p * kStageBytes;
     const uint32_t bytes = mid > 0 ? (uint32_t)(mid - off < kStageBytes ? mid - off : kStageBytes) : 0u;
     d.elem0 = (int)((A0 + (uintptr_t)off - rowaddr) / ES);
     d.nvec = (int)(bytes / 16);
     d.flags = (p == 0 ? F_FIRST : 0) | (p == npieces - 1 ? F_LAST : 0);
-    if (!put_stage(S, stage, phase, d, A0 + (uintptr_t)off, bytes)) return false;
+    if (!put_stage(S, stage, phase, d, p == 0 ? &it : nullptr, A0 + (uintptr_t)off, bytes)) return false;
   }
   return true;
 }
@@ -717,22 +734,21 @@ __device__ bool stage_stats_item(const Params& P, VSmem& S, int& stage, uint32_t
 // consumers fill themselves.
 template <int DT>
 __device__ __forceinline__ bool put_row_range(const Params& P, VSmem& S, int& stage, uint32_t& phase,
-                                              StageDesc d, int kind, int b, int i, int e0, int e1) {
+                                              StageDesc d, const ItemDesc* it, int kind, int b, int i, int e0,
+                                              int e1) {
   constexpr int ES = DT == SPEC_BF16 ? 2 : 4;
   const unsigned char* tens = kind == KIND_TARGET ? P.target : P.draft;
   const long long src = row_elem_offset(kind, b, i, P.G, P.V) + e0;
   d.elem0 = e0;
-  d.n_elems = e1 - e0;
-  d.src_elem = src;
-  d.kind = kind;
+  d.item = (d.item & (kItemSlots - 1)) | (kind << 4);
   if (P.aligned_rows) {
     const uint32_t bytes = (uint32_t)((e1 - e0) * ES);
     d.nvec = (int)(bytes / 16);
-    return put_stage(S, stage, phase, d, reinterpret_cast<uintptr_t>(tens) + (uintptr_t)(src * ES), bytes);
+    return put_stage(S, stage, phase, d, it, reinterpret_cast<uintptr_t>(tens) + (uintptr_t)(src * ES), bytes);
   }
   d.flags |= F_DIRECT;
   d.nvec = (e1 - e0 + (16 / ES) - 1) / (16 / ES);
-  return put_stage(S, stage, phase, d, 0, 0u);
+  return put_stage(S, stage, phase, d, it, 0, 0u);
 }
 
 // A draw slice: rows k of the request (the descriptor, written by the owner
@@ -740,7 +756,7 @@ __device__ __forceinline__ bool put_row_range(const Params& P, VSmem& S, int& st
 // tag; bounded).
 template <int DT>
 __device__ bool stage_dyn_item(const Params& P, VSmem& S, int& stage, uint32_t& phase, const DynItem& it,
-                               unsigned epoch) {
+                               unsigned epoch, int islot) {
   const int V = P.V, se = stage_elems(DT);
   const int b = it.b, ch = it.slice;
   const unsigned tag = draw_tag(epoch, it.round);
@@ -759,26 +775,27 @@ __device__ bool stage_dyn_item(const Params& P, VSmem& S, int& stage, uint32_t& 
   }
   const unsigned kk = tw_u32(w[DW_KIND]);
   const int kind = (int)(kk & 0xffu), k = (int)(kk >> 8);
-  StageDesc d{};
-  d.type = IT_DSUM;
-  d.b = b;
-  d.i = k;
-  d.chunk = ch;
-  d.aux = kind;
-  d.c = tw_f32(w[DW_C]);
-  d.m1 = tw_f32(w[DW_M1]); d.s1 = tw_f32(w[DW_S1]);
-  d.m2 = tw_f32(w[DW_M2]); d.s2 = tw_f32(w[DW_S2]);
-  d.y = (int)tw_u32(w[DW_EXCL]);
-  d.tag = tag;
+  ItemDesc id{};
+  id.b = b;
+  id.i = k;
+  id.chunk = ch;
+  id.aux = kind;
+  id.c = tw_f32(w[DW_C]);
+  id.m1 = tw_f32(w[DW_M1]); id.s1 = tw_f32(w[DW_S1]);
+  id.m2 = tw_f32(w[DW_M2]); id.s2 = tw_f32(w[DW_S2]);
+  id.y = (int)tw_u32(w[DW_EXCL]);
+  id.tag = tag;
   const int e0 = ch * se, e1 = min(e0 + se, V);
+  StageDesc d;
+  d.item = islot;
   if (kind == DK_RESID) {
-    d.flags = F_FIRST;
-    if (!put_row_range<DT>(P, S, stage, phase, d, KIND_TARGET, b, k, e0, e1)) return false;
-    d.flags = F_LAST;
-    return put_row_range<DT>(P, S, stage, phase, d, KIND_DRAFT, b, k, e0, e1);
+    d.flags = F_DRAW | F_FIRST;
+    if (!put_row_range<DT>(P, S, stage, phase, d, &id, KIND_TARGET, b, k, e0, e1)) return false;
+    d.flags = F_DRAW | F_LAST;
+    return put_row_range<DT>(P, S, stage, phase, d, nullptr, KIND_DRAFT, b, k, e0, e1);
   }
-  d.flags = F_FIRST | F_LAST;
-  return put_row_range<DT>(P, S, stage, phase, d, KIND_TARGET, b, k, e0, e1);
+  d.flags = F_DRAW | F_FIRST | F_LAST;
+  return put_row_range<DT>(P, S, stage, phase, d, &id, KIND_TARGET, b, k, e0, e1);
 }
 
 template <int DT, bool GREEDY>
@@ -787,6 +804,7 @@ __device__ void producer_role(const Params& P, VSmem& S, unsigned epoch) {
   const unsigned n_valid = HDR_N_VALID(P.hdr);
   int stage = 0;
   uint32_t phase = 0;
+  int islot = 0;              // items issued (their descriptor slots)
   bool ok = true;
   const bool dyn = !GREEDY && (P.mode == MODE_SAMPLE || P.mode == MODE_ONEHOT);
   unsigned ticket = dyn ? atomicAdd(&P.hdr->dq_head.v, 1u) : 0xffffffffu;
@@ -816,7 +834,7 @@ __device__ void producer_role(const Params& P, VSmem& S, unsigned epoch) {
       const RawMeta nxt = item_meta_raw<GREEDY>(P, q_next, rid_next, n_items);
       const int rid2 = item_row(P, q2, n_items);
       const unsigned q3 = q2 < n_items ? atomicAdd(&P.hdr->queue.v, 1u) : q2;
-      if (!cur.skip) ok = stage_stats_item<DT, GREEDY>(P, S, stage, phase, cur);   // a voided row is not read
+      if (!cur.skip) ok = stage_stats_item<DT, GREEDY>(P, S, stage, phase, cur, islot++ & (kItemSlots - 1));   // a voided row is not read
       cur = finish_meta(P, nxt, n_items);
       q_next = q2;
       rid_next = rid2;
@@ -829,7 +847,7 @@ __device__ void producer_role(const Params& P, VSmem& S, unsigned epoch) {
       it.slice = (int)(tw_u32(t1) & 0x3fffffffu);
       it.round = (int)(tw_u32(t1) >> 30);
       ticket = atomicAdd(&P.hdr->dq_head.v, 1u);
-      ok = stage_dyn_item<DT>(P, S, stage, phase, it, epoch);
+      ok = stage_dyn_item<DT>(P, S, stage, phase, it, epoch, islot++ & (kItemSlots - 1));
       did = true;
     }
     if (did) {
@@ -870,15 +888,18 @@ __device__ void producer_role(const Params& P, VSmem& S, unsigned epoch) {
 template <int DT>
 __device__ void fill_direct(const Params& P, VSmem& S, int stage, const StageDesc& d, int tid) {
   constexpr int N = VecT<DT>::N;
-  const unsigned char* tens = d.kind == KIND_TARGET ? P.target : P.draft;
-  const int n = d.n_elems, npad = d.nvec * N;
+  const ItemDesc& it = S.item[d.item & (kItemSlots - 1)];
+  const int kind = (d.item >> 4) & 1;
+  const unsigned char* tens = kind == KIND_TARGET ? P.target : P.draft;
+  const long long src_elem = row_elem_offset(kind, it.b, it.i, P.G, P.V) + d.elem0;
+  const int n = min(stage_elems(DT), P.V - d.elem0), npad = d.nvec * N;
   if (DT == SPEC_BF16) {
     unsigned short* dst = reinterpret_cast<unsigned short*>(S.ring[stage]);
-    const unsigned short* src = reinterpret_cast<const unsigned short*>(tens) + d.src_elem;
+    const unsigned short* src = reinterpret_cast<const unsigned short*>(tens) + src_elem;
     for (int j = tid; j < npad; j += kConsumerThreads) dst[j] = j < n ? __ldg(src + j) : (unsigned short)0xff80u;
   } else {
     float* dst = reinterpret_cast<float*>(S.ring[stage]);
-    const float* src = reinterpret_cast<const float*>(tens) + d.src_elem;
+    const float* src = reinterpret_cast<const float*>(tens) + src_elem;
     for (int j = tid; j < npad; j += kConsumerThreads) dst[j] = j < n ? __ldg(src + j) : -INFINITY;
   }
   consumer_bar();
@@ -906,6 +927,7 @@ __device__ void consumer_role(const Params& P, VSmem& S, int cw, int lane) {
   run_reset(r);
   bool ent = false;
   float c = 0.f, xy = qnan();
+  int y = -1;                     // draft token of the current statistics item (x_y capture)
   auto advance = [&]() {
     if (++stage == kStages) { stage = 0; phase ^= 1u; }
   };
@@ -916,8 +938,8 @@ __device__ void consumer_role(const Params& P, VSmem& S, int cw, int lane) {
   // hand one finished item to the epilogue warps
   auto to_epilogue = [&](auto write_fields) -> bool {
     const int eslot = seq % kEpiSlots;
-    const uint32_t epar = ((uint32_t)(seq / kEpiSlots) & 1u) ^ 1u;
-    if (!wait_bar(S, &S.epi_empty[eslot], epar)) { set_abort(P, S); return false; }
+    const uint32_t round = (uint32_t)(seq / kEpiSlots) & 1u;
+    if (!wait_bar(S, &S.epi_empty[eslot], round ^ 1u)) { set_abort(P, S); return false; }
     write_fields(S.slot[eslot]);
     __syncwarp();
     if (lane == 0) mbar_arrive(&S.epi_full[eslot]);
@@ -937,18 +959,20 @@ __device__ void consumer_role(const Params& P, VSmem& S, int cw, int lane) {
     if (d.flags & F_DIRECT) fill_direct<DT>(P, S, stage, d, tid);
     const uint4* vec = reinterpret_cast<const uint4*>(S.ring[stage]);
 
-    if (d.type == IT_STATS) {
+    if (!(d.flags & F_DRAW)) {
+      const ItemDesc& it = S.item[d.item & (kItemSlots - 1)];
       if (d.flags & F_FIRST) {
         run_reset(r);
-        ent = !GREEDY && d.kind == KIND_DRAFT && P.signals_on;
-        c = d.c;
+        ent = !GREEDY && it.kind == KIND_DRAFT && P.signals_on;
+        c = it.c;
+        y = it.y;
         xy = qnan();
       }
       uint4 w[kVecPerThread];
       load_stage<DT>(vec, d.nvec, tid, w);
       // the logit at the draft token, if this stage holds it (one shared load)
       if (!GREEDY && tid == 0) {
-        const int off = d.y - d.elem0;
+        const int off = y - d.elem0;
         if (off >= 0 && off < d.nvec * N)
           xy = DT == SPEC_BF16 ? __uint_as_float((uint32_t)reinterpret_cast<const unsigned short*>(vec)[off] << 16)
                                : reinterpret_cast<const float*>(vec)[off];
@@ -959,18 +983,18 @@ __device__ void consumer_role(const Params& P, VSmem& S, int cw, int lane) {
       release(stage);
       advance();
       if (d.flags & F_LAST) {
-        if (tid == 0 && (d.nhead > 0 || d.ntail > 0)) {
-          const unsigned char* tens = d.kind == KIND_TARGET ? P.target : P.draft;
-          const long long row0 = row_elem_offset(d.kind, d.b, d.i, P.G, P.V);
-          for (int k = 0; k < d.nhead; ++k) {
-            const float x = load_logit(tens, DT, row0 + d.head0 + k);
-            if (d.head0 + k == d.y) xy = x;
-            run_scalar<GREEDY>(r, x, d.head0 + k, c, ent);
+        if (tid == 0 && (it.nhead > 0 || it.ntail > 0)) {
+          const unsigned char* tens = it.kind == KIND_TARGET ? P.target : P.draft;
+          const long long row0 = row_elem_offset(it.kind, it.b, it.i, P.G, P.V);
+          for (int k = 0; k < it.nhead; ++k) {
+            const float x = load_logit(tens, DT, row0 + it.head0 + k);
+            if (it.head0 + k == y) xy = x;
+            run_scalar<GREEDY>(r, x, it.head0 + k, c, ent);
           }
-          for (int k = 0; k < d.ntail; ++k) {
-            const float x = load_logit(tens, DT, row0 + d.tail0 + k);
-            if (d.tail0 + k == d.y) xy = x;
-            run_scalar<GREEDY>(r, x, d.tail0 + k, c, ent);
+          for (int k = 0; k < it.ntail; ++k) {
+            const float x = load_logit(tens, DT, row0 + it.tail0 + k);
+            if (it.tail0 + k == y) xy = x;
+            run_scalar<GREEDY>(r, x, it.tail0 + k, c, ent);
           }
         }
         Part p;
@@ -984,8 +1008,8 @@ __device__ void consumer_role(const Params& P, VSmem& S, int cw, int lane) {
         if (!to_epilogue([&](EpiSlot& E) {
               if (lane == 0) E.part[cw] = p;
               if (tid == 0) {
-                E.type = IT_STATS; E.row_id = d.row_id; E.b = d.b; E.i = d.i; E.kind = d.kind;
-                E.chunk = d.chunk; E.xy = xy;
+                E.type = IT_STATS; E.row_id = it.row_id; E.b = it.b; E.i = it.i; E.kind = it.kind;
+                E.chunk = it.chunk; E.xy = xy;
               }
             }))
           return;
@@ -994,7 +1018,8 @@ __device__ void consumer_role(const Params& P, VSmem& S, int cw, int lane) {
     }
 
     // IT_DSUM: one slice of the draw's weights (a stage pair for the residual)
-    const bool resid = d.aux == DK_RESID;
+    const ItemDesc& it = S.item[d.item & (kItemSlots - 1)];
+    const bool resid = it.aux == DK_RESID;
     const int st1 = stage;
     const uint4* vec2 = vec;
     if (resid) {
@@ -1008,9 +1033,12 @@ __device__ void consumer_role(const Params& P, VSmem& S, int cw, int lane) {
     load_stage<DT>(vec, d.nvec, tid, wt);
     if (resid) load_stage<DT>(vec2, d.nvec, tid, wd);
     ResidW R;
-    R.c = d.c; R.mpc = d.m1 * d.c; R.mqc = d.m2 * d.c; R.rp = 1.f / d.s1; R.rq = 1.f / d.s2;
-    const float mc = d.m1 * d.c;
-    tword* gs_out = P.gsum + ((size_t)d.b * P.nres + d.chunk) * kGroupsPerStage;
+    R.c = it.c; R.mpc = it.m1 * it.c; R.mqc = it.m2 * it.c; R.rp = 1.f / it.s1; R.rq = 1.f / it.s2;
+    const float mc = it.m1 * it.c;
+    const float cd = it.c;
+    const int excl = it.y;
+    const unsigned dtag = it.tag;
+    tword* gs_out = P.gsum + ((size_t)it.b * P.nres + it.chunk) * kGroupsPerStage;
     double dsum = 0.0;                  // lane 0: this warp's groups, in q order
 #pragma unroll
     for (int q = 0; q < kVecPerThread; ++q) {
@@ -1024,9 +1052,9 @@ __device__ void consumer_role(const Params& P, VSmem& S, int cw, int lane) {
         for (int k = 0; k < N; ++k) e[k] = R(xt[k], xd[k]);
       } else {
 #pragma unroll
-        for (int k = 0; k < N; ++k) e[k] = ex2(fmaf(xt[k], d.c, -mc));
-        if (d.y >= 0) {
-          const int off = d.y - (d.elem0 + v * N);
+        for (int k = 0; k < N; ++k) e[k] = ex2(fmaf(xt[k], cd, -mc));
+        if (excl >= 0) {
+          const int off = excl - (d.elem0 + v * N);
           if (off >= 0 && off < N)
 #pragma unroll
             for (int k = 0; k < N; ++k)
@@ -1041,7 +1069,7 @@ __device__ void consumer_role(const Params& P, VSmem& S, int cw, int lane) {
       for (int off = 16; off >= 1; off >>= 1) g += __shfl_xor_sync(0xffffffffu, g, off);
       const int gi = v / kGroupVecs;
       if (lane == 0 && gi * kGroupVecs < d.nvec) {
-        st_tw(gs_out + gi, tw_make(__float_as_uint(g), d.tag));
+        st_tw(gs_out + gi, tw_make(__float_as_uint(g), dtag));
         dsum += (double)g;
       }
     }
@@ -1050,7 +1078,7 @@ __device__ void consumer_role(const Params& P, VSmem& S, int cw, int lane) {
     advance();
     if (!to_epilogue([&](EpiSlot& E) {
           if (lane == 0) E.dsum[cw] = dsum;
-          if (tid == 0) { E.type = IT_DSUM; E.b = d.b; E.chunk = d.chunk; E.i = d.i; E.tag = d.tag; }
+          if (tid == 0) { E.type = IT_DSUM; E.b = it.b; E.chunk = it.chunk; E.i = it.i; E.tag = dtag; }
         }))
       return;
   }
@@ -1650,6 +1678,23 @@ cudaError_t configure_kernels() {
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(verify_kernel<SPEC_BF16, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   return e;
+}
+
+// Resident CTAs per SM of the verify kernel (the least over its
+// instantiations).  The kernel is persistent and its CTAs wait on one
+// another, so its grid never exceeds what is resident at once.
+cudaError_t verify_blocks_per_sm(int* out) {
+  void (*ks[4])(Params) = {verify_kernel<SPEC_F32, false>, verify_kernel<SPEC_F32, true>,
+                           verify_kernel<SPEC_BF16, false>, verify_kernel<SPEC_BF16, true>};
+  int best = 1 << 30;
+  for (auto k : ks) {
+    int n = 0;
+    const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, kStatsThreads, verify_smem_bytes());
+    if (e != cudaSuccess) return e;
+    best = n < best ? n : best;
+  }
+  *out = best;
+  return cudaSuccess;
 }
 
 cudaError_t launch_plan(const Params& P, cudaStream_t s) {
