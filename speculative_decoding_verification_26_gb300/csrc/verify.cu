@@ -683,9 +683,9 @@ __device__ __forceinline__ bool put_stage(VSmem& S, int& stage, uint32_t& phase,
   return true;
 }
 
-template <int DT, bool GREEDY>
+template <int DT, bool GREEDY, class Hook>
 __device__ bool stage_stats_item(const Params& P, VSmem& S, int& stage, uint32_t& phase, const ItemMeta& cur,
-                                 int islot) {
+                                 int islot, Hook&& after_piece) {
   constexpr int ES = DT == SPEC_BF16 ? 2 : 4;
   const int G = P.G, V = P.V;
   const int ce = chunk_elems(DT);
@@ -725,6 +725,7 @@ __device__ bool stage_stats_item(const Params& P, VSmem& S, int& stage, uint32_t
     d.nvec = (int)(bytes / 16);
     d.flags = (p == 0 ? F_FIRST : 0) | (p == npieces - 1 ? F_LAST : 0);
     if (!put_stage(S, stage, phase, d, p == 0 ? &it : nullptr, A0 + (uintptr_t)off, bytes)) return false;
+    after_piece();
   }
   return true;
 }
@@ -808,14 +809,13 @@ __device__ void producer_role(const Params& P, VSmem& S, unsigned epoch) {
   bool ok = true;
   const bool dyn = !GREEDY && (P.mode == MODE_SAMPLE || P.mode == MODE_ONEHOT);
   unsigned ticket = dyn ? atomicAdd(&P.hdr->dq_head.v, 1u) : 0xffffffffu;
-  // software pipeline over static items: cur (metadata complete), item n+1
-  // (row id known), item n+2 (claimed)
+  // Static items are claimed one ahead: the next item is claimed before the
+  // current one is staged, and its row id and per-request values are fetched
+  // between the current item's stages (each of which waits for a ring slot,
+  // hiding the loads).  So no claimed item waits long in a busy CTA at the
+  // end, and the skip test reads a recent first reject.
   const unsigned q0 = atomicAdd(&P.hdr->queue.v, 1u);
-  const unsigned q1 = atomicAdd(&P.hdr->queue.v, 1u);
-  unsigned q2 = atomicAdd(&P.hdr->queue.v, 1u);
   ItemMeta cur = finish_meta(P, item_meta_raw<GREEDY>(P, q0, item_row(P, q0, n_items), n_items), n_items);
-  unsigned q_next = q1;
-  int rid_next = item_row(P, q1, n_items);
   long long idle_since = -1;      // clock64 at the start of the current idle spell
   unsigned sleep_ns = 64;
   while (ok) {
@@ -830,15 +830,18 @@ __device__ void producer_role(const Params& P, VSmem& S, unsigned epoch) {
       t1 = ld_tw(P.dq + 2 * (size_t)ticket + 1);
     }
     if (cur.valid) {
-      // loads for the next items, issued before the (blocking) staging
-      const RawMeta nxt = item_meta_raw<GREEDY>(P, q_next, rid_next, n_items);
-      const int rid2 = item_row(P, q2, n_items);
-      const unsigned q3 = q2 < n_items ? atomicAdd(&P.hdr->queue.v, 1u) : q2;
-      if (!cur.skip) ok = stage_stats_item<DT, GREEDY>(P, S, stage, phase, cur, islot++ & (kItemSlots - 1));   // a voided row is not read
+      const unsigned qn = atomicAdd(&P.hdr->queue.v, 1u);
+      int step = 0, rid = 0;
+      RawMeta nxt;
+      auto fetch_next = [&]() {      // one dependent step of the next item's metadata
+        if (step == 0) rid = item_row(P, qn, n_items);
+        else if (step == 1) nxt = item_meta_raw<GREEDY>(P, qn, rid, n_items);
+        ++step;
+      };
+      if (!cur.skip)                 // a voided row is not read
+        ok = stage_stats_item<DT, GREEDY>(P, S, stage, phase, cur, islot++ & (kItemSlots - 1), fetch_next);
+      while (step < 2) fetch_next();
       cur = finish_meta(P, nxt, n_items);
-      q_next = q2;
-      rid_next = rid2;
-      q2 = q3;
       did = true;
     }
     if (ok && tw_ok(t0, part_tag(epoch)) && tw_ok(t1, part_tag(epoch))) {
@@ -863,7 +866,7 @@ __device__ void producer_role(const Params& P, VSmem& S, unsigned epoch) {
     if (idle_since < 0) idle_since = now;
     else if (now - idle_since > kWaitLimitCycles) { ok = false; break; }
     __nanosleep(sleep_ns);
-    if (sleep_ns < 1024) sleep_ns *= 2;
+    if (sleep_ns < 256) sleep_ns *= 2;
   }
   if (ok && wait_bar(S, &S.empty[stage], phase ^ 1u)) {
     S.desc[stage].flags = F_TERM;
@@ -1147,13 +1150,17 @@ __device__ void epilogue_role(const Params& P, VSmem& S, int lane, int e, unsign
 // role of any CTA has given up (the header error word).
 struct OwnerClock {
   long long c0;
-  __device__ __forceinline__ void start() { c0 = clock64(); }
-  __device__ __forceinline__ bool expired(const Params& P) const {
+  int polls;
+  __device__ __forceinline__ void start() { c0 = clock64(); polls = 0; }
+  __device__ __forceinline__ bool expired(const Params& P) {
     const bool mine = __any_sync(0xffffffffu, clock64() - c0 > kWaitLimitCycles);
     if (mine) {   // this wait gave up: every other role gives up too
       if ((threadIdx.x & 31) == 0) atomicOr(&P.hdr->error.v, (unsigned)SPEC_ST_TIMEOUT);
       return true;
     }
+    // the error word of the other roles is read every 8th poll only (a read
+    // per poll would double the round trips of every poll)
+    if ((++polls & 7) != 0) return false;
     return __any_sync(0xffffffffu, ld_relaxed_u32(&P.hdr->error.v) != 0u);
   }
 };
@@ -1205,6 +1212,54 @@ __device__ bool merge_row(const Params& P, int rid, int y, float c, bool ent, un
   }
   out.st.m = r.m; out.st.s = r.s; out.st.t = r.t; out.st.idx = r.idx;
   out.xy = (ychunk >= 0 && ychunk < nch) ? __shfl_sync(0xffffffffu, xy, ychunk & 31) : qnan();
+  return true;
+}
+
+// Target row ridT and draft row ridD of one position, merged together
+// (warp-wide; needs 2 * nch <= 32): lanes 0-15 take the target's chunks,
+// lanes 16-31 the draft's, so one poll covers both rows.  Each half merges
+// with the same tree as merge_row (its xor-16 level only meets empty
+// partials, which merge exactly), so the results are identical to two
+// merge_row calls.  False if the wait gave up.
+__device__ bool merge_pair(const Params& P, int ridT, int ridD, int y, float c, bool entD, unsigned epoch, int lane,
+                           RowRes& T, RowRes& D) {
+  const int nch = P.nch;
+  const int half = lane >> 4, k = lane & 15;
+  const tword* base = P.cparts + (size_t)(half ? ridD : ridT) * nch * kPartWords;
+  const bool ent = half ? entD : false;
+  const int ychunk = y >= 0 ? y / chunk_elems(P.dtype) : -1;
+  tword w[kPartWords];
+  OwnerClock clk;
+  clk.start();
+  while (true) {
+    bool ok = true;
+    if (k < nch) {
+#pragma unroll
+      for (int j = 0; j < kPartWords; ++j) {
+        w[j] = ld_tw(base + (size_t)k * kPartWords + j);
+        ok &= tw_ok(w[j], part_tag(epoch));
+      }
+    }
+    if (__all_sync(0xffffffffu, ok)) break;
+    if (clk.expired(P)) return false;
+  }
+  Part r = empty_part();
+  float xy = qnan();
+  if (k < nch) {
+    Part q;
+    q.m = tw_f32(w[0]); q.s = tw_f32(w[1]); q.t = tw_f32(w[2]); q.idx = (int)tw_u32(w[3]);
+    r = merge_parts(r, q, c, ent);
+    if (k == ychunk) xy = tw_f32(w[4]);
+  }
+#pragma unroll
+  for (int off = 8; off >= 1; off >>= 1) r = merge_parts(r, shfl_part(r, off), c, ent);
+  T.st.m = __shfl_sync(0xffffffffu, r.m, 0);  T.st.s = __shfl_sync(0xffffffffu, r.s, 0);
+  T.st.t = __shfl_sync(0xffffffffu, r.t, 0);  T.st.idx = __shfl_sync(0xffffffffu, r.idx, 0);
+  D.st.m = __shfl_sync(0xffffffffu, r.m, 16); D.st.s = __shfl_sync(0xffffffffu, r.s, 16);
+  D.st.t = __shfl_sync(0xffffffffu, r.t, 16); D.st.idx = __shfl_sync(0xffffffffu, r.idx, 16);
+  const bool yin = ychunk >= 0 && ychunk < nch;
+  T.xy = yin ? __shfl_sync(0xffffffffu, xy, ychunk) : qnan();
+  D.xy = yin ? __shfl_sync(0xffffffffu, xy, 16 + ychunk) : qnan();
   return true;
 }
 
@@ -1542,12 +1597,22 @@ __device__ void serve_request(const Params& P, int b, unsigned epoch, int lane) 
     for (int i = 0; i < gam; ++i) {
       const int y = P.draft_tokens[(size_t)b * G + i];
       RowRes T, D{};
-      if (!merge_row<GREEDY>(P, target_row_id(b, i, G), GREEDY ? -1 : y, c, false, epoch, lane, T)) {
-        failed = true;
-        break;
+      if (sample && 2 * P.nch <= 32) {
+        if (!merge_pair(P, target_row_id(b, i, G), draft_row_id(b, i, B, G), y, c, sig, epoch, lane, T, D)) {
+          failed = true;
+          break;
+        }
+      } else {
+        if (!merge_row<GREEDY>(P, target_row_id(b, i, G), GREEDY ? -1 : y, c, false, epoch, lane, T)) {
+          failed = true;
+          break;
+        }
+        if (sample && !merge_row<false>(P, draft_row_id(b, i, B, G), y, c, sig, epoch, lane, D)) {
+          failed = true;
+          break;
+        }
       }
       if (sample) {
-        if (!merge_row<false>(P, draft_row_id(b, i, B, G), y, c, sig, epoch, lane, D)) { failed = true; break; }
         take_draft(i, D);
         ndraft = i + 1;
       }
