@@ -144,6 +144,16 @@ int run(const Call& c) {
   P.dq = reinterpret_cast<tword*>(ws + L.dq);
   P.nrows = L.nrows; P.nch = L.nch; P.nres = L.nres; P.dq_cap = L.dq_cap;
   P.aligned_rows = ((size_t)c.V * es) % 16 == 0 && aligned(c.target, 16) && aligned(c.draft, 16);
+  // Rows a draw may read again (positions 0 .. keep_pos, both models in the
+  // full-q mode) are loaded with an evict-last L2 policy, as long as they
+  // fill at most 3/4 of the 129 MB L2 of a GB300; the draw then reads them
+  // from L2.  Calls without draws keep nothing.
+  P.keep_pos = -1;
+  if (sample || c.mode == MODE_ONEHOT) {
+    const double per_pos = (double)c.B * (sample ? 2 : 1) * c.V * es;
+    const double budget = 0.75 * 129.0 * 1024 * 1024;
+    for (int j = 0; j <= c.G && (j + 1) * per_pos <= budget; ++j) P.keep_pos = j;
+  }
 
   // persistent grid: every CTA resident at once (two per SM), never more
   // CTAs than work items

@@ -669,13 +669,13 @@ __device__ __forceinline__ ItemMeta finish_meta(const Params& P, const RawMeta& 
 // (first piece of an item) and the stage's, start the bulk copy (bytes > 0)
 // or just mark it full.
 __device__ __forceinline__ bool put_stage(VSmem& S, int& stage, uint32_t& phase, const StageDesc& d,
-                                          const ItemDesc* it, uintptr_t src, uint32_t bytes) {
+                                          const ItemDesc* it, uintptr_t src, uint32_t bytes, uint64_t policy) {
   if (!wait_bar(S, &S.empty[stage], phase ^ 1u)) return false;
   if (it) S.item[d.item & (kItemSlots - 1)] = *it;
   S.desc[stage] = d;
   if (bytes > 0) {
     mbar_arrive_expect_tx(&S.full[stage], bytes);
-    bulk_load(S.ring[stage], reinterpret_cast<const void*>(src), bytes, &S.full[stage]);
+    bulk_load_hint(S.ring[stage], reinterpret_cast<const void*>(src), bytes, &S.full[stage], policy);
   } else {
     mbar_arrive(&S.full[stage]);
   }
@@ -718,13 +718,14 @@ __device__ bool stage_stats_item(const Params& P, VSmem& S, int& stage, uint32_t
   it.y = cur.y;
   StageDesc d;
   d.item = islot;
+  const uint64_t pol = l2_policy(cur.i <= P.keep_pos);
   for (int p = 0; p < npieces; ++p) {
     const long long off = (long long)p * kStageBytes;
     const uint32_t bytes = mid > 0 ? (uint32_t)(mid - off < kStageBytes ? mid - off : kStageBytes) : 0u;
     d.elem0 = (int)((A0 + (uintptr_t)off - rowaddr) / ES);
     d.nvec = (int)(bytes / 16);
     d.flags = (p == 0 ? F_FIRST : 0) | (p == npieces - 1 ? F_LAST : 0);
-    if (!put_stage(S, stage, phase, d, p == 0 ? &it : nullptr, A0 + (uintptr_t)off, bytes)) return false;
+    if (!put_stage(S, stage, phase, d, p == 0 ? &it : nullptr, A0 + (uintptr_t)off, bytes, pol)) return false;
     after_piece();
   }
   return true;
@@ -745,11 +746,12 @@ __device__ __forceinline__ bool put_row_range(const Params& P, VSmem& S, int& st
   if (P.aligned_rows) {
     const uint32_t bytes = (uint32_t)((e1 - e0) * ES);
     d.nvec = (int)(bytes / 16);
-    return put_stage(S, stage, phase, d, it, reinterpret_cast<uintptr_t>(tens) + (uintptr_t)(src * ES), bytes);
+    return put_stage(S, stage, phase, d, it, reinterpret_cast<uintptr_t>(tens) + (uintptr_t)(src * ES), bytes,
+                     l2_policy(false));
   }
   d.flags |= F_DIRECT;
   d.nvec = (e1 - e0 + (16 / ES) - 1) / (16 / ES);
-  return put_stage(S, stage, phase, d, it, 0, 0u);
+  return put_stage(S, stage, phase, d, it, 0, 0u, 0ull);
 }
 
 // A draw slice: rows k of the request (the descriptor, written by the owner
