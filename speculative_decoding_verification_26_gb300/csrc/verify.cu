@@ -1265,6 +1265,75 @@ __device__ bool merge_pair(const Params& P, int ridT, int ridD, int y, float c, 
   return true;
 }
 
+// Up to four rows at once (warp-wide; needs nch <= 8): row s in lanes
+// 8s .. 8s+7, given per lane by its segment's row id (< 0: no row), draft
+// token and entropy flag.  Segments in need_mask are waited for; the others
+// are taken only if already complete.  Each row merges with the same tree as
+// merge_row (its xor-16 and xor-8 levels only meet empty partials, which
+// merge exactly), so results are identical.  Every lane of segment s ends
+// with row s's statistics in pm and its x_y in xy.  Returns the mask of the
+// segments taken (absent rows count as taken), or -1 if the wait gave up.
+template <bool GREEDY>
+__device__ int merge_rows4(const Params& P, int rid, int y, bool ent, unsigned need_mask, float c, unsigned epoch,
+                           int lane, Part& pm, float& xy) {
+  const int nch = P.nch;
+  const int seg = lane >> 3, k = lane & 7;
+  const bool has = rid >= 0 && k < nch;
+  const tword* base = P.cparts + ((size_t)(rid < 0 ? 0 : rid) * nch + k) * kPartWords;
+  tword w[kPartWords];
+  unsigned ready = 0;
+  OwnerClock clk;
+  clk.start();
+  while (true) {
+    bool ok = true;
+    if (has) {
+#pragma unroll
+      for (int j = 0; j < kPartWords; ++j) {
+        w[j] = ld_tw(base + j);
+        ok &= tw_ok(w[j], part_tag(epoch));
+      }
+    }
+    const unsigned bal = __ballot_sync(0xffffffffu, ok);
+    ready = 0;
+#pragma unroll
+    for (int s2 = 0; s2 < 4; ++s2)
+      if (((bal >> (8 * s2)) & 0xffu) == 0xffu) ready |= 1u << s2;
+    if ((ready & need_mask) == need_mask) break;
+    if (clk.expired(P)) return -1;
+  }
+  const bool take = has && ((ready >> seg) & 1u);
+  Part r = empty_part();
+  float x = qnan();
+  if (take) {
+    Part q;
+    q.m = tw_f32(w[0]); q.s = tw_f32(w[1]); q.t = tw_f32(w[2]); q.idx = (int)tw_u32(w[3]);
+    r = GREEDY ? merge_argmax(r, q) : merge_parts(r, q, c, ent);
+    x = tw_f32(w[4]);
+  }
+#pragma unroll
+  for (int off = 4; off >= 1; off >>= 1) {
+    const Part o = shfl_part(r, off);
+    r = GREEDY ? merge_argmax(r, o) : merge_parts(r, o, c, ent);
+  }
+  pm = r;
+  const int ychunk = y >= 0 ? y / chunk_elems(P.dtype) : -1;
+  const bool yin = ychunk >= 0 && ychunk < nch;
+  const float xs = __shfl_sync(0xffffffffu, x, (seg << 3) | (yin ? ychunk : 0));
+  xy = yin ? xs : qnan();
+  return (int)ready;
+}
+
+// Row s of a merge_rows4 result, as every lane sees it.
+__device__ __forceinline__ RowRes row_of(const Part& pm, float xy, int s) {
+  RowRes o;
+  o.st.m = __shfl_sync(0xffffffffu, pm.m, 8 * s);
+  o.st.s = __shfl_sync(0xffffffffu, pm.s, 8 * s);
+  o.st.t = __shfl_sync(0xffffffffu, pm.t, 8 * s);
+  o.st.idx = __shfl_sync(0xffffffffu, pm.idx, 8 * s);
+  o.xy = __shfl_sync(0xffffffffu, xy, 8 * s);
+  return o;
+}
+
 __device__ __forceinline__ int status_of_code(int code) {
   return code == PC_NONFINITE ? SPEC_ST_NONFINITE
        : code == PC_BAD_TOKEN ? SPEC_ST_BAD_TOKEN
@@ -1595,7 +1664,57 @@ __device__ void serve_request(const Params& P, int b, unsigned epoch, int lane) 
     }
   };
 
-  if (P.mode != MODE_SIGNALS) {
+  // Position i decided from its merged rows; false once the scan stops.
+  auto decide = [&](int i, int y, const RowRes& T, const RowRes& D) -> bool {
+    if (sample) {
+      take_draft(i, D);
+      ndraft = i + 1;
+    }
+    float a;
+    const int code = evaluate_pos<GREEDY>(P, b, i, T, D, y, c, &a);
+    if (lane == i) a_lane = a;
+    if (code & PC_UNCERTAIN) {
+      if (lane == 0) atomicAdd(&HDR_UNCERTAIN(P.hdr), 1u);
+    } else if (code != PC_ACCEPT && lane == 0) {
+      asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" ::"l"(P.known_reject + b), "r"(i) : "memory");  // early exit
+    }
+    if ((code & 15) == PC_ACCEPT) return true;
+    k = i;
+    if ((code & 15) == PC_REJECT) { rejected = true; rt = T; rd = D; }
+    else st = status_of_code(code & 15);
+    return false;
+  };
+  bool bonus = false;                         // the bonus row is merged (into rt)
+  if (P.mode != MODE_SIGNALS && P.nch <= 8) {
+    // position i, and position i+1 (or the bonus row) too when its rows are
+    // already complete: an owner behind the stream catches up two at a time
+    for (int i = 0; i < gam;) {
+      const int i1 = i + 1;
+      const int y0 = P.draft_tokens[(size_t)b * G + i];
+      const int y1 = i1 < gam ? P.draft_tokens[(size_t)b * G + i1] : -1;
+      const int seg = lane >> 3;
+      int rid = -1;
+      if (seg == 0) rid = target_row_id(b, i, G);
+      else if (seg == 1) rid = sample ? draft_row_id(b, i, B, G) : -1;
+      else if (seg == 2) rid = i1 <= gam ? target_row_id(b, i1, G) : -1;
+      else rid = (sample && i1 < gam) ? draft_row_id(b, i1, B, G) : -1;
+      const int yl = GREEDY ? -1 : (seg < 2 ? y0 : y1);
+      Part pm;
+      float xy;
+      const int ready = merge_rows4<GREEDY>(P, rid, yl, (seg & 1) && sig, 3u, c, epoch, lane, pm, xy);
+      if (ready < 0) { failed = true; break; }
+      const RowRes T0 = row_of(pm, xy, 0), D0 = row_of(pm, xy, 1);
+      if (!decide(i, y0, T0, D0)) break;
+      if (i1 < gam && (ready & 12) == 12) {
+        const RowRes T1 = row_of(pm, xy, 2), D1 = row_of(pm, xy, 3);
+        if (!decide(i1, y1, T1, D1)) break;
+        i += 2;
+      } else {
+        if (i1 == gam && (ready & 4)) { rt = row_of(pm, xy, 2); bonus = true; }
+        i += 1;
+      }
+    }
+  } else if (P.mode != MODE_SIGNALS) {
     for (int i = 0; i < gam; ++i) {
       const int y = P.draft_tokens[(size_t)b * G + i];
       RowRes T, D{};
@@ -1614,29 +1733,12 @@ __device__ void serve_request(const Params& P, int b, unsigned epoch, int lane) 
           break;
         }
       }
-      if (sample) {
-        take_draft(i, D);
-        ndraft = i + 1;
-      }
-      float a;
-      const int code = evaluate_pos<GREEDY>(P, b, i, T, D, y, c, &a);
-      if (lane == i) a_lane = a;
-      if (code & PC_UNCERTAIN) {
-        if (lane == 0) atomicAdd(&HDR_UNCERTAIN(P.hdr), 1u);
-      } else if (code != PC_ACCEPT && lane == 0) {
-        asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" ::"l"(P.known_reject + b), "r"(i) : "memory");  // early exit
-      }
-      if ((code & 15) != PC_ACCEPT) {
-        k = i;
-        if ((code & 15) == PC_REJECT) { rejected = true; rt = T; rd = D; }
-        else st = status_of_code(code & 15);
-        break;
-      }
+      if (!decide(i, y, T, D)) break;
     }
-    if (!failed && st == 0 && !rejected) {      // every position accepted: the bonus row
-      if (!merge_row<GREEDY>(P, target_row_id(b, gam, G), -1, c, false, epoch, lane, rt)) failed = true;
-      else if (!row_ok(rt.st, GREEDY)) st = SPEC_ST_NONFINITE;
-    }
+  }
+  if (P.mode != MODE_SIGNALS && !failed && st == 0 && !rejected) {   // every position accepted: the bonus row
+    if (!bonus && !merge_row<GREEDY>(P, target_row_id(b, gam, G), -1, c, false, epoch, lane, rt)) failed = true;
+    else if (!row_ok(rt.st, GREEDY)) st = SPEC_ST_NONFINITE;
   }
   // the draw rounds are started before the remaining signal rows are merged
   const bool draw = !GREEDY && P.mode != MODE_SIGNALS && !failed && st == 0;
@@ -1653,10 +1755,23 @@ __device__ void serve_request(const Params& P, int b, unsigned epoch, int lane) 
     }
   }
   if (sig && !failed) {
-    for (int i = ndraft; i < gam; ++i) {
-      RowRes D;
-      if (!merge_row<false>(P, draft_row_id(b, i, B, G), -1, c, true, epoch, lane, D)) { failed = true; break; }
-      take_draft(i, D);
+    for (int i = ndraft; i < gam;) {
+      if (P.nch <= 8) {            // up to four draft rows per pass: the first waited for
+        const int j = i + (lane >> 3);
+        Part pm;
+        float xy;
+        const int ready = merge_rows4<false>(P, j < gam ? draft_row_id(b, j, B, G) : -1, -1, true, 1u, c, epoch,
+                                             lane, pm, xy);
+        if (ready < 0) { failed = true; break; }
+        int s2 = 0;
+        for (; s2 < 4 && i + s2 < gam && ((ready >> s2) & 1); ++s2) take_draft(i + s2, row_of(pm, xy, s2));
+        i += s2;
+      } else {
+        RowRes D;
+        if (!merge_row<false>(P, draft_row_id(b, i, B, G), -1, c, true, epoch, lane, D)) { failed = true; break; }
+        take_draft(i, D);
+        ++i;
+      }
     }
   }
   if (draw && st == 0 && !failed) {
