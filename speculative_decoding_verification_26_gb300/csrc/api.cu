@@ -142,7 +142,8 @@ int run(const Call& c) {
   P.gsum = reinterpret_cast<tword*>(ws + L.gsum);
   P.dd = reinterpret_cast<tword*>(ws + L.dd);
   P.dq = reinterpret_cast<tword*>(ws + L.dq);
-  P.nrows = L.nrows; P.nch = L.nch; P.nres = L.nres; P.dq_cap = L.dq_cap;
+  P.defq = reinterpret_cast<tword*>(ws + L.defq);
+  P.nrows = L.nrows; P.nch = L.nch; P.nres = L.nres; P.dq_cap = L.dq_cap; P.def_cap = L.def_cap;
   P.aligned_rows = ((size_t)c.V * es) % 16 == 0 && aligned(c.target, 16) && aligned(c.draft, 16);
   // Rows a draw may read again (positions 0 .. keep_pos, both models in the
   // full-q mode) are loaded with an evict-last L2 policy, as long as they

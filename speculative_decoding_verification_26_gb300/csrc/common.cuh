@@ -82,11 +82,12 @@ struct alignas(16) RowStats {
 
 struct Layout {
   size_t hdr, req_flags, known_reject, row_list, req_scale, req_gam, req_status, req_fin, cparts, dsum, gsum, dd, dq,
-      total;
+      defq, total;
   int nrows;      // B*(G+1) + B*G row ids
   int nch;        // statistics chunks per row
   int nres;       // draw slices per row (one stage each)
   int dq_cap;     // dynamic queue capacity
+  int def_cap;    // deferred queue capacity (statistics items of draft rows)
 };
 
 // Counters of one call, each on its own 128-byte line: they are hit by
@@ -100,6 +101,8 @@ struct Header {
   Counter queue;        // next static (statistics) item to claim
   Counter dq_head;      // next dynamic-queue ticket
   Counter dq_tail;      // dynamic items reserved
+  Counter def_head;     // next deferred-queue ticket
+  Counter def_tail;     // deferred static items reserved
   Counter done;         // requests whose outputs are written
   Counter error;        // SPEC_ST_TIMEOUT when any wait gave up
   Counter misc;         // n_items, n_valid, exited, n_uncertain, epoch, magic (rarely written)
@@ -135,6 +138,7 @@ __host__ inline Layout make_layout(int B, int G, int V, int dtype) {
   L.nch = (V + ce - 1) / ce;
   L.nres = (V + se - 1) / se;
   L.dq_cap = B * (2 * L.nres + 2);   // a draw restarted once after zero mass
+  L.def_cap = B * G * L.nch;
   size_t o = 0;
   L.hdr = o;          o = align256(o + sizeof(Header));
   L.req_flags = o;    o = align256(o + sizeof(int) * B);
@@ -149,6 +153,7 @@ __host__ inline Layout make_layout(int B, int G, int V, int dtype) {
   L.gsum = o;         o = align256(o + sizeof(tword) * (size_t)B * L.nres * kGroupsPerStage);
   L.dd = o;           o = align256(o + sizeof(tword) * kDrawWords * (size_t)B);
   L.dq = o;           o = align256(o + sizeof(tword) * 2 * (size_t)L.dq_cap);
+  L.defq = o;         o = align256(o + sizeof(tword) * (size_t)L.def_cap);
   L.total = o;
   return L;
 }
@@ -186,7 +191,8 @@ struct Params {
   tword* gsum;                   // [B][nres][kGroupsPerStage] draw group sums (fp32)
   tword* dd;                     // [B][kDrawWords] draw descriptors
   tword* dq;                     // [dq_cap][2] dynamic work queue
-  int nrows, nch, nres, dq_cap;
+  tword* defq;                   // [def_cap] deferred statistics items (item index)
+  int nrows, nch, nres, dq_cap, def_cap;
 };
 
 // row ids: target rows first, then draft rows

@@ -81,29 +81,22 @@ struct Block {
   int type, i;
 };
 
-// Schedule blocks in position-major order.  Full-q with signals reads every
-// draft row anyway, so draft blocks are used as filler between target
-// positions: PAIR(0) | D1 D2 | T1 | D3 D4 | T2 | ... | T_G.  Between the
-// target rows of positions i-1 and i there are then about 2B rows of other
-// work, longer than the reading window of the whole GPU, so the test at i-1
-// is usually decided before target row i of the request is claimed.  Draft
-// block j always precedes target block j, as the test at j needs both.
+// Schedule blocks in position-major order: PAIR(i) holds target row i and
+// (full q) draft row i of every request, so the rows a position's test
+// needs come together.  Draft rows of requests already rejected at an
+// earlier position are only needed for the signals: the producer defers them
+// to the end (deferred queue), so live requests' rows are read first and
+// their tests and draws finish while the signal rows stream.
 __device__ inline int build_blocks(int mode, int signals_on, int G, Block* out) {
   int n = 0;
   if (mode == MODE_SIGNALS) {
     for (int i = 0; i < G; ++i) out[n++] = {BT_D, i};
-  } else if (mode == MODE_SAMPLE && signals_on && G > 0) {
-    out[n++] = {BT_PAIR, 0};
-    int dnext = 1;
-    for (int i = 1; i <= G; ++i) {
-      for (int f = 0; f < 2 && dnext <= G - 1; ++f) out[n++] = {BT_D, dnext++};
-      out[n++] = {BT_T, i};
-    }
   } else if (mode == MODE_SAMPLE) {
     for (int i = 0; i <= G; ++i) out[n++] = {BT_PAIR, i};
   } else {
     for (int i = 0; i <= G; ++i) out[n++] = {BT_T, i};
   }
+  (void)signals_on;
   return n;
 }
 
@@ -127,6 +120,7 @@ __device__ inline void clear_tagged(const Params& P, int tid, int nth) {
   for (size_t j = tid; j < n_gsum; j += nth) P.gsum[j] = 0ull;
   for (size_t j = tid; j < (size_t)kDrawWords * P.B; j += nth) P.dd[j] = 0ull;
   for (size_t j = tid; j < 2 * (size_t)P.dq_cap; j += nth) P.dq[j] = 0ull;
+  for (size_t j = tid; j < (size_t)P.def_cap; j += nth) P.defq[j] = 0ull;
 }
 
 __global__ void __launch_bounds__(1024) plan_kernel(Params P) {
@@ -205,6 +199,8 @@ __global__ void __launch_bounds__(1024) plan_kernel(Params P) {
     HDR_UNCERTAIN(P.hdr) = 0u;
     P.hdr->dq_head.v = 0u;
     P.hdr->dq_tail.v = 0u;
+    P.hdr->def_head.v = 0u;
+    P.hdr->def_tail.v = 0u;
     P.hdr->done.v = 0u;
     HDR_N_VALID(P.hdr) = (unsigned)B - s_settled;
     HDR_EXITED(P.hdr) = 0u;
@@ -613,7 +609,7 @@ enum DrawWord : int { DW_KIND = 0, DW_EXCL, DW_M1, DW_S1, DW_M2, DW_S2, DW_C, DW
 struct ItemMeta {
   unsigned q;
   int rid, b, i, kind, chunk, y;
-  bool valid, skip;
+  bool valid, skip, defer;          // defer: a signal-only draft row, read after the main queue
   float c;
 };
 
@@ -645,7 +641,7 @@ __device__ __forceinline__ RawMeta item_meta_raw(const Params& P, unsigned q, in
   const int G = P.G;
   decode_row(rid, P.B, G, m.kind, m.b, m.i);
   const int b = m.b, i = m.i;
-  if (m.kind == KIND_TARGET || !P.signals_on) m.kr = ld_relaxed(P.known_reject + b);
+  m.kr = ld_relaxed(P.known_reject + b);
   if (!GREEDY) m.c = __ldg(P.req_scale + b);
   m.gam = __ldg(P.req_gam + b);
   // the draft token (sample / one-hot only: signals-only calls have no tokens)
@@ -659,7 +655,11 @@ __device__ __forceinline__ ItemMeta finish_meta(const Params& P, const RawMeta& 
   m.valid = r.q < n_items;
   m.rid = r.rid; m.b = r.b; m.i = r.i; m.kind = r.kind;
   m.chunk = (int)(r.q % (unsigned)P.nch);
-  m.skip = r.kr < r.i;          // a reject at an earlier position voids this row
+  // a reject at an earlier position voids this row, or (draft rows with
+  // signals) leaves it needed for the signals only: it is then deferred
+  const bool late = r.kr < r.i;
+  m.defer = late && r.kind == KIND_DRAFT && P.signals_on;
+  m.skip = late && !m.defer;
   m.c = r.c;
   m.y = r.i < r.gam ? r.tok : -1;
   return m;
@@ -811,6 +811,32 @@ __device__ void producer_role(const Params& P, VSmem& S, unsigned epoch) {
   bool ok = true;
   const bool dyn = !GREEDY && (P.mode == MODE_SAMPLE || P.mode == MODE_ONEHOT);
   unsigned ticket = dyn ? atomicAdd(&P.hdr->dq_head.v, 1u) : 0xffffffffu;
+  // The draw item at the held ticket: its entry words as last loaded, staged
+  // once both carry this call's tag (one static and one draw item per round:
+  // neither kind starves the other).
+  tword t0 = 0ull, t1 = 0ull;
+  auto load_ticket = [&]() {
+    if (dyn && ticket < (unsigned)P.dq_cap) {
+      t0 = ld_tw(P.dq + 2 * (size_t)ticket);
+      t1 = ld_tw(P.dq + 2 * (size_t)ticket + 1);
+    } else {
+      t0 = t1 = 0ull;
+    }
+  };
+  auto take_draw = [&]() -> bool {
+    if (!(ok && tw_ok(t0, part_tag(epoch)) && tw_ok(t1, part_tag(epoch)))) return false;
+    DynItem it;
+    it.b = (int)tw_u32(t0);
+    it.slice = (int)(tw_u32(t1) & 0x3fffffffu);
+    it.round = (int)(tw_u32(t1) >> 30);
+    ticket = atomicAdd(&P.hdr->dq_head.v, 1u);
+    t0 = t1 = 0ull;
+    ok = stage_dyn_item<DT>(P, S, stage, phase, it, epoch, islot++ & (kItemSlots - 1));
+    return true;
+  };
+  unsigned dticket = 0xffffffffu;   // deferred-queue ticket, taken when the main queue is done
+  bool dready = false;              // dmeta holds the next deferred item
+  RawMeta dmeta;
   // Static items are claimed one ahead: the next item is claimed before the
   // current one is staged, and its row id and per-request values are fetched
   // between the current item's stages (each of which waits for a ring slot,
@@ -825,36 +851,68 @@ __device__ void producer_role(const Params& P, VSmem& S, unsigned epoch) {
     // starve the other (late target rows and early draws are both on the
     // critical path of some request)
     bool did = false;
-    // the ticket's entry words, in flight while the static item is staged
-    tword t0 = 0ull, t1 = 0ull;
-    if (dyn && ticket < (unsigned)P.dq_cap) {
-      t0 = ld_tw(P.dq + 2 * (size_t)ticket);
-      t1 = ld_tw(P.dq + 2 * (size_t)ticket + 1);
-    }
+    load_ticket();                   // in flight while the static item is staged
     if (cur.valid) {
       const unsigned qn = atomicAdd(&P.hdr->queue.v, 1u);
       int step = 0, rid = 0;
       RawMeta nxt;
-      auto fetch_next = [&]() {      // one dependent step of the next item's metadata
+      auto fetch_next = [&]() {      // one dependent step of the next item's metadata, between pieces
         if (step == 0) rid = item_row(P, qn, n_items);
         else if (step == 1) nxt = item_meta_raw<GREEDY>(P, qn, rid, n_items);
         ++step;
       };
-      if (!cur.skip)                 // a voided row is not read
-        ok = stage_stats_item<DT, GREEDY>(P, S, stage, phase, cur, islot++ & (kItemSlots - 1), fetch_next);
+      if (cur.defer) {               // read after the main queue
+        const unsigned slot = atomicAdd(&P.hdr->def_tail.v, 1u);
+        if (slot < (unsigned)P.def_cap) st_tw(P.defq + slot, tw_make(cur.q, part_tag(epoch)));
+        else atomicOr(&P.hdr->error.v, (unsigned)SPEC_ST_TIMEOUT);   // cannot happen (one entry per draft item)
+      } else if (!cur.skip) {        // a voided row is not read
+        const bool r = stage_stats_item<DT, GREEDY>(P, S, stage, phase, cur, islot++ & (kItemSlots - 1), fetch_next);
+        ok = ok && r;
+      }
       while (step < 2) fetch_next();
       cur = finish_meta(P, nxt, n_items);
       did = true;
     }
-    if (ok && tw_ok(t0, part_tag(epoch)) && tw_ok(t1, part_tag(epoch))) {
-      DynItem it;
-      it.b = (int)tw_u32(t0);
-      it.slice = (int)(tw_u32(t1) & 0x3fffffffu);
-      it.round = (int)(tw_u32(t1) >> 30);
-      ticket = atomicAdd(&P.hdr->dq_head.v, 1u);
-      ok = stage_dyn_item<DT>(P, S, stage, phase, it, epoch, islot++ & (kItemSlots - 1));
-      did = true;
+    if (ok && !cur.valid && dyn) {
+      // the main queue is done: deferred signal rows, one per round; the
+      // next entry and its metadata are fetched while one is staged
+      if (dticket == 0xffffffffu) dticket = atomicAdd(&P.hdr->def_head.v, 1u);
+      if (!dready && dticket < (unsigned)P.def_cap) {
+        const tword w = ld_tw(P.defq + dticket);
+        if (tw_ok(w, part_tag(epoch))) {
+          const unsigned qd = tw_u32(w);
+          dmeta = item_meta_raw<GREEDY>(P, qd, item_row(P, qd, n_items), n_items);
+          dready = true;
+          dticket = atomicAdd(&P.hdr->def_head.v, 1u);
+        }
+      }
+      if (dready) {
+        ItemMeta m = finish_meta(P, dmeta, n_items);
+        m.skip = m.defer = false;
+        dready = false;
+        int step = 0;
+        RawMeta nx;
+        tword wn = 0ull;
+        auto fetch_next = [&]() {    // the next entry, then its metadata, between this item's stages
+          if (step == 0) { if (dticket < (unsigned)P.def_cap) wn = ld_tw(P.defq + dticket); }
+          else if (step == 1 && tw_ok(wn, part_tag(epoch))) {
+            const unsigned qd = tw_u32(wn);
+            nx = item_meta_raw<GREEDY>(P, qd, item_row(P, qd, n_items), n_items);
+            dready = true;
+          }
+          ++step;
+        };
+        const bool r = stage_stats_item<DT, GREEDY>(P, S, stage, phase, m, islot++ & (kItemSlots - 1), fetch_next);
+        ok = ok && r;
+        while (step < 2) fetch_next();
+        if (dready) {
+          dmeta = nx;
+          dticket = atomicAdd(&P.hdr->def_head.v, 1u);
+        }
+        did = true;
+      }
     }
+    if (take_draw()) did = true;
     if (did) {
       idle_since = -1;
       sleep_ns = 64;
@@ -1740,7 +1798,8 @@ __device__ void serve_request(const Params& P, int b, unsigned epoch, int lane) 
     if (!bonus && !merge_row<GREEDY>(P, target_row_id(b, gam, G), -1, c, false, epoch, lane, rt)) failed = true;
     else if (!row_ok(rt.st, GREEDY)) st = SPEC_ST_NONFINITE;
   }
-  // the draw rounds are started before the remaining signal rows are merged
+  // the draw is started as soon as k is known, and finished before the
+  // remaining signal rows are merged (they are read last)
   const bool draw = !GREEDY && P.mode != MODE_SIGNALS && !failed && st == 0;
   int kind = DK_P, excl = -1;
   float ud = 0.f;
@@ -1754,6 +1813,22 @@ __device__ void serve_request(const Params& P, int b, unsigned epoch, int lane) 
       start_draw(P, b, kind, k, excl, rt.st, rd.st, c, 0, epoch, lane);
     }
   }
+  if (draw && st == 0 && !failed) {
+    int r = draw_round<DT>(P, b, kind, k, excl, rt.st, rd.st, c, ud, draw_tag(epoch, 0), lane, &z);
+    if (r == DR_ZERO && (kind == DK_RESID || excl >= 0)) {
+      // residual mass rounded to zero: draw from p_k itself
+      st |= SPEC_ST_ZERO_RESIDUAL;
+      kind = DK_P;
+      excl = -1;
+      start_draw(P, b, kind, k, excl, rt.st, rd.st, c, 1, epoch, lane);
+      r = draw_round<DT>(P, b, kind, k, excl, rt.st, rd.st, c, ud, draw_tag(epoch, 1), lane, &z);
+    }
+    if (r != DR_OK) {
+      failed = true;
+      z = -1;
+    }
+  }
+  // the signal rows not merged yet (read last, after the main queue)
   if (sig && !failed) {
     for (int i = ndraft; i < gam;) {
       if (P.nch <= 8) {            // up to four draft rows per pass: the first waited for
@@ -1772,21 +1847,6 @@ __device__ void serve_request(const Params& P, int b, unsigned epoch, int lane) 
         take_draft(i, D);
         ++i;
       }
-    }
-  }
-  if (draw && st == 0 && !failed) {
-    int r = draw_round<DT>(P, b, kind, k, excl, rt.st, rd.st, c, ud, draw_tag(epoch, 0), lane, &z);
-    if (r == DR_ZERO && (kind == DK_RESID || excl >= 0)) {
-      // residual mass rounded to zero: draw from p_k itself
-      st |= SPEC_ST_ZERO_RESIDUAL;
-      kind = DK_P;
-      excl = -1;
-      start_draw(P, b, kind, k, excl, rt.st, rd.st, c, 1, epoch, lane);
-      r = draw_round<DT>(P, b, kind, k, excl, rt.st, rd.st, c, ud, draw_tag(epoch, 1), lane, &z);
-    }
-    if (r != DR_OK) {
-      failed = true;
-      z = -1;
     }
   }
   if (GREEDY && !failed && st == 0) z = rt.st.idx & ~kIdxNaN;
