@@ -1,41 +1,39 @@
 // verify.cu -- the two kernels of one verification call.
 //
-// plan_kernel (1 CTA): resets the workspace counters, settles the requests
-// whose inputs are invalid up front, and writes the position-major row
-// schedule.
+// plan_kernel (1 CTA): sets the call's epoch, resets the counters, settles
+// the requests whose inputs are invalid up front, and writes the
+// position-major row schedule.
 //
-// verify_kernel: a persistent, warp-specialised kernel (2 CTAs per SM) that
-// takes a request from its logits to its committed tokens.  Work items come
-// from two queues: the static schedule of 64 KB chunks of logit rows, and a
-// device-side queue of items created on the fly (drained first):
+// verify_kernel: a persistent, warp-specialised kernel (every CTA resident,
+// 2 per SM) that takes a request from its logits to its committed tokens.
+// Work items come from three queues: the static schedule of 64 KB chunks of
+// logit rows, the deferred queue (draft rows needed for the signals only,
+// read after the static queue), and the draw queue created on the fly:
 //   IT_STATS   softmax statistics of one chunk of a row (max m, s = sum
 //              2^{(x-m)c}, for signal rows t = sum (x-m)c 2^{(x-m)c}, greedy
 //              rows the max and its lowest index);
 //   IT_DSUM    the weights of the final draw over one 16 KB slice of row k:
 //              the residual [p_k - q_k]_+ (reject, full q: rows k of both
 //              models) or p_k (bonus draw; one-hot reject with y_k removed);
-//              fp32 sums per 64-token group are kept, their fp64 total is
-//              the slice sum.  The CTA completing the last slice locates the
-//              slice, the group and the token (tutorial page, sections 3.2,
-//              3.3 and 5.2).
+//              fp32 sums per 256-token group and the fp64 slice sum are kept
+//              (tutorial page "5.1 投机解码核心原理", sections 3.2, 3.3, 5.2).
 // Roles inside a CTA:
-//   producer warp   claims items (dynamic queue first), skips rows that an
-//                   earlier reject has voided, stages the bytes into a 6-deep
-//                   ring of 16 KB shared-memory buffers with cp.async.bulk
-//                   completed on mbarriers;
+//   producer (1 thread)  claims items, skips rows an earlier reject voided
+//                   (defers signal-only draft rows), stages the bytes into a
+//                   6-deep ring of 16 KB shared-memory buffers with
+//                   cp.async.bulk completed on mbarriers;
 //   8 consumer warps  read the staged bytes with 128-bit shared loads and do
 //                   the arithmetic of the item;
-//   2 epilogue warps  publish per-item partials; the CTA that completes a row
-//                   merges its chunks (fixed order, so results do not depend
-//                   on scheduling), evaluates the acceptance test of the
-//                   position (tutorial page "5.1 投机解码核心原理", sections
-//                   3.1-3.3), and tracks per request when its first reject k
-//                   (section 5.1) and its signal rows are known; then it
-//                   settles the request or creates its draw items.
-// Rows of a request after a decided reject are skipped (early exit).  Draw
-// items run right after the decision, while rows k are still in L2.
-// Every spin is bounded in time; a wait that gives up sets SPEC_ST_TIMEOUT,
-// and the last CTA to leave voids any request left unfinished.
+//   2 epilogue warps  merge each chunk's 8 warp partials and publish them as
+//                   tagged words (see tword);
+//   owner warp      serves requests b = CTA, CTA + grid, ...: merges their
+//                   rows from the tagged partials in fixed order, tests the
+//                   positions in order (sections 3.1-3.3, 5.1), publishes the
+//                   first reject (early exit), runs the draw and writes the
+//                   outputs.  Every decision of a request is taken in one warp.
+// Every spin is bounded; a wait that gives up sets SPEC_ST_TIMEOUT, the other
+// roles then give up too, and the last CTA to leave voids any request left
+// unfinished.
 #include <climits>
 
 #include "common.cuh"
