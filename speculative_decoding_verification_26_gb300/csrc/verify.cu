@@ -353,6 +353,7 @@ __device__ __forceinline__ void run_reset(RunState& r) {
 // their exp2 and adds pipeline.  Vectors past the staged bytes read as -inf.
 
 constexpr int kVecPerThread = kStageBytes / 16 / kConsumerThreads;   // 4
+static_assert(kVecPerThread == 4, "the draw's group sums take four vectors per thread");
 
 __device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {       // NaN-ignoring
   uint32_t d;
@@ -966,16 +967,40 @@ __device__ void fill_direct(const Params& P, VSmem& S, int stage, const StageDes
   consumer_bar();
 }
 
-// residual weight [p - q]_+ of one element pair (the same expression
-// everywhere, so sums and the search agree term by term)
+// Residual weight [p - q]_+ of one element pair, p = 2^{x_p c - m_p c} / s_p
+// and q likewise: one rounding order everywhere (the scalar form and the
+// packed pair form give the same bits), so the slice and group sums and
+// the token search agree term by term.
 struct ResidW {
-  float c, mpc, mqc, rp, rq;
+  float c, mpc, mqc, rp, nrq;       // nrq = -1 / s_q
   __device__ __forceinline__ float operator()(float xp, float xq) const {
-    const float p = ex2(fmaf(xp, c, -mpc)) * rp;
-    const float q = ex2(fmaf(xq, c, -mqc)) * rq;
-    return fmaxf(p - q, 0.f);
+    const float p = ex2(fmaf(xp, c, -mpc));
+    const float q = ex2(fmaf(xq, c, -mqc));
+    return fmaxf(fmaf(p, rp, __fmul_rn(q, nrq)), 0.f);
+  }
+  __device__ __forceinline__ float2 pair(float2 xp, float2 xq) const {
+    const float2 a = __ffma2_rn(xp, make_float2(c, c), make_float2(-mpc, -mpc));
+    const float2 b = __ffma2_rn(xq, make_float2(c, c), make_float2(-mqc, -mqc));
+    const float2 p = make_float2(ex2(a.x), ex2(a.y));
+    const float2 q = make_float2(ex2(b.x), ex2(b.y));
+    const float2 d = __ffma2_rn(p, make_float2(rp, rp), __fmul2_rn(q, make_float2(nrq, nrq)));
+    return make_float2(fmaxf(d.x, 0.f), fmaxf(d.y, 0.f));
   }
 };
+
+// Four sums over the warp's 32 lanes in six shuffles (the values are halved
+// across lanes at the first two steps): lane l ends with the total of
+// v[(l >> 3) & 3].
+__device__ __forceinline__ float warp_sum4(const float (&v)[4], int lane) {
+  const bool h16 = (lane & 16) != 0, h8 = (lane & 8) != 0;
+  const float k0 = (h16 ? v[2] : v[0]) + __shfl_xor_sync(0xffffffffu, h16 ? v[0] : v[2], 16);
+  const float k1 = (h16 ? v[3] : v[1]) + __shfl_xor_sync(0xffffffffu, h16 ? v[1] : v[3], 16);
+  float k = (h8 ? k1 : k0) + __shfl_xor_sync(0xffffffffu, h8 ? k0 : k1, 8);
+  k += __shfl_xor_sync(0xffffffffu, k, 4);
+  k += __shfl_xor_sync(0xffffffffu, k, 2);
+  k += __shfl_xor_sync(0xffffffffu, k, 1);
+  return k;
+}
 
 template <int DT, bool GREEDY>
 __device__ void consumer_role(const Params& P, VSmem& S, int cw, int lane) {
@@ -1094,13 +1119,13 @@ __device__ void consumer_role(const Params& P, VSmem& S, int cw, int lane) {
     load_stage<DT>(vec, d.nvec, tid, wt);
     if (resid) load_stage<DT>(vec2, d.nvec, tid, wd);
     ResidW R;
-    R.c = it.c; R.mpc = it.m1 * it.c; R.mqc = it.m2 * it.c; R.rp = 1.f / it.s1; R.rq = 1.f / it.s2;
+    R.c = it.c; R.mpc = it.m1 * it.c; R.mqc = it.m2 * it.c; R.rp = 1.f / it.s1; R.nrq = -1.f / it.s2;
     const float mc = it.m1 * it.c;
     const float cd = it.c;
     const int excl = it.y;
     const unsigned dtag = it.tag;
     tword* gs_out = P.gsum + ((size_t)it.b * P.nres + it.chunk) * kGroupsPerStage;
-    double dsum = 0.0;                  // lane 0: this warp's groups, in q order
+    float gq[kVecPerThread];            // the lane's vector sums
 #pragma unroll
     for (int q = 0; q < kVecPerThread; ++q) {
       const int v = tid + q * kConsumerThreads;
@@ -1110,10 +1135,16 @@ __device__ void consumer_role(const Params& P, VSmem& S, int cw, int lane) {
         float xd[N];
         VecT<DT>::unpack(wd[q], xd);
 #pragma unroll
-        for (int k = 0; k < N; ++k) e[k] = R(xt[k], xd[k]);
+        for (int k = 0; k < N; k += 2) {
+          const float2 w2 = R.pair(make_float2(xt[k], xt[k + 1]), make_float2(xd[k], xd[k + 1]));
+          e[k] = w2.x; e[k + 1] = w2.y;
+        }
       } else {
 #pragma unroll
-        for (int k = 0; k < N; ++k) e[k] = ex2(fmaf(xt[k], cd, -mc));
+        for (int k = 0; k < N; k += 2) {
+          const float2 a = __ffma2_rn(make_float2(xt[k], xt[k + 1]), make_float2(cd, cd), make_float2(-mc, -mc));
+          e[k] = ex2(a.x); e[k + 1] = ex2(a.y);
+        }
         if (excl >= 0) {
           const int off = excl - (d.elem0 + v * N);
           if (off >= 0 && off < N)
@@ -1122,17 +1153,23 @@ __device__ void consumer_role(const Params& P, VSmem& S, int cw, int lane) {
               if (k == off) e[k] = 0.f;
         }
       }
-      float g;
-      if (N == 8) g = ((e[0] + e[1]) + (e[2] + e[3])) + ((e[4] + e[5]) + (e[6] + e[7]));
-      else g = (e[0] + e[1]) + (e[2] + e[3]);
-      // the vectors 32 cw + 256 q + lane of one warp form group cw + 8 q
+      if (N == 8) gq[q] = ((e[0] + e[1]) + (e[2] + e[3])) + ((e[4] + e[5]) + (e[6] + e[7]));
+      else gq[q] = (e[0] + e[1]) + (e[2] + e[3]);
+    }
+    // the vectors 32 cw + 256 q + lane of one warp form group cw + 8 q; lane
+    // 8 q ends with its sum and publishes it
+    const float gsum = warp_sum4(gq, lane);
+    if ((lane & 7) == 0 && (cw + (lane >> 3) * 8) * kGroupVecs < d.nvec)
+      st_tw(gs_out + cw + (lane >> 3) * 8, tw_make(__float_as_uint(gsum), dtag));
+    double dsum = 0.0;                  // lane 0: this warp's groups, in q order
+    {
+      const float g1 = __shfl_sync(0xffffffffu, gsum, 8), g2 = __shfl_sync(0xffffffffu, gsum, 16),
+                  g3 = __shfl_sync(0xffffffffu, gsum, 24);
+      const float gg[kVecPerThread] = {gsum, g1, g2, g3};
+      if (lane == 0)
 #pragma unroll
-      for (int off = 16; off >= 1; off >>= 1) g += __shfl_xor_sync(0xffffffffu, g, off);
-      const int gi = v / kGroupVecs;
-      if (lane == 0 && gi * kGroupVecs < d.nvec) {
-        st_tw(gs_out + gi, tw_make(__float_as_uint(g), dtag));
-        dsum += (double)g;
-      }
+        for (int q = 0; q < kVecPerThread; ++q)
+          if ((cw + 8 * q) * kGroupVecs < d.nvec) dsum += (double)gg[q];
     }
     release(st1);
     if (resid) release(stage);
@@ -1177,13 +1214,31 @@ __device__ void epilogue_role(const Params& P, VSmem& S, int lane, int e, unsign
       }
       continue;
     }
-    // IT_STATS: merge the consumer warps' partials (fixed tree), publish
-    const bool ent = !GREEDY && kind == KIND_DRAFT && P.signals_on;
-    const float c = GREEDY ? 0.f : __ldg(P.req_scale + b);
+    // IT_STATS: merge the consumer warps' partials (lanes 0..7), publish.
+    // Softmax partials: the max first, one rescale of each partial to it,
+    // then plain sums (fixed xor tree: deterministic).
+    if (GREEDY) {
 #pragma unroll
-    for (int off = 4; off >= 1; off >>= 1) {
-      const Part o = shfl_part(p, off);
-      p = GREEDY ? merge_argmax(p, o) : merge_parts(p, o, c, ent);
+      for (int off = 4; off >= 1; off >>= 1) p = merge_argmax(p, shfl_part(p, off));
+    } else {
+      const bool ent = kind == KIND_DRAFT && P.signals_on;
+      const float c = __ldg(P.req_scale + b);
+      float m = p.m;
+#pragma unroll
+      for (int off = 4; off >= 1; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+      float ss = 0.f, tt = 0.f;
+      if (p.s != 0.f) {            // an empty partial contributes 0
+        const float dd = (p.m - m) * c;
+        const float f = ex2(dd);
+        ss = p.s * f;
+        if (ent) tt = f * fmaf(dd, p.s, p.t);
+      }
+#pragma unroll
+      for (int off = 4; off >= 1; off >>= 1) {
+        ss += __shfl_xor_sync(0xffffffffu, ss, off);
+        if (ent) tt += __shfl_xor_sync(0xffffffffu, tt, off);
+      }
+      p.m = m; p.s = ss; p.t = tt;
     }
     if (lane == 0) {
       tword* o = P.cparts + ((size_t)rid * nch + chunk) * kPartWords;
@@ -1529,11 +1584,16 @@ __device__ int draw_round(const Params& P, int b, int kind, int k, int excl, con
   // 0. every slice summed
   OwnerClock clk;
   clk.start();
+  tword wa = 0ull, wb = 0ull;     // lane j: the two words of slice j, as polled (nres <= 32)
   for (int j0 = 0; j0 < nres; j0 += 32) {
     const int j = j0 + lane;
     while (true) {
       bool ok = true;
-      if (j < nres) ok = tw_ok(ld_tw(sums + 2 * j), tag) && tw_ok(ld_tw(sums + 2 * j + 1), tag);
+      if (j < nres) {
+        wa = ld_tw(sums + 2 * j);
+        wb = ld_tw(sums + 2 * j + 1);
+        ok = tw_ok(wa, tag) && tw_ok(wb, tag);
+      }
       if (__all_sync(0xffffffffu, ok)) break;
       if (clk.expired(P)) return DR_FAIL;
     }
@@ -1542,7 +1602,8 @@ __device__ int draw_round(const Params& P, int b, int kind, int k, int excl, con
   double W, before;
   int cs;
   if (nres <= 32) {
-    const double v = lane < nres ? slice_sum(sums, lane) : 0.0;
+    const double v =
+        lane < nres ? __longlong_as_double((long long)(((unsigned long long)tw_u32(wa) << 32) | tw_u32(wb))) : 0.0;
     const double incl = warp_incl_scan(v, lane);
     W = __shfl_sync(0xffffffffu, incl, 31);
     const double t = (double)ud * W;
@@ -1583,27 +1644,40 @@ __device__ int draw_round(const Params& P, int b, int kind, int k, int excl, con
   const int g = gcross ? __ffs(gcross) - 1 : (gpos ? 31 - __clz(gpos) : 0);
   const double gbefore = __shfl_sync(0xffffffffu, gincl - lsum, g);
   const double tl2 = tl - gbefore;
-  // 3. the token: lane l takes PER consecutive tokens of the group
+  // 3. the token: lane l takes the PER consecutive tokens of vector l of the
+  // group (one 16-byte load per row when the rows are 16-byte aligned)
   ResidW R;
-  R.c = c; R.mpc = tr.m * c; R.mqc = dr.m * c; R.rp = 1.f / tr.s; R.rq = 1.f / dr.s;
+  R.c = c; R.mpc = tr.m * c; R.mqc = dr.m * c; R.rp = 1.f / tr.s; R.nrq = -1.f / dr.s;
   const float mc = tr.m * c;
   const long long trow = row_elem_offset(KIND_TARGET, b, k, G, V);
   const long long drow = resid ? row_elem_offset(KIND_DRAFT, b, k, G, V) : 0;
   float w[PER];
   const int g0 = e0 + g * GE;
+  const int t0 = g0 + lane * PER;
+  if (P.aligned_rows && t0 + PER <= e1) {
+    constexpr int ES = DT == SPEC_BF16 ? 2 : 4;
+    float xt[PER], xd[PER];
+    VecT<DT>::unpack(__ldg(reinterpret_cast<const uint4*>(P.target + (size_t)(trow + t0) * ES)), xt);
+    if (resid) VecT<DT>::unpack(__ldg(reinterpret_cast<const uint4*>(P.draft + (size_t)(drow + t0) * ES)), xd);
+#pragma unroll
+    for (int u = 0; u < PER; ++u)
+      w[u] = resid ? R(xt[u], xd[u]) : (t0 + u == excl ? 0.f : ex2(fmaf(xt[u], c, -mc)));
+  } else {
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {
+      const int e = t0 + u;
+      float wu = 0.f;
+      if (e < e1) {
+        const float xt = load_logit(P.target, DT, trow + e);
+        if (resid) wu = R(xt, load_logit(P.draft, DT, drow + e));
+        else wu = e == excl ? 0.f : ex2(fmaf(xt, c, -mc));
+      }
+      w[u] = wu;
+    }
+  }
   double mine = 0.0;
 #pragma unroll
-  for (int u = 0; u < PER; ++u) {
-    const int e = g0 + lane * PER + u;
-    float wu = 0.f;
-    if (e < e1) {
-      const float xt = load_logit(P.target, DT, trow + e);
-      if (resid) wu = R(xt, load_logit(P.draft, DT, drow + e));
-      else wu = e == excl ? 0.f : ex2(fmaf(xt, c, -mc));
-    }
-    w[u] = wu;
-    mine += (double)wu;
-  }
+  for (int u = 0; u < PER; ++u) mine += (double)w[u];
   const double incl = warp_incl_scan(mine, lane);
   const double ex = incl - mine;
   const unsigned cross = __ballot_sync(0xffffffffu, incl > tl2);
