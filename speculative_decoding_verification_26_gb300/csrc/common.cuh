@@ -51,7 +51,7 @@ constexpr int kChunkBytes = 4 * kStageBytes;            // one work item of a ro
 constexpr int kEpiSlots = 12;                           // consumer -> epilogue ring (multiple of kEpiWarps)
 constexpr int kGroupVecs = 32;                          // draw group: one warp's 32 vectors (256 bf16 / 128 fp32 tokens)
 constexpr int kGroupsPerStage = kStageBytes / 16 / kGroupVecs;   // 32
-constexpr int kPartWords = 5;                           // tagged words of a chunk partial: m, s, t, idx, x_y
+constexpr int kPartWords = 3;                           // tagged words of a chunk partial: m, s (argmax: idx), t
 constexpr int kDrawWords = 8;                           // tagged words of a draw descriptor
 constexpr int kNoReject = 0x7fffffff;
 constexpr unsigned kEpochMax = 0x3ffffff0u;             // tags are 4 * epoch + kind (kind < 4)

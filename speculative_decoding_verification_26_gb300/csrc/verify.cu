@@ -270,9 +270,8 @@ struct StageDesc {
 struct EpiSlot {
   int type, row_id, b, i;
   int kind, chunk, term, z;
-  float xy;
   unsigned tag;                     // draw: tag of the draw's words
-  int pad[2];
+  int pad[3];
   double dsum[kConsumerWarps];      // draw-weight sums per consumer warp (IT_DSUM)
   Part part[kConsumerWarps];        // statistics per consumer warp (IT_STATS)
 };
@@ -1012,8 +1011,7 @@ __device__ void consumer_role(const Params& P, VSmem& S, int cw, int lane) {
   RunState r;
   run_reset(r);
   bool ent = false;
-  float c = 0.f, xy = qnan();
-  int y = -1;                     // draft token of the current statistics item (x_y capture)
+  float c = 0.f;
   auto advance = [&]() {
     if (++stage == kStages) { stage = 0; phase ^= 1u; }
   };
@@ -1051,18 +1049,9 @@ __device__ void consumer_role(const Params& P, VSmem& S, int cw, int lane) {
         run_reset(r);
         ent = !GREEDY && it.kind == KIND_DRAFT && P.signals_on;
         c = it.c;
-        y = it.y;
-        xy = qnan();
       }
       uint4 w[kVecPerThread];
       load_stage<DT>(vec, d.nvec, tid, w);
-      // the logit at the draft token, if this stage holds it (one shared load)
-      if (!GREEDY && tid == 0) {
-        const int off = y - d.elem0;
-        if (off >= 0 && off < d.nvec * N)
-          xy = DT == SPEC_BF16 ? __uint_as_float((uint32_t)reinterpret_cast<const unsigned short*>(vec)[off] << 16)
-                               : reinterpret_cast<const float*>(vec)[off];
-      }
       if (GREEDY) stage_argmax<DT>(r, w, d.elem0, tid);
       else if (ent) stage_softmax<DT, true>(r, w, c);
       else stage_softmax<DT, false>(r, w, c);
@@ -1073,14 +1062,10 @@ __device__ void consumer_role(const Params& P, VSmem& S, int cw, int lane) {
           const unsigned char* tens = it.kind == KIND_TARGET ? P.target : P.draft;
           const long long row0 = row_elem_offset(it.kind, it.b, it.i, P.G, P.V);
           for (int k = 0; k < it.nhead; ++k) {
-            const float x = load_logit(tens, DT, row0 + it.head0 + k);
-            if (it.head0 + k == y) xy = x;
-            run_scalar<GREEDY>(r, x, it.head0 + k, c, ent);
+            run_scalar<GREEDY>(r, load_logit(tens, DT, row0 + it.head0 + k), it.head0 + k, c, ent);
           }
           for (int k = 0; k < it.ntail; ++k) {
-            const float x = load_logit(tens, DT, row0 + it.tail0 + k);
-            if (it.tail0 + k == y) xy = x;
-            run_scalar<GREEDY>(r, x, it.tail0 + k, c, ent);
+            run_scalar<GREEDY>(r, load_logit(tens, DT, row0 + it.tail0 + k), it.tail0 + k, c, ent);
           }
         }
         Part p;
@@ -1095,7 +1080,7 @@ __device__ void consumer_role(const Params& P, VSmem& S, int cw, int lane) {
               if (lane == 0) E.part[cw] = p;
               if (tid == 0) {
                 E.type = IT_STATS; E.row_id = it.row_id; E.b = it.b; E.i = it.i; E.kind = it.kind;
-                E.chunk = it.chunk; E.xy = xy;
+                E.chunk = it.chunk;
               }
             }))
           return;
@@ -1195,7 +1180,6 @@ __device__ void epilogue_role(const Params& P, VSmem& S, int lane, int e, unsign
     const EpiSlot& E = S.slot[eslot];
     if (E.term) return;
     const int type = E.type, rid = E.row_id, b = E.b, kind = E.kind, chunk = E.chunk;
-    const float xy = E.xy;
     const unsigned dtag = E.tag;
     Part p = lane < kConsumerWarps ? E.part[lane] : empty_part();
     double ws = 0.0;
@@ -1244,10 +1228,8 @@ __device__ void epilogue_role(const Params& P, VSmem& S, int lane, int e, unsign
       tword* o = P.cparts + ((size_t)rid * nch + chunk) * kPartWords;
       const unsigned ptag = part_tag(epoch);
       st_tw(o + 0, tw_make(__float_as_uint(p.m), ptag));
-      st_tw(o + 1, tw_make(__float_as_uint(p.s), ptag));
-      st_tw(o + 2, tw_make(__float_as_uint(p.t), ptag));
-      st_tw(o + 3, tw_make((unsigned)p.idx, ptag));
-      st_tw(o + 4, tw_make(__float_as_uint(xy), ptag));
+      st_tw(o + 1, tw_make(GREEDY ? (unsigned)p.idx : __float_as_uint(p.s), ptag));
+      if (!GREEDY) st_tw(o + 2, tw_make(__float_as_uint(p.t), ptag));
     }
   }
 }
@@ -1280,30 +1262,47 @@ struct OwnerClock {
 
 struct RowRes {
   RowStats st;   // merged statistics (every lane)
-  float xy;      // logit at the requested element (NaN if not requested)
+  float xy;      // logit at the draft token (NaN if not loaded)
 };
 
-// Merged statistics of row rid (warp-wide).  Waits until every chunk
-// partial carries the call's tag, merges them in chunk order (lane l takes
-// chunks l, l+32, ...; then a fixed xor tree) and takes x_y from the chunk
-// that holds element y (y < 0: none).  False if the wait gave up.
+// Tagged words of a chunk partial that carry data, and the partial they hold.
 template <bool GREEDY>
-__device__ bool merge_row(const Params& P, int rid, int y, float c, bool ent, unsigned epoch, int lane, RowRes& out) {
+constexpr int part_words() { return GREEDY ? 2 : 3; }
+template <bool GREEDY>
+__device__ __forceinline__ Part part_of(const tword (&w)[kPartWords]) {
+  Part q;
+  q.m = tw_f32(w[0]);
+  if (GREEDY) {
+    q.idx = (int)tw_u32(w[1]);
+    q.s = q.t = 0.f;
+  } else {
+    q.s = tw_f32(w[1]);
+    q.t = tw_f32(w[2]);
+    q.idx = 0x3fffffff;
+  }
+  return q;
+}
+
+// Merged statistics of row rid (warp-wide).  Waits until every chunk
+// partial carries the call's tag and merges them in chunk order (lane l
+// takes chunks l, l+32, ...; then a fixed xor tree).  False if the wait gave
+// up.
+template <bool GREEDY>
+__device__ bool merge_row(const Params& P, int rid, float c, bool ent, unsigned epoch, int lane, RowRes& out) {
+  constexpr int NW = part_words<GREEDY>();
   const int nch = P.nch;
   const tword* base = P.cparts + (size_t)rid * nch * kPartWords;
-  const int ychunk = y >= 0 ? y / chunk_elems(P.dtype) : -1;
   Part r = empty_part();
-  float xy = qnan();
   OwnerClock clk;
   clk.start();
   for (int k0 = 0; k0 < nch; k0 += 32) {
     const int k = k0 + lane;
-    tword w[kPartWords];
+    tword w[kPartWords] = {};
     while (true) {
       bool ok = true;
       if (k < nch) {
 #pragma unroll
-        for (int j = 0; j < kPartWords; ++j) {
+        for (int j = 0; j < NW; ++j) {
           w[j] = ld_tw(base + (size_t)k * kPartWords + j);
           ok &= tw_ok(w[j], part_tag(epoch));
         }
@@ -1311,12 +1310,7 @@ __device__ bool merge_row(const Params& P, int rid, int y, float c, bool ent, un
       if (__all_sync(0xffffffffu, ok)) break;
       if (clk.expired(P)) return false;
     }
-    if (k < nch) {
-      Part q;
-      q.m = tw_f32(w[0]); q.s = tw_f32(w[1]); q.t = tw_f32(w[2]); q.idx = (int)tw_u32(w[3]);
-      r = GREEDY ? merge_argmax(r, q) : merge_parts(r, q, c, ent);
-      if (k == ychunk) xy = tw_f32(w[4]);
-    }
+    if (k < nch) r = GREEDY ? merge_argmax(r, part_of<GREEDY>(w)) : merge_parts(r, part_of<GREEDY>(w), c, ent);
   }
 #pragma unroll
   for (int off = 16; off >= 1; off >>= 1) {
@@ -1324,7 +1318,7 @@ __device__ bool merge_row(const Params& P, int rid, int y, float c, bool ent, un
     r = GREEDY ? merge_argmax(r, o) : merge_parts(r, o, c, ent);
   }
   out.st.m = r.m; out.st.s = r.s; out.st.t = r.t; out.st.idx = r.idx;
-  out.xy = (ychunk >= 0 && ychunk < nch) ? __shfl_sync(0xffffffffu, xy, ychunk & 31) : qnan();
+  out.xy = qnan();
   return true;
 }
 
@@ -1334,21 +1328,20 @@ __device__ bool merge_row(const Params& P, int rid, int y, float c, bool ent, un
 // with the same tree as merge_row (its xor-16 level only meets empty
 // partials, which merge exactly), so the results are identical to two
 // merge_row calls.  False if the wait gave up.
-__device__ bool merge_pair(const Params& P, int ridT, int ridD, int y, float c, bool entD, unsigned epoch, int lane,
+__device__ bool merge_pair(const Params& P, int ridT, int ridD, float c, bool entD, unsigned epoch, int lane,
                            RowRes& T, RowRes& D) {
   const int nch = P.nch;
   const int half = lane >> 4, k = lane & 15;
   const tword* base = P.cparts + (size_t)(half ? ridD : ridT) * nch * kPartWords;
   const bool ent = half ? entD : false;
-  const int ychunk = y >= 0 ? y / chunk_elems(P.dtype) : -1;
-  tword w[kPartWords];
+  tword w[kPartWords] = {};
   OwnerClock clk;
   clk.start();
   while (true) {
     bool ok = true;
     if (k < nch) {
 #pragma unroll
-      for (int j = 0; j < kPartWords; ++j) {
+      for (int j = 0; j < part_words<false>(); ++j) {
         w[j] = ld_tw(base + (size_t)k * kPartWords + j);
         ok &= tw_ok(w[j], part_tag(epoch));
       }
@@ -1357,41 +1350,34 @@ __device__ bool merge_pair(const Params& P, int ridT, int ridD, int y, float c, 
     if (clk.expired(P)) return false;
   }
   Part r = empty_part();
-  float xy = qnan();
-  if (k < nch) {
-    Part q;
-    q.m = tw_f32(w[0]); q.s = tw_f32(w[1]); q.t = tw_f32(w[2]); q.idx = (int)tw_u32(w[3]);
-    r = merge_parts(r, q, c, ent);
-    if (k == ychunk) xy = tw_f32(w[4]);
-  }
+  if (k < nch) r = merge_parts(r, part_of<false>(w), c, ent);
 #pragma unroll
   for (int off = 8; off >= 1; off >>= 1) r = merge_parts(r, shfl_part(r, off), c, ent);
   T.st.m = __shfl_sync(0xffffffffu, r.m, 0);  T.st.s = __shfl_sync(0xffffffffu, r.s, 0);
   T.st.t = __shfl_sync(0xffffffffu, r.t, 0);  T.st.idx = __shfl_sync(0xffffffffu, r.idx, 0);
   D.st.m = __shfl_sync(0xffffffffu, r.m, 16); D.st.s = __shfl_sync(0xffffffffu, r.s, 16);
   D.st.t = __shfl_sync(0xffffffffu, r.t, 16); D.st.idx = __shfl_sync(0xffffffffu, r.idx, 16);
-  const bool yin = ychunk >= 0 && ychunk < nch;
-  T.xy = yin ? __shfl_sync(0xffffffffu, xy, ychunk) : qnan();
-  D.xy = yin ? __shfl_sync(0xffffffffu, xy, 16 + ychunk) : qnan();
+  T.xy = D.xy = qnan();
   return true;
 }
 
 // Up to four rows at once (warp-wide; needs nch <= 8): row s in lanes
-// 8s .. 8s+7, given per lane by its segment's row id (< 0: no row), draft
-// token and entropy flag.  Segments in need_mask are waited for; the others
-// are taken only if already complete.  Each row merges with the same tree as
+// 8s .. 8s+7, given per lane by its segment's row id (< 0: no row) and
+// entropy flag.  Segments in need_mask are waited for; the others are taken
+// only if already complete.  Each row merges with the same tree as
 // merge_row (its xor-16 and xor-8 levels only meet empty partials, which
 // merge exactly), so results are identical.  Every lane of segment s ends
-// with row s's statistics in pm and its x_y in xy.  Returns the mask of the
-// segments taken (absent rows count as taken), or -1 if the wait gave up.
+// with row s's statistics in pm.  Returns the mask of the segments taken
+// (absent rows count as taken), or -1 if the wait gave up.
 template <bool GREEDY>
-__device__ int merge_rows4(const Params& P, int rid, int y, bool ent, unsigned need_mask, float c, unsigned epoch,
-                           int lane, Part& pm, float& xy) {
+__device__ int merge_rows4(const Params& P, int rid, bool ent, unsigned need_mask, float c, unsigned epoch, int lane,
+                           Part& pm) {
+  constexpr int NW = part_words<GREEDY>();
   const int nch = P.nch;
   const int seg = lane >> 3, k = lane & 7;
   const bool has = rid >= 0 && k < nch;
   const tword* base = P.cparts + ((size_t)(rid < 0 ? 0 : rid) * nch + k) * kPartWords;
-  tword w[kPartWords];
+  tword w[kPartWords] = {};
   unsigned ready = 0;
   OwnerClock clk;
   clk.start();
@@ -1399,7 +1385,7 @@ __device__ int merge_rows4(const Params& P, int rid, int y, bool ent, unsigned n
     bool ok = true;
     if (has) {
 #pragma unroll
-      for (int j = 0; j < kPartWords; ++j) {
+      for (int j = 0; j < NW; ++j) {
         w[j] = ld_tw(base + j);
         ok &= tw_ok(w[j], part_tag(epoch));
       }
@@ -1414,34 +1400,24 @@ __device__ int merge_rows4(const Params& P, int rid, int y, bool ent, unsigned n
   }
   const bool take = has && ((ready >> seg) & 1u);
   Part r = empty_part();
-  float x = qnan();
-  if (take) {
-    Part q;
-    q.m = tw_f32(w[0]); q.s = tw_f32(w[1]); q.t = tw_f32(w[2]); q.idx = (int)tw_u32(w[3]);
-    r = GREEDY ? merge_argmax(r, q) : merge_parts(r, q, c, ent);
-    x = tw_f32(w[4]);
-  }
+  if (take) r = GREEDY ? merge_argmax(r, part_of<GREEDY>(w)) : merge_parts(r, part_of<GREEDY>(w), c, ent);
 #pragma unroll
   for (int off = 4; off >= 1; off >>= 1) {
     const Part o = shfl_part(r, off);
     r = GREEDY ? merge_argmax(r, o) : merge_parts(r, o, c, ent);
   }
   pm = r;
-  const int ychunk = y >= 0 ? y / chunk_elems(P.dtype) : -1;
-  const bool yin = ychunk >= 0 && ychunk < nch;
-  const float xs = __shfl_sync(0xffffffffu, x, (seg << 3) | (yin ? ychunk : 0));
-  xy = yin ? xs : qnan();
   return (int)ready;
 }
 
-// Row s of a merge_rows4 result, as every lane sees it.
-__device__ __forceinline__ RowRes row_of(const Part& pm, float xy, int s) {
+// Row s of a merge_rows4 result, as every lane sees it (x_y not loaded).
+__device__ __forceinline__ RowRes row_of(const Part& pm, int s) {
   RowRes o;
   o.st.m = __shfl_sync(0xffffffffu, pm.m, 8 * s);
   o.st.s = __shfl_sync(0xffffffffu, pm.s, 8 * s);
   o.st.t = __shfl_sync(0xffffffffu, pm.t, 8 * s);
   o.st.idx = __shfl_sync(0xffffffffu, pm.idx, 8 * s);
-  o.xy = __shfl_sync(0xffffffffu, xy, 8 * s);
+  o.xy = qnan();
   return o;
 }
 
@@ -1814,6 +1790,12 @@ __device__ void serve_request(const Params& P, int b, unsigned epoch, int lane) 
     else st = status_of_code(code & 15);
     return false;
   };
+  // the logit of row (kind, i) at the draft token y, read by the owner
+  // (NaN when y is out of range: the position is then voided as a bad token)
+  auto logit_at = [&](int kind, int i, int y) -> float {
+    if (GREEDY || y < 0 || y >= P.V) return qnan();
+    return load_logit(kind == KIND_TARGET ? P.target : P.draft, DT, row_elem_offset(kind, b, i, G, P.V) + y);
+  };
   bool bonus = false;                         // the bonus row is merged (into rt)
   if (P.mode != MODE_SIGNALS && P.nch <= 8) {
     // position i, and position i+1 (or the bonus row) too when its rows are
@@ -1828,19 +1810,26 @@ __device__ void serve_request(const Params& P, int b, unsigned epoch, int lane) 
       else if (seg == 1) rid = sample ? draft_row_id(b, i, B, G) : -1;
       else if (seg == 2) rid = i1 <= gam ? target_row_id(b, i1, G) : -1;
       else rid = (sample && i1 < gam) ? draft_row_id(b, i1, B, G) : -1;
-      const int yl = GREEDY ? -1 : (seg < 2 ? y0 : y1);
+      // x_y of the four rows, in flight while the partials are polled
+      float xl = qnan();
+      if (lane == 0) xl = logit_at(KIND_TARGET, i, y0);
+      else if (lane == 1 && sample) xl = logit_at(KIND_DRAFT, i, y0);
+      else if (lane == 2 && i1 < gam) xl = logit_at(KIND_TARGET, i1, y1);
+      else if (lane == 3 && sample && i1 < gam) xl = logit_at(KIND_DRAFT, i1, y1);
       Part pm;
-      float xy;
-      const int ready = merge_rows4<GREEDY>(P, rid, yl, (seg & 1) && sig, 3u, c, epoch, lane, pm, xy);
+      const int ready = merge_rows4<GREEDY>(P, rid, (seg & 1) && sig, 3u, c, epoch, lane, pm);
       if (ready < 0) { failed = true; break; }
-      const RowRes T0 = row_of(pm, xy, 0), D0 = row_of(pm, xy, 1);
-      if (!decide(i, y0, T0, D0)) break;
+      auto row_xy = [&](int s2) {
+        RowRes o = row_of(pm, s2);
+        o.xy = __shfl_sync(0xffffffffu, xl, s2);
+        return o;
+      };
+      if (!decide(i, y0, row_xy(0), row_xy(1))) break;
       if (i1 < gam && (ready & 12) == 12) {
-        const RowRes T1 = row_of(pm, xy, 2), D1 = row_of(pm, xy, 3);
-        if (!decide(i1, y1, T1, D1)) break;
+        if (!decide(i1, y1, row_xy(2), row_xy(3))) break;
         i += 2;
       } else {
-        if (i1 == gam && (ready & 4)) { rt = row_of(pm, xy, 2); bonus = true; }
+        if (i1 == gam && (ready & 4)) { rt = row_of(pm, 2); bonus = true; }
         i += 1;
       }
     }
@@ -1848,26 +1837,29 @@ __device__ void serve_request(const Params& P, int b, unsigned epoch, int lane) 
     for (int i = 0; i < gam; ++i) {
       const int y = P.draft_tokens[(size_t)b * G + i];
       RowRes T, D{};
+      const float xt = logit_at(KIND_TARGET, i, y), xd = sample ? logit_at(KIND_DRAFT, i, y) : qnan();
       if (sample && 2 * P.nch <= 32) {
-        if (!merge_pair(P, target_row_id(b, i, G), draft_row_id(b, i, B, G), y, c, sig, epoch, lane, T, D)) {
+        if (!merge_pair(P, target_row_id(b, i, G), draft_row_id(b, i, B, G), c, sig, epoch, lane, T, D)) {
           failed = true;
           break;
         }
       } else {
-        if (!merge_row<GREEDY>(P, target_row_id(b, i, G), GREEDY ? -1 : y, c, false, epoch, lane, T)) {
+        if (!merge_row<GREEDY>(P, target_row_id(b, i, G), c, false, epoch, lane, T)) {
           failed = true;
           break;
         }
-        if (sample && !merge_row<false>(P, draft_row_id(b, i, B, G), y, c, sig, epoch, lane, D)) {
+        if (sample && !merge_row<false>(P, draft_row_id(b, i, B, G), c, sig, epoch, lane, D)) {
           failed = true;
           break;
         }
       }
+      T.xy = xt;
+      D.xy = xd;
       if (!decide(i, y, T, D)) break;
     }
   }
   if (P.mode != MODE_SIGNALS && !failed && st == 0 && !rejected) {   // every position accepted: the bonus row
-    if (!bonus && !merge_row<GREEDY>(P, target_row_id(b, gam, G), -1, c, false, epoch, lane, rt)) failed = true;
+    if (!bonus && !merge_row<GREEDY>(P, target_row_id(b, gam, G), c, false, epoch, lane, rt)) failed = true;
     else if (!row_ok(rt.st, GREEDY)) st = SPEC_ST_NONFINITE;
   }
   // the draw is started as soon as k is known, and finished before the
@@ -1906,16 +1898,14 @@ __device__ void serve_request(const Params& P, int b, unsigned epoch, int lane) 
       if (P.nch <= 8) {            // up to four draft rows per pass: the first waited for
         const int j = i + (lane >> 3);
         Part pm;
-        float xy;
-        const int ready = merge_rows4<false>(P, j < gam ? draft_row_id(b, j, B, G) : -1, -1, true, 1u, c, epoch,
-                                             lane, pm, xy);
+        const int ready = merge_rows4<false>(P, j < gam ? draft_row_id(b, j, B, G) : -1, true, 1u, c, epoch, lane, pm);
         if (ready < 0) { failed = true; break; }
         int s2 = 0;
-        for (; s2 < 4 && i + s2 < gam && ((ready >> s2) & 1); ++s2) take_draft(i + s2, row_of(pm, xy, s2));
+        for (; s2 < 4 && i + s2 < gam && ((ready >> s2) & 1); ++s2) take_draft(i + s2, row_of(pm, s2));
         i += s2;
       } else {
         RowRes D;
-        if (!merge_row<false>(P, draft_row_id(b, i, B, G), -1, c, true, epoch, lane, D)) { failed = true; break; }
+        if (!merge_row<false>(P, draft_row_id(b, i, B, G), c, true, epoch, lane, D)) { failed = true; break; }
         take_draft(i, D);
         ++i;
       }
