@@ -1267,7 +1267,7 @@ struct RowRes {
 
 // Tagged words of a chunk partial that carry data, and the partial they hold.
 template <bool GREEDY>
-constexpr int part_words() { return GREEDY ? 2 : 3; }
+__host__ __device__ constexpr int part_words() { return GREEDY ? 2 : 3; }
 template <bool GREEDY>
 __device__ __forceinline__ Part part_of(const tword (&w)[kPartWords]) {
   Part q;
