@@ -367,6 +367,11 @@ __device__ __forceinline__ uint32_t bmax2_nan(uint32_t a, uint32_t b) {   // NaN
 
 template <int DT>
 __device__ __forceinline__ void load_stage(const uint4* vec, int nvec, int tid, uint4 (&w)[kVecPerThread]) {
+  if (nvec == kStageBytes / 16) {     // a full stage (all but a row's last)
+#pragma unroll
+    for (int r = 0; r < kVecPerThread; ++r) w[r] = vec[tid + r * kConsumerThreads];
+    return;
+  }
   const uint32_t ninf = DT == SPEC_BF16 ? 0xff80ff80u : 0xff800000u;
 #pragma unroll
   for (int r = 0; r < kVecPerThread; ++r) {
