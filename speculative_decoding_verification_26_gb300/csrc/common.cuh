@@ -54,7 +54,12 @@ constexpr int kGroupsPerStage = kStageBytes / 16 / kGroupVecs;   // 32
 constexpr int kPartWords = 3;                           // tagged words of a chunk partial: m, s (argmax: idx), t
 constexpr int kDrawWords = 8;                           // tagged words of a draw descriptor
 constexpr int kNoReject = 0x7fffffff;
-constexpr unsigned kEpochMax = 0x3ffffff0u;             // tags are 4 * epoch + kind (kind < 4)
+constexpr unsigned kEpochMax = 0x3ffffff0u;             // tags come from 4 * epoch + kind (kind < 4)
+// Tags are (4 * epoch + kind) * kTagMul: an odd multiplier is a bijection of
+// the 32-bit integers that maps 0 to 0 only, and sends the small integers an
+// epoch starts from to values that stale data (counts, indices, tokens) does
+// not hold.
+constexpr unsigned kTagMul = 0x9E3779B1u;
 constexpr unsigned long long kWorkspaceMagic = 0x5356455246595631ull;
 // Every bounded wait counts SM clock cycles (clock64 is a register of the SM
 // and costs a few cycles to read; the global timer is read from outside the
@@ -113,16 +118,18 @@ struct Header {
 #define HDR_UNCERTAIN(h) ((h)->misc.pad[3])
 #define HDR_EPOCH(h) ((h)->misc.pad[4])
 #define HDR_MAGIC(h) (*reinterpret_cast<unsigned long long*>(&(h)->misc.pad[7]))   // byte offset 32: 8-aligned
+#define HDR_GEN(h) (*reinterpret_cast<unsigned long long*>(&(h)->misc.pad[9]))     // byte offset 40: 8-aligned
 
 // Data that crosses CTAs travels in tagged 64-bit words: payload in the high
-// 32 bits, the tag in the low 32 bits: 4 * epoch for chunk partials and
-// queue entries, 4 * epoch + 1 + round for the words of a draw round (one
-// tag space per kind of word, so that a word left by an earlier call in an
-// array laid out differently can never carry a tag of this call).  An aligned 64-bit relaxed access is
-// single-copy atomic, so a reader that sees the current tag has the payload
-// written in this call, whatever the order in which words become visible:
-// no fence and no counter is needed to publish them.  Every call has a new
-// epoch, so words left by earlier calls are never mistaken for new ones.
+// 32 bits, the tag in the low 32 bits: (4 * epoch) * kTagMul for chunk
+// partials and queue entries, (4 * epoch + 1 + round) * kTagMul for the words
+// of a draw round (one tag space per kind of word).  An aligned 64-bit
+// relaxed access is single-copy atomic, so a reader that sees the current tag
+// has the payload written in this call, whatever the order in which words
+// become visible: no fence and no counter is needed to publish them.  Every
+// call on the device has its own epoch (one counter for all workspaces), so
+// words left by earlier calls, in this workspace or in memory another
+// workspace or tensor held before, are not mistaken for new ones.
 typedef unsigned long long tword;
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -185,7 +192,7 @@ struct Params {
   float* req_scale;              // log2(e) / T_b (plan kernel)
   int* req_gam;                  // gamma_b (plan kernel)
   int* req_status;               // kFinished: settled by the plan kernel
-  unsigned* req_fin;             // epoch of the call whose outputs were written
+  unsigned* req_fin;             // tag of the call whose outputs were written
   tword* cparts;                 // [nrows][nch][kPartWords] chunk partials
   tword* dsum;                   // [B][nres][2] draw slice sums (fp64 as hi, lo)
   tword* gsum;                   // [B][nres][kGroupsPerStage] draw group sums (fp32)

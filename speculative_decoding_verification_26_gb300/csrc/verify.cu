@@ -121,6 +121,9 @@ __device__ inline void clear_tagged(const Params& P, int tid, int nth) {
   for (size_t j = tid; j < (size_t)P.def_cap; j += nth) P.defq[j] = 0ull;
 }
 
+// Calls of the plan kernel on this device so far (the source of every epoch).
+__device__ unsigned long long g_calls = 0ull;
+
 __global__ void __launch_bounds__(1024) plan_kernel(Params P) {
   griddep_launch();
   const int B = P.B, G = P.G, tid = threadIdx.x, nth = blockDim.x;
@@ -131,19 +134,23 @@ __global__ void __launch_bounds__(1024) plan_kernel(Params P) {
   __shared__ int s_nb;
   __shared__ unsigned s_settled;
   __shared__ unsigned s_epoch;
+  __shared__ unsigned long long s_gen;
   __shared__ int s_clear;
 
-  // The epoch of this call: one more than the last call's on this workspace.
-  // A workspace without the magic word (first use) or at the end of the
-  // epoch range has its tagged arrays cleared, so that no old word carries
-  // a tag this call will use (tag 0 is never used).
+  // The epoch of this call comes from one counter of calls on the device,
+  // shared by every workspace: no two calls of a generation (kEpochMax - 1
+  // calls) have the same epoch, so a word left in memory by any earlier call,
+  // in this workspace or in another one that held the same memory, never
+  // carries a tag of this call.  A workspace without the magic word (first
+  // use) or last cleared in another generation has its tagged arrays
+  // cleared (tag 0 is never used).
   if (tid == 0) {
     s_settled = 0u;
-    const bool known = HDR_MAGIC(P.hdr) == kWorkspaceMagic;
-    unsigned e = known ? HDR_EPOCH(P.hdr) + 1u : 1u;
-    s_clear = !known || e >= kEpochMax || e == 0u;
-    if (s_clear) e = 1u;
-    s_epoch = e;
+    const unsigned long long n = atomicAdd(&g_calls, 1ull);
+    const unsigned long long gen = n / (kEpochMax - 1u);
+    s_epoch = 1u + (unsigned)(n % (kEpochMax - 1u));
+    s_gen = gen;
+    s_clear = !(HDR_MAGIC(P.hdr) == kWorkspaceMagic && HDR_GEN(P.hdr) == gen);
   }
   __syncthreads();
   if (s_clear) clear_tagged(P, tid, nth);
@@ -192,6 +199,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(Params P) {
     P.hdr->queue.v = 0u;
     HDR_EPOCH(P.hdr) = s_epoch;
     HDR_MAGIC(P.hdr) = kWorkspaceMagic;
+    HDR_GEN(P.hdr) = s_gen;
     HDR_N_ITEMS(P.hdr) = (unsigned)acc * (unsigned)P.nch;
     P.hdr->error.v = 0u;
     HDR_UNCERTAIN(P.hdr) = 0u;
@@ -569,8 +577,8 @@ __device__ __forceinline__ void consumer_bar() { asm volatile("bar.sync 1, %0;" 
 // device work queue
 
 // Tags of this call's words (see tword).
-__device__ __forceinline__ unsigned draw_tag(unsigned epoch, int round) { return 4u * epoch + 1u + (unsigned)round; }
-__device__ __forceinline__ unsigned part_tag(unsigned epoch) { return 4u * epoch; }   // partials, queue entries
+__device__ __forceinline__ unsigned draw_tag(unsigned epoch, int round) { return (4u * epoch + 1u + (unsigned)round) * kTagMul; }
+__device__ __forceinline__ unsigned part_tag(unsigned epoch) { return 4u * epoch * kTagMul; }   // partials, queue entries
 
 // An entry is two tagged words: (b) and (slice | round << 30), both with the
 // call's partial tag.  The owner of request b reserves n consecutive entries
@@ -1744,7 +1752,7 @@ __device__ void owner_outputs(const Params& P, int b, int gam, int st, int k, in
   }
   __syncwarp();
   if (lane == 0) {
-    P.req_fin[b] = epoch;
+    P.req_fin[b] = part_tag(epoch);
     atomicAdd(&P.hdr->done.v, 1u);
   }
 }
@@ -1969,7 +1977,7 @@ __global__ void __launch_bounds__(kStatsThreads, 2) verify_kernel(Params P) {
     if (ex == gridDim.x && ld_relaxed_u32(&P.hdr->error.v) != 0u) {
       __threadfence();
       for (int b = 0; b < P.B; ++b)
-        if (!(__ldcg(P.req_status + b) & kFinished) && __ldcg(P.req_fin + b) != epoch)
+        if (!(__ldcg(P.req_status + b) & kFinished) && __ldcg(P.req_fin + b) != part_tag(epoch))
           write_void_outputs(P, b, SPEC_ST_TIMEOUT, 0, 1);
     }
   }

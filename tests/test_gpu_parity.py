@@ -160,6 +160,38 @@ def test_repeatable(o, dev):
         np.testing.assert_array_equal(a[k], b[k])
 
 
+def test_stale_words_in_reused_memory(o, dev):
+    """Memory a workspace takes over may hold small integers left by earlier
+    tensors or calls.  Here every word after the header is overwritten with a
+    value whose low half is 4 * (e + 1) (+ 0..3), the tag an epoch counted per
+    workspace would use on the next call, and a payload of 1 (in range as a
+    request, slice, item or chunk index, so a word taken by mistake reads no
+    memory out of bounds); the next call must not take any of them for its
+    own partials, queue entries or draw words (tags are scrambled and epochs
+    unique on the device)."""
+    import torch
+
+    import speculative_decoding_verification_26_gb300 as sv
+    wl = PT.make_workload(o, "c3", 11, B=24)
+    B, G, V = wl.B, wl.G, wl.V
+    ws = torch.empty(sv.workspace_bytes(B, G, V), dtype=torch.uint8, device=dev)
+    args = (PT.logits_dev(wl, "target", dev), PT.logits_dev(wl, "draft", dev), PT.to_dev(wl.draft_tokens, dev),
+            PT.to_dev(wl.gamma, dev), PT.to_dev(wl.temperature, dev), PT.to_dev(wl.uniforms, dev))
+    ref = PT.run_oracle(o, "sample", wl)
+    for rep in range(3):
+        sv.verify_sample(*args, signals=True, accept_prob=True, ws=ws)
+        torch.cuda.synchronize()
+        # header: 8 counters of 128 bytes; the epoch is word 5 of the last one
+        epoch = int(ws[7 * 128 + 4 * 5: 7 * 128 + 4 * 6].view(torch.int32).item())
+        words = ws[1024:(ws.numel() // 8) * 8].view(torch.int64)
+        idx = torch.arange(words.numel(), device=dev, dtype=torch.int64)
+        words.copy_((1 << 32) | (4 * (epoch + 1) + (idx % 4)))
+        r = sv.verify_sample(*args, signals=True, accept_prob=True, ws=ws)
+        torch.cuda.synchronize()
+        g = {k: v.cpu().numpy() for k, v in r.items()}
+        PT.compare(o, "sample", wl, g, ref, PT.Tally())
+
+
 def test_draft_signals_standalone(o, dev):
     import torch
 
