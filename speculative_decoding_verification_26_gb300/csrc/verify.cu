@@ -136,6 +136,11 @@ __global__ void __launch_bounds__(1024) plan_kernel(Params P) {
   __shared__ unsigned s_epoch;
   __shared__ unsigned long long s_gen;
   __shared__ int s_clear;
+  // gamma of each request whose rows are read (-1: none), for the row loops
+  // below (calls with more requests read req_flags and gamma again)
+  constexpr int kPlanB = 4096;
+  __shared__ int s_gam[kPlanB];
+  const bool small = B <= kPlanB;
 
   // The epoch of this call comes from one counter of calls on the device,
   // shared by every workspace: no two calls of a generation (kEpochMax - 1
@@ -144,16 +149,15 @@ __global__ void __launch_bounds__(1024) plan_kernel(Params P) {
   // carries a tag of this call.  A workspace without the magic word (first
   // use) or last cleared in another generation has its tagged arrays
   // cleared (tag 0 is never used).
+  // (taken while the requests are checked below)
+  unsigned long long n_calls = 0ull, hdr_magic = 0ull, hdr_gen = 0ull;
   if (tid == 0) {
     s_settled = 0u;
-    const unsigned long long n = atomicAdd(&g_calls, 1ull);
-    const unsigned long long gen = n / (kEpochMax - 1u);
-    s_epoch = 1u + (unsigned)(n % (kEpochMax - 1u));
-    s_gen = gen;
-    s_clear = !(HDR_MAGIC(P.hdr) == kWorkspaceMagic && HDR_GEN(P.hdr) == gen);
+    n_calls = atomicAdd(&g_calls, 1ull);
+    hdr_magic = HDR_MAGIC(P.hdr);
+    hdr_gen = HDR_GEN(P.hdr);
   }
-  __syncthreads();
-  if (s_clear) clear_tagged(P, tid, nth);
+  __syncthreads();   // s_settled
   for (int b = tid; b < B; b += nth) {
     P.known_reject[b] = kNoReject;
     int st = 0;
@@ -174,9 +178,22 @@ __global__ void __launch_bounds__(1024) plan_kernel(Params P) {
     } else {
       P.req_status[b] = 0;
     }
+    if (small) s_gam[b] = st == 0 ? gam : -1;
   }
-  if (tid == 0) s_nb = build_blocks(P.mode, P.signals_on, G, s_blk);
-  __syncthreads();   // req_flags and the block table visible to the whole block
+  if (tid == 0) {
+    s_nb = build_blocks(P.mode, P.signals_on, G, s_blk);
+    const unsigned long long gen = n_calls / (kEpochMax - 1u);
+    s_epoch = 1u + (unsigned)(n_calls % (kEpochMax - 1u));
+    s_gen = gen;
+    s_clear = !(hdr_magic == kWorkspaceMagic && hdr_gen == gen);
+  }
+  __syncthreads();   // req_flags, s_gam, the block table and the epoch visible to the whole block
+  if (s_clear) clear_tagged(P, tid, nth);
+  // gamma of request b if its rows are read, else -1
+  auto eligible = [&](int b) -> int {
+    if (small) return s_gam[b];
+    return P.req_flags[b] == 0 ? gamma_of(P, b) : -1;
+  };
 
   const int nb = s_nb;
   // rows per block
@@ -186,7 +203,10 @@ __global__ void __launch_bounds__(1024) plan_kernel(Params P) {
     for (int b0 = 0; b0 < B; b0 += 32) {
       const int b = b0 + lane;
       int n = 0;
-      if (b < B && P.req_flags[b] == 0) n = rows_for(bl, gamma_of(P, b));
+      if (b < B) {
+        const int g = eligible(b);
+        if (g >= 0) n = rows_for(bl, g);
+      }
       cnt += __reduce_add_sync(0xffffffffu, n);
     }
     if (lane == 0) s_count[k] = cnt;
@@ -219,9 +239,9 @@ __global__ void __launch_bounds__(1024) plan_kernel(Params P) {
     for (int b0 = 0; b0 < B; b0 += 32) {
       const int b = b0 + lane;
       int n = 0, gam = 0;
-      if (b < B && P.req_flags[b] == 0) {
-        gam = gamma_of(P, b);
-        n = rows_for(bl, gam);
+      if (b < B) {
+        gam = eligible(b);
+        if (gam >= 0) n = rows_for(bl, gam);
       }
       int incl = n;
 #pragma unroll
