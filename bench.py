@@ -313,30 +313,50 @@ def run_ours(args):
                 h[key] = torch.empty_like(s[key], device="cpu").pin_memory()
                 h[key].copy_(s[key])
             host.append(h)
-        dbuf = {key: torch.empty_like(sets[0][key]) for key in host[0]}
+        # two device input buffers: the inputs of step k+1 cross the host link
+        # (on a copy stream) while step k's call and result readback run
+        dbufs = [{key: torch.empty_like(sets[0][key]) for key in host[0]} for _ in range(2)]
         hout = {key: torch.empty_like(v, device="cpu").pin_memory() for key, v in out.items()}
         h2d = sum(v.numel() * v.element_size() for v in host[0].values())
         d2h = sum(v.numel() * v.element_size() for v in hout.values())
         Ke = min(K, args.e2e_steps)
+        copy_stream = torch.cuda.Stream(device=dev)
+        copied = [torch.cuda.Event() for _ in range(2)]
+        consumed = [torch.cuda.Event() for _ in range(2)]
 
-        def e2e_step(k):
-            h = host[k % len(host)]
-            for key in h:
-                dbuf[key].copy_(h[key], non_blocking=True)
-            r = sv.verify_sample(dbuf["target"], dbuf["draft"], dbuf["tokens"], dbuf["gamma"], dbuf["temperature"],
-                                 dbuf["uniforms"], signals=True, ws=ws, out=out)
-            for key in hout:
-                hout[key].copy_(r[key], non_blocking=True)
+        def h2d_copy(k):
+            j = k % 2
+            with torch.cuda.stream(copy_stream):
+                copy_stream.wait_event(consumed[j])       # step k-2 is done with this buffer
+                h = host[k % len(host)]
+                for key in h:
+                    dbufs[j][key].copy_(h[key], non_blocking=True)
+                copied[j].record(copy_stream)
+
+        def e2e_run(k0, n):
+            """Steps k0 .. k0+n-1; each step's inputs go host -> device and its
+            results device -> host inside the run."""
+            copy_stream.wait_stream(stream)     # no copy starts before the run does
+            h2d_copy(k0)
+            for k in range(k0, k0 + n):
+                j = k % 2
+                if k + 1 < k0 + n:
+                    h2d_copy(k + 1)
+                stream.wait_event(copied[j])
+                d = dbufs[j]
+                r = sv.verify_sample(d["target"], d["draft"], d["tokens"], d["gamma"], d["temperature"],
+                                     d["uniforms"], signals=True, ws=ws, out=out)
+                consumed[j].record(stream)
+                for key in hout:
+                    hout[key].copy_(r[key], non_blocking=True)
             stream.synchronize()
-        for k in range(3):
-            e2e_step(k)
+        e2e_run(0, 3)
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        for k in range(Ke):
-            e2e_step(k)
+        e2e_run(0, Ke)
         b.record(stream)
         torch.cuda.synchronize()
         te = max_over_ranks(a.elapsed_time(b) / 1e3, world, dev)
