@@ -170,7 +170,7 @@ int spec_draft_signals(const void* draft_logits, int dtype, int B, int G, int V,
 
 /* Size of the library-owned scratch used by spec_verify_sample_static: 8 MiB.
  * It holds the workspace of spec_workspace_bytes(B, G, V) <= this value, e.g.
- * B <= 437 at G = 8, V = 151936, or B <= 458 at G = 7, V = 151936. */
+ * B <= 509 at G = 8, V = 151936, or B <= 527 at G = 7, V = 151936. */
 #define SPEC_STATIC_WORKSPACE_BYTES (8u << 20)
 
 /* spec_verify_sample without a caller workspace.  The pages have no
