@@ -36,8 +36,20 @@ from speculative_decoding_verification_26_gb300 import workloads as W  # noqa: E
 METRIC = "verify rounds/s and HBM GB/s (% of 8 TB/s) at B=64, gamma=7, V=151936 bf16"
 UNIT = "rounds/s"
 WORKLOAD = "m"
-WORKLOAD_DESC = ("B=64 gamma=7 V=151936 bf16, full-q stochastic verify + draft signals; T=0.7, "
-                 "target N(0,3^2)+Zipf(1.1) bias, draft = target + N(0,1.5^2), y ~ q")
+# The headline workload is m; --workload times the other configurations of
+# the same seeded generator with the same contract (call kind per config).
+WORKLOADS = {
+    "m": ("sample", "B=64 gamma=7 V=151936 bf16, full-q stochastic verify + draft signals; T=0.7, "
+                    "target N(0,3^2)+Zipf(1.1) bias, draft = target + N(0,1.5^2), y ~ q"),
+    "c2": ("greedy", "B=64 gamma=7 V=151936 bf16, greedy verify; target N(0,3^2)+Zipf(1.1) bias, "
+                     "y = argmax replaced w.p. 0.3 by a uniform token"),
+    "c3": ("sample", "B=32 gamma=4 V=128256 bf16, full-q stochastic verify + draft signals; T=0.7, "
+                     "draft = target + N(0,1.5^2), y ~ q"),
+    "c4": ("onehot", "B=64 gamma=8 V=151936 bf16, one-hot q verify; T=1, y = argmax(target + N(0,2^2))"),
+    "c5": ("sample", "B=256 gamma_b in {2,4,6,8} (G=8) V=151936 bf16, full-q stochastic verify + draft signals; "
+                     "T=0.6, draft = target + N(0,1), y ~ q"),
+}
+WORKLOAD_DESC = WORKLOADS[WORKLOAD][1]
 L2_BYTES = 129 * 2**20
 
 
@@ -165,23 +177,32 @@ def peaks():
 
 
 def build_inputs(dev, rank, nsets, sv, torch):
-    """Seeded input sets resident on the device (draft tokens drawn from q by
-    the library's own gamma = 0 draw on the draft rows)."""
-    sets = []
-    for s in range(nsets):
-        wl = W.make(WORKLOAD, rank_round_index(rank, s))
-        B, G, V = wl.B, wl.G, wl.V
-        tgt = torch.from_numpy(wl.target.view(np.int16)).to(dev).view(torch.bfloat16)
-        dr = torch.from_numpy(wl.draft.view(np.int16)).to(dev).view(torch.bfloat16)
-        rows = dr.view(B * G, 1, V)
-        temps = torch.from_numpy(np.repeat(wl.temperature, G)).to(dev)
-        u = torch.from_numpy(wl.draft_aux["uniforms"].reshape(B * G, 1)).to(dev)
-        r = sv.verify_sample(rows, None, torch.zeros(B * G, 0, dtype=torch.int32, device=dev), None, temps, u,
+    """Seeded input sets resident on the device.  Draft tokens: y ~ q by the
+    library's own gamma = 0 draw on the draft rows, or an argmax (torch, lowest
+    index on ties) for the greedy and one-hot configurations."""
+    def bf16_dev(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    def sample_rows(rows, temps, u):
+        n, V = rows.shape
+        r = sv.verify_sample(bf16_dev(rows).view(n, 1, V), None, torch.zeros(n, 0, dtype=torch.int32, device=dev),
+                             None, torch.from_numpy(np.ascontiguousarray(temps, np.float32)).to(dev),
+                             torch.from_numpy(np.ascontiguousarray(u, np.float32).reshape(n, 1)).to(dev),
                              signals=False)
         torch.cuda.synchronize()
         assert int(r["status"].abs().sum()) == 0
-        y = r["tokens"][:, 0].reshape(B, G).contiguous()
-        sets.append(dict(target=tgt, draft=dr, tokens=y, gamma=torch.from_numpy(wl.gamma).to(dev),
+        return r["tokens"][:, 0].cpu().numpy()
+
+    def argmax_rows(rows):
+        x = bf16_dev(rows).float() if rows.dtype == np.uint16 else torch.from_numpy(rows).to(dev)
+        return x.argmax(dim=-1).int().cpu().numpy()
+
+    sets = []
+    for s in range(nsets):
+        wl = W.make(WORKLOAD, rank_round_index(rank, s))
+        W.resolve_draft_tokens(wl, sample_rows, argmax_rows)
+        sets.append(dict(target=bf16_dev(wl.target), draft=bf16_dev(wl.draft) if wl.draft is not None else None,
+                         tokens=torch.from_numpy(wl.draft_tokens).to(dev), gamma=torch.from_numpy(wl.gamma).to(dev),
                          temperature=torch.from_numpy(wl.temperature).to(dev),
                          uniforms=torch.from_numpy(wl.uniforms).to(dev), host=wl))
     return sets
@@ -202,15 +223,24 @@ def run_ours(args):
     sets = build_inputs(dev, rank, args.sets, sv, torch)
     B, G, V = sets[0]["host"].B, sets[0]["host"].G, sets[0]["host"].V
     ws = torch.empty(sv.workspace_bytes(B, G, V), dtype=torch.uint8, device=dev)
+    mode = WORKLOADS[WORKLOAD][0]
     out = dict(accept_len=torch.empty(B, dtype=torch.int32, device=dev),
                tokens=torch.empty(B, G + 1, dtype=torch.int32, device=dev),
-               status=torch.empty(B, dtype=torch.int32, device=dev),
-               signals=torch.empty(B, 4, dtype=torch.float32, device=dev))
+               status=torch.empty(B, dtype=torch.int32, device=dev))
+    if mode == "sample":
+        out["signals"] = torch.empty(B, 4, dtype=torch.float32, device=dev)
 
-    def step(k):
-        s = sets[k % len(sets)]
+    def call(s):
+        if mode == "greedy":
+            return sv.verify_greedy(s["target"], s["tokens"], s["gamma"], ws=ws, out=out)
+        if mode == "onehot":
+            return sv.verify_onehot(s["target"], s["tokens"], s["gamma"], s["temperature"], s["uniforms"],
+                                    ws=ws, out=out)
         return sv.verify_sample(s["target"], s["draft"], s["tokens"], s["gamma"], s["temperature"], s["uniforms"],
                                 signals=True, ws=ws, out=out)
+
+    def step(k):
+        return call(sets[k % len(sets)])
 
     # per-set outcome (accept lengths) -> committed tokens and algorithmic bytes
     rows_needed, committed = [], []
@@ -219,11 +249,13 @@ def run_ours(args):
         torch.cuda.synchronize()
         kk = r["accept_len"].cpu().numpy().astype(np.int64)
         gam = sets[k]["host"].gamma.astype(np.int64)
-        rows_needed.append(int(np.sum(kk + 1) + np.sum(gam)))      # target 0..k, every draft row
+        # target rows 0..k, and with the signals every draft row
+        rows_needed.append(int(np.sum(kk + 1) + (np.sum(gam) if mode == "sample" else 0)))
         committed.append(int(np.sum(kk + 1)))
         assert int(r["status"].abs().sum()) == 0
     es = 2
-    F_bytes = int((2 * sets[0]["host"].gamma.astype(np.int64) + 1).sum()) * V * es   # every valid row once
+    gam0 = sets[0]["host"].gamma.astype(np.int64)
+    F_bytes = int(((2 * gam0 + 1) if mode == "sample" else (gam0 + 1)).sum()) * V * es   # every valid row once
 
     # warm-up (at least W calls and ~0.5 s so clocks settle)
     props = torch.cuda.get_device_properties(dev)
@@ -309,7 +341,10 @@ def run_ours(args):
         host = []
         for s in sets:
             h = {}
-            for key in ("target", "draft", "tokens", "gamma", "temperature", "uniforms"):
+            keys = {"greedy": ("target", "tokens", "gamma"),
+                    "onehot": ("target", "tokens", "gamma", "temperature", "uniforms")}.get(
+                mode, ("target", "draft", "tokens", "gamma", "temperature", "uniforms"))
+            for key in keys:
                 h[key] = torch.empty_like(s[key], device="cpu").pin_memory()
                 h[key].copy_(s[key])
             host.append(h)
@@ -343,9 +378,7 @@ def run_ours(args):
                 if k + 1 < k0 + n:
                     h2d_copy(k + 1)
                 stream.wait_event(copied[j])
-                d = dbufs[j]
-                r = sv.verify_sample(d["target"], d["draft"], d["tokens"], d["gamma"], d["temperature"],
-                                     d["uniforms"], signals=True, ws=ws, out=out)
+                r = call(dbufs[j])
                 consumed[j].record(stream)
                 for key in hout:
                     hout[key].copy_(r[key], non_blocking=True)
@@ -365,7 +398,7 @@ def run_ours(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
-        cpu = cpu_baseline(sets[0]["host"], sets[0]["tokens"].cpu().numpy(), args.cpu_seconds)
+        cpu = cpu_baseline(sets[0]["host"], sets[0]["tokens"].cpu().numpy(), args.cpu_seconds, mode)
 
     if rank == 0:
         mean_committed = statistics.mean(committed)
@@ -404,7 +437,7 @@ def run_ours(args):
 # ----------------------------------------------------------------------------
 # the oracle on the host cores
 
-def cpu_baseline(wl, tokens, seconds):
+def cpu_baseline(wl, tokens, seconds, mode="sample"):
     """The fp64 oracle (test infrastructure, as it stands) on full rounds of the
     same workload, repeated on one input set for about `seconds` of wall time."""
     import oracle
@@ -414,8 +447,13 @@ def cpu_baseline(wl, tokens, seconds):
     t0 = time.perf_counter()
     n = 0
     while n < 1 or time.perf_counter() - t0 < seconds:
-        o.verify_sample(wl.target, wl.draft, wl.draft_tokens, wl.gamma, wl.temperature, wl.uniforms,
-                        want_signals=True, nthreads=cores)
+        if mode == "greedy":
+            o.verify_greedy(wl.target, wl.draft_tokens, wl.gamma, nthreads=cores)
+        elif mode == "onehot":
+            o.verify_onehot(wl.target, wl.draft_tokens, wl.gamma, wl.temperature, wl.uniforms, nthreads=cores)
+        else:
+            o.verify_sample(wl.target, wl.draft, wl.draft_tokens, wl.gamma, wl.temperature, wl.uniforms,
+                            want_signals=True, nthreads=cores)
         n += 1
     dt = time.perf_counter() - t0
     return {"value": n / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
@@ -480,9 +518,20 @@ def main(argv=None):
     ap.add_argument("--min-warmup-s", type=float, default=0.5, help="keep warming up at least this long")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="m",
+                    help="m (default) is the headline; c2..c5 time the other configurations")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    global WORKLOAD, WORKLOAD_DESC, METRIC
+    WORKLOAD = args.workload
+    WORKLOAD_DESC = WORKLOADS[WORKLOAD][1]
+    if WORKLOAD != "m":
+        c = W.CONFIGS[WORKLOAD]
+        METRIC = (f"verify rounds/s and HBM GB/s (% of 8 TB/s) at B={c['B']}, gamma={c['G']}, V={c['V']} bf16, "
+                  f"{WORKLOADS[WORKLOAD][0]}")
+        if args.impl == "reference" and WORKLOADS[WORKLOAD][0] != "sample":
+            ap.error("the reference arm times the full-q workloads (m, c3, c5)")
     if args.impl == "reference":
         run_reference(args)
     else:
