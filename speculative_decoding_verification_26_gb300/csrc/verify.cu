@@ -1,8 +1,8 @@
 // verify.cu -- the two kernels of one verification call.
 //
-// plan_kernel (1 CTA): sets the call's epoch, resets the counters, settles
-// the requests whose inputs are invalid up front, and writes the
-// position-major row schedule.
+// plan_kernel (1 CTA): takes the call's epoch from the device-wide call
+// counter, resets the counters, settles the requests whose inputs are
+// invalid up front, and writes the position-major row schedule.
 //
 // verify_kernel: a persistent, warp-specialised kernel (every CTA resident,
 // 2 per SM) that takes a request from its logits to its committed tokens.
@@ -27,8 +27,9 @@
 //   2 epilogue warps  merge each chunk's 8 warp partials and publish them as
 //                   tagged words (see tword);
 //   owner warp      serves requests b = CTA, CTA + grid, ...: merges their
-//                   rows from the tagged partials in fixed order, tests the
-//                   positions in order (sections 3.1-3.3, 5.1), publishes the
+//                   rows from the tagged partials in fixed order, reads the
+//                   logits at the draft tokens itself, tests the positions in
+//                   order (sections 3.1-3.3, 5.1), publishes the
 //                   first reject (early exit), runs the draw and writes the
 //                   outputs.  Every decision of a request is taken in one warp.
 // Every spin is bounded; a wait that gives up sets SPEC_ST_TIMEOUT, the other
