@@ -160,6 +160,36 @@ def test_repeatable(o, dev):
         np.testing.assert_array_equal(a[k], b[k])
 
 
+def test_more_requests_than_ctas(o, dev):
+    """B above the grid (2 CTAs per SM on 152 SMs): each owner warp serves
+    several requests, one after the other; past 4096 requests the plan
+    kernel reads the request checks back from global memory."""
+    for B, G, V in [(700, 3, 1500), (4200, 1, 200)]:
+        wl = PT.make_workload(o, "c3", 21, B=B, G=G, V=V)
+        for mode in ["greedy", "sample", "onehot"]:
+            PT.compare(o, mode, wl, PT.run_gpu(mode, wl, dev), PT.run_oracle(o, mode, wl), PT.Tally())
+
+
+def test_max_gamma_and_long_acceptance(o, dev):
+    """G = 31, the largest the boundary allows, with a draft close to the
+    target so that most requests accept deep into the block (every lane of
+    the owner's per-position values is used)."""
+    wl = PT.make_workload(o, "c3", 22, B=12, G=31, V=2500, overrides=dict(sigma_d=0.02))
+    # (draft tokens past a request's gamma are never read)
+    wl.gamma[:] = np.array([31, 31, 30, 0, 1, 16, 31, 29, 31, 7, 31, 2], np.int32)
+    for mode in ["greedy", "sample", "onehot"]:
+        t = PT.Tally()
+        PT.compare(o, mode, wl, PT.run_gpu(mode, wl, dev), PT.run_oracle(o, mode, wl), t)
+    ref = PT.run_oracle(o, "sample", wl)
+    assert int(ref["accept_len"].max()) >= 20          # deep positions are exercised
+
+
+def test_single_request(o, dev):
+    wl = PT.make_workload(o, "m", 23, B=1)
+    for mode in ["greedy", "sample", "onehot"]:
+        PT.compare(o, mode, wl, PT.run_gpu(mode, wl, dev), PT.run_oracle(o, mode, wl), PT.Tally())
+
+
 def test_stale_words_in_reused_memory(o, dev):
     """Memory a workspace takes over may hold small integers left by earlier
     tensors or calls.  Here every word after the header is overwritten with a
