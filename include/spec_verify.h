@@ -96,7 +96,10 @@ enum {
     SPEC_ST_BAD_UNIFORM = 128    /* a uniform that was used is not in [0,1) */
 };
 
-/* Limits checked by the host: 1 <= B <= 65535, 0 <= G <= 31, 2 <= V < 2^28. */
+/* Limits checked by the host: 1 <= B <= 65535, 0 <= G <= 31, 2 <= V < 2^28,
+ * and the internal work and queue counts (B (2G+1) ceil(V / 16384) chunks,
+ * B (2 ceil(V / 4096) + 2) draw entries) below 2^31; no device could hold
+ * the logits of sizes past those. */
 #define SPEC_MAX_B 65535
 #define SPEC_MAX_G 31
 

@@ -69,10 +69,12 @@ int device_state(int* ctas) {
 
 bool sizes_ok(int B, int G, int V) {
   if (B < 1 || B > SPEC_MAX_B || G < 0 || G > SPEC_MAX_G || V < 2 || V >= (1 << 28)) return false;
-  // work items are counted in 32 bits
-  const long long ce = chunk_elems(SPEC_F32);
+  // work items, draw-queue and deferred-queue entries are counted in 32 bits
+  const long long ce = chunk_elems(SPEC_F32), se = stage_elems(SPEC_F32);
   const long long rows = (long long)B * (2 * G + 1);
-  return rows * ((V + ce - 1) / ce) < (1ll << 31);
+  const long long nch = (V + ce - 1) / ce, nres = (V + se - 1) / se;
+  return rows * nch < (1ll << 31) && (long long)B * (2 * nres + 2) < (1ll << 31) &&
+         (long long)B * G * nch < (1ll << 31);
 }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }

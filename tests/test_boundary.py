@@ -40,6 +40,9 @@ def test_workspace_bytes(L):
     assert L.spec_workspace_bytes(0, 7, 151936) == 0
     assert L.spec_workspace_bytes(64, 32, 151936) == 0
     assert L.spec_workspace_bytes(64, 7, 1) == 0
+    # sizes whose queue capacities would not fit in 32 bits are refused, not
+    # wrapped (their logits could not exist on a device anyway)
+    assert L.spec_workspace_bytes(65535, 0, (1 << 28) - 1) == 0
     a = L.spec_workspace_bytes(64, 7, 151936)
     b = L.spec_workspace_bytes(128, 7, 151936)
     assert 0 < a < b
