@@ -640,15 +640,14 @@ enum DrawWord : int { DW_KIND = 0, DW_EXCL, DW_M1, DW_S1, DW_M2, DW_S2, DW_C, DW
 
 struct ItemMeta {
   unsigned q;
-  int rid, b, i, kind, chunk, y;
+  int rid, b, i, kind, chunk;
   bool valid, skip, defer;          // defer: a signal-only draft row, read after the main queue
   float c;
 };
 
 // Metadata of a claimed static item, in two dependent levels so the producer
 // can keep them in flight while it stages earlier items: the row id (from the
-// schedule), then per-request values (first known reject, temperature,
-// gamma, draft token).
+// schedule), then per-request values (first known reject, temperature).
 __device__ __forceinline__ int item_row(const Params& P, unsigned q, unsigned n_items) {
   return q < n_items ? __ldg(P.row_list + q / (unsigned)P.nch) : 0;
 }
@@ -658,7 +657,7 @@ __device__ __forceinline__ int item_row(const Params& P, unsigned q, unsigned n_
 // item in between, so the loads are not waited for).
 struct RawMeta {
   unsigned q;
-  int rid, b, i, kind, kr, gam, tok;
+  int rid, b, i, kind, kr;
   float c;
 };
 
@@ -668,16 +667,11 @@ __device__ __forceinline__ RawMeta item_meta_raw(const Params& P, unsigned q, in
   m.q = q;
   m.rid = rid;
   m.b = m.i = m.kind = 0;
-  m.kr = kNoReject; m.gam = 0; m.tok = -1; m.c = 0.f;
+  m.kr = kNoReject; m.c = 0.f;
   if (q >= n_items) return m;
-  const int G = P.G;
-  decode_row(rid, P.B, G, m.kind, m.b, m.i);
-  const int b = m.b, i = m.i;
-  m.kr = ld_relaxed(P.known_reject + b);
-  if (!GREEDY) m.c = __ldg(P.req_scale + b);
-  m.gam = __ldg(P.req_gam + b);
-  // the draft token (sample / one-hot only: signals-only calls have no tokens)
-  if (!GREEDY && P.mode != MODE_SIGNALS && i < G) m.tok = __ldg(P.draft_tokens + (size_t)b * G + i);
+  decode_row(rid, P.B, P.G, m.kind, m.b, m.i);
+  m.kr = ld_relaxed(P.known_reject + m.b);
+  if (!GREEDY) m.c = __ldg(P.req_scale + m.b);
   return m;
 }
 
@@ -693,7 +687,6 @@ __device__ __forceinline__ ItemMeta finish_meta(const Params& P, const RawMeta& 
   m.defer = late && r.kind == KIND_DRAFT && P.signals_on;
   m.skip = late && !m.defer;
   m.c = r.c;
-  m.y = r.i < r.gam ? r.tok : -1;
   return m;
 }
 
@@ -747,7 +740,6 @@ __device__ bool stage_stats_item(const Params& P, VSmem& S, int& stage, uint32_t
   it.head0 = e_begin; it.nhead = nhead;
   it.tail0 = e_end - ntail; it.ntail = ntail;
   it.c = cur.c;
-  it.y = cur.y;
   StageDesc d;
   d.item = islot;
   const uint64_t pol = l2_policy(cur.i <= P.keep_pos);
