@@ -89,8 +89,7 @@ enum {
     SPEC_ST_BAD_TOKEN = 2,       /* draft token outside [0, V)              */
     SPEC_ST_BAD_GAMMA = 4,       /* gamma_b outside [0, G]                  */
     SPEC_ST_ZERO_RESIDUAL = 8,   /* residual mass rounded to 0: drew from p */
-    SPEC_ST_GUARDED = 16,        /* a near-tie decision was re-taken in
-                                    extended precision (informational)     */
+    SPEC_ST_GUARDED = 16,        /* reserved: never set by this version     */
     SPEC_ST_TIMEOUT = 32,        /* an internal wait hit its time limit     */
     SPEC_ST_BAD_TEMPERATURE = 64,/* temperature <= 0 or not finite          */
     SPEC_ST_BAD_UNIFORM = 128    /* a uniform that was used is not in [0,1) */

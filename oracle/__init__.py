@@ -46,6 +46,9 @@ PLANTS = {
     "onehot_keep_y": 10,
     "no_stop": 11,
     "accept_nonstrict": 12,
+    "probe_next_bucket": 13,
+    "margin_one_sided": 14,
+    "accept_margin_unnormalised": 15,
 }
 
 _lock = threading.Lock()

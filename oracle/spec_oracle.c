@@ -62,8 +62,12 @@
  *   - accept_prob: pinned through A = 1 - TV(p, q) (section 4.3);
  *   - signals: pinned by closed forms (uniform, two-way tie, near one-hot rows)
  *     and by scipy's entropy on random rows;
- *   - the decision margins (accept_margin, draw_margin, probe_distance) are
- *     diagnostics of this oracle only and have no pin ("parity unpinned").
+ *   - the decision margins: accept_margin = |u_i - a_i| (the distance of the
+ *     acceptance test of section 3.2 from its threshold), draw_margin (the
+ *     distance of t = u W from the nearer edge of the drawn bucket, over W)
+ *     and probe_distance (the distance of t from the bucket of a given token,
+ *     over W) are pinned by hand-computed cases on rows whose probabilities
+ *     are exact binary fractions (tests).
  *
  * Planted mistakes: compiling with -DORACLE_PLANT=n introduces one deliberate
  * error (see the ORACLE_PLANT switch below).  The tests build each planted
@@ -92,6 +96,9 @@
 #define PLANT_ONEHOT_KEEP_Y 10       /* one-hot residual keeps y               */
 #define PLANT_NO_STOP 11             /* keeps testing after a reject           */
 #define PLANT_ACCEPT_NONSTRICT 12    /* accept iff u <= a                      */
+#define PLANT_PROBE_NEXT_BUCKET 13   /* probe distance to the bucket after it  */
+#define PLANT_MARGIN_ONE_SIDED 14    /* draw margin to the upper edge only     */
+#define PLANT_ACCEPT_MARGIN_UNNORM 15 /* accept margin |u q(y) - p(y)|         */
 
 /* dtype codes of the input logits */
 #define ORACLE_F32 0
@@ -207,7 +214,11 @@ static int draw_inverse_cdf(const double* w, int V, double u, double* margin,
     for (int v = 0; v < V; ++v) {
         Cprev = C;
         C += w[v];
+#if ORACLE_PLANT == PLANT_PROBE_NEXT_BUCKET
+        if (probe == v - 1 && probe_dist) {
+#else
         if (probe == v && probe_dist) {
+#endif
             double d = 0.0;
             if (t < Cprev) d = Cprev - t;
             else if (t >= C) d = t - C;
@@ -220,6 +231,9 @@ static int draw_inverse_cdf(const double* w, int V, double u, double* margin,
 #endif
             z = v;
             double d0 = t - Cprev, d1 = C - t;
+#if ORACLE_PLANT == PLANT_MARGIN_ONE_SIDED
+            d0 = d1;
+#endif
             *margin = (d0 < d1 ? d0 : d1) / W;
         }
     }
@@ -383,7 +397,11 @@ static void run_request(const job_t* J, int b, double* x, double* p, double* q, 
         int accept = ui * qy < py;
 #endif
         if (J->accept_prob) J->accept_prob[(size_t)b * G + i] = a;
+#if ORACLE_PLANT == PLANT_ACCEPT_MARGIN_UNNORM
+        if (J->accept_margin) J->accept_margin[(size_t)b * G + i] = fabs(ui * qy - py);
+#else
         if (J->accept_margin) J->accept_margin[(size_t)b * G + i] = fabs(ui - a);
+#endif
         if (!accept) {
 #if ORACLE_PLANT == PLANT_NO_STOP
             /* keeps going and remembers the residual of the last reject */

@@ -228,7 +228,7 @@ const char* spec_request_status_string(int bit) {
     case SPEC_ST_BAD_TOKEN: return "draft token outside [0, V)";
     case SPEC_ST_BAD_GAMMA: return "gamma outside [0, G]";
     case SPEC_ST_ZERO_RESIDUAL: return "residual mass rounded to zero; drew from p";
-    case SPEC_ST_GUARDED: return "near-tie decision re-taken in extended precision";
+    case SPEC_ST_GUARDED: return "reserved (never set)";
     case SPEC_ST_TIMEOUT: return "internal wait timed out";
     case SPEC_ST_BAD_TEMPERATURE: return "temperature not positive and finite";
     case SPEC_ST_BAD_UNIFORM: return "uniform outside [0, 1)";

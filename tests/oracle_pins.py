@@ -442,6 +442,57 @@ def pin_status_semantics(o):
     assert r["status"][0] == 0
 
 
+def pin_decision_margins(o):
+    """The near-tie diagnostics the parity comparison relies on, on rows whose
+    probabilities are exact binary fractions (values computed by hand):
+      accept_margin  = |u - a|, a = min(1, p(y)/q(y))   (tutorial section 3.2);
+      draw_margin    = min(t - C(z-1), C(z) - t) / W with t = u W, z the drawn
+                       token and C the ascending cumulative weight;
+      probe_distance = the distance from t to the bucket [C(v-1), C(v)) of a
+                       given token v, over W (0 when t lies inside it)."""
+    one = np.ones(1, np.float32)
+    # draw from p = [1/2, 0, 1/2, 0] (gamma = 0, W = 1): buckets [0, .5), -, [.5, 1), -
+    xt = np.array([[[0.0, -np.inf, 0.0, -np.inf]]])
+    for u, z, margin in [(0.5 - 2**-24, 0, 2**-24), (0.25, 0, 0.25), (0.125, 0, 0.125),
+                         (0.625, 2, 0.125), (0.75, 2, 0.25), (0.5, 2, 0.0)]:
+        r = o.run(O.SAMPLE, target=xt, draft=None, draft_tokens=None, temperature=one,
+                  uniforms=np.array([[u]], np.float32))
+        assert r["tokens"][0, 0] == z, (u, r["tokens"][0, 0])
+        assert r["draw_margin"][0] == margin, (u, r["draw_margin"][0], margin)
+    # probe distances on p = [1/2, 1/4, 1/4] (logits ln 2, 0, 0): buckets
+    # [0, .5), [.5, .75), [.75, 1)
+    xt = np.array([[[math.log(2.0), 0.0, 0.0]]])
+    for u, probe, dist in [(0.125, 1, 0.375), (0.125, 2, 0.625), (0.125, 0, 0.0),
+                           (0.875, 0, 0.375), (0.875, 1, 0.125), (0.625, 1, 0.0),
+                           (0.625, 2, 0.125), (0.5, 0, 0.0), (0.5, 1, 0.0)]:
+        r = o.run(O.SAMPLE, target=xt, draft=None, draft_tokens=None, temperature=one,
+                  uniforms=np.array([[u]], np.float32), probe_token=np.array([probe], np.int32))
+        assert abs(r["probe_distance"][0] - dist) < 1e-15, (u, probe, r["probe_distance"][0], dist)
+    # on a residual: p = [1/2, 1/4, 1/4], q = [1/4, 1/2, 1/4] -> [p - q]_+ = [1/4, 0, 0];
+    # W = 1/4, so t = u / 4 and the margin is measured over W
+    xd = np.array([[[0.0, math.log(2.0), 0.0]]])
+    tgt = np.concatenate([xt, xt], axis=1)
+    for u_draw, margin in [(0.5, 0.5), (0.125, 0.125), (0.875, 0.125)]:
+        r = o.run(O.SAMPLE, target=tgt, draft=xd, draft_tokens=np.array([[1]], np.int32), temperature=one,
+                  uniforms=np.array([[1 - 2**-24, u_draw]], np.float32))
+        assert r["accept_len"][0] == 0 and r["tokens"][0, 0] == 0
+        assert abs(r["draw_margin"][0] - margin) < 1e-15, (u_draw, r["draw_margin"][0])
+    # acceptance margins: worked example p = [.6, .3, .1], q = [.2, .5, .3]
+    # a(0) = 1, a(1) = 0.6, a(2) = 1/3
+    g = golden("worked_example.json")
+    tg = np.stack([_f64_logits(g["p"]), _f64_logits(g["p"])])[None]
+    dr = _f64_logits(g["q"])[None, None]
+    for y, u, margin in [(1, 0.5, 0.1), (1, 0.75, 0.15), (2, 0.25, 1.0 / 12), (0, 0.875, 0.125),
+                         (2, 0.5, 1.0 / 6)]:
+        r = o.run(O.SAMPLE, target=tg, draft=dr, draft_tokens=np.array([[y]], np.int32), temperature=one,
+                  uniforms=np.array([[u, 0.5]], np.float32))
+        assert abs(r["accept_margin"][0, 0] - margin) < 1e-12, (y, u, r["accept_margin"][0, 0], margin)
+    # one-hot: the margin is |u - p(y)|
+    r = o.run(O.ONEHOT, target=tg, draft_tokens=np.array([[1]], np.int32), temperature=one,
+              uniforms=np.array([[0.5, 0.5]], np.float32))
+    assert abs(r["accept_margin"][0, 0] - 0.2) < 1e-12
+
+
 ALL_PINS = [
     pin_worked_example,
     pin_worked_example_onehot,
@@ -458,4 +509,5 @@ ALL_PINS = [
     pin_signals_closed_forms,
     pin_bf16_inputs,
     pin_status_semantics,
+    pin_decision_margins,
 ]
