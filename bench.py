@@ -177,21 +177,12 @@ def peaks():
 
 
 def build_inputs(dev, rank, nsets, sv, torch):
-    """Seeded input sets resident on the device.  Draft tokens: y ~ q by the
-    library's own gamma = 0 draw on the draft rows, or an argmax (torch, lowest
-    index on ties) for the greedy and one-hot configurations."""
+    """Seeded input sets resident on the device.  Draft tokens come from the
+    workload's stand-in drafter (the same tokens the reference arm uses); the
+    argmax drafters of the greedy and one-hot configurations use torch's
+    argmax (lowest index on ties)."""
     def bf16_dev(a):
         return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
-
-    def sample_rows(rows, temps, u):
-        n, V = rows.shape
-        r = sv.verify_sample(bf16_dev(rows).view(n, 1, V), None, torch.zeros(n, 0, dtype=torch.int32, device=dev),
-                             None, torch.from_numpy(np.ascontiguousarray(temps, np.float32)).to(dev),
-                             torch.from_numpy(np.ascontiguousarray(u, np.float32).reshape(n, 1)).to(dev),
-                             signals=False)
-        torch.cuda.synchronize()
-        assert int(r["status"].abs().sum()) == 0
-        return r["tokens"][:, 0].cpu().numpy()
 
     def argmax_rows(rows):
         x = bf16_dev(rows).float() if rows.dtype == np.uint16 else torch.from_numpy(rows).to(dev)
@@ -200,12 +191,26 @@ def build_inputs(dev, rank, nsets, sv, torch):
     sets = []
     for s in range(nsets):
         wl = W.make(WORKLOAD, rank_round_index(rank, s))
-        W.resolve_draft_tokens(wl, sample_rows, argmax_rows)
+        W.resolve_draft_tokens(wl, argmax_rows)
         sets.append(dict(target=bf16_dev(wl.target), draft=bf16_dev(wl.draft) if wl.draft is not None else None,
                          tokens=torch.from_numpy(wl.draft_tokens).to(dev), gamma=torch.from_numpy(wl.gamma).to(dev),
                          temperature=torch.from_numpy(wl.temperature).to(dev),
                          uniforms=torch.from_numpy(wl.uniforms).to(dev), host=wl))
     return sets
+
+
+def all_rows_bytes(wl, mode):
+    """Bytes of every valid logit row of one round, each read once."""
+    gam = wl.gamma.astype(np.int64)
+    rows = ((2 * gam + 1) if mode == "sample" else (gam + 1)).sum()
+    return int(rows) * wl.V * wl.elem_bytes
+
+
+def config_dict(wl, world, nsets, F_bytes):
+    """The `config` of the JSON line, identical for both arms."""
+    return {"workload": WORKLOAD_DESC, "B": wl.B, "gamma": wl.G, "V": wl.V,
+            "l2": f"{nsets} rotating input sets of {F_bytes/1e6:.0f} MB ({nsets*F_bytes/1e9:.2f} GB > 4x L2)",
+            "parallelism": f"{world} independent request shards, no collective"}
 
 
 def run_ours(args):
@@ -254,8 +259,7 @@ def run_ours(args):
         committed.append(int(np.sum(kk + 1)))
         assert int(r["status"].abs().sum()) == 0
     es = 2
-    gam0 = sets[0]["host"].gamma.astype(np.int64)
-    F_bytes = int(((2 * gam0 + 1) if mode == "sample" else (gam0 + 1)).sum()) * V * es   # every valid row once
+    F_bytes = all_rows_bytes(sets[0]["host"], mode)
 
     # warm-up (at least W calls and ~0.5 s so clocks settle)
     props = torch.cuda.get_device_properties(dev)
@@ -398,7 +402,7 @@ def run_ours(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
-        cpu = cpu_baseline(sets[0]["host"], sets[0]["tokens"].cpu().numpy(), args.cpu_seconds, mode)
+        cpu = cpu_baseline(sets[0]["host"], args.cpu_seconds, mode)
 
     if rank == 0:
         mean_committed = statistics.mean(committed)
@@ -406,10 +410,7 @@ def run_ours(args):
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
             "ms_per_step": t_max / K * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": WORKLOAD_DESC, "B": B, "gamma": G, "V": V,
-                       "l2": f"{nsets} rotating input sets of {F_bytes/1e6:.0f} MB "
-                             f"({nsets*F_bytes/1e9:.2f} GB > 4x L2)",
-                       "parallelism": f"{world} independent request shards, no collective"},
+            "config": config_dict(sets[0]["host"], world, nsets, F_bytes),
             "roofline": {"bound": "hbm", "kernel": "verify_kernel", "achieved": achieved, "peak": hbm_peak,
                          "unit": "GB/s", "frac": achieved / hbm_peak, "peak_kind": peak_kind,
                          "traffic": traffic, "algorithmic_bytes_per_launch": N_bytes,
@@ -437,23 +438,29 @@ def run_ours(args):
 # ----------------------------------------------------------------------------
 # the oracle on the host cores
 
-def cpu_baseline(wl, tokens, seconds, mode="sample"):
+def oracle_round(o, wl, mode, idx, cores):
+    """The fp64 oracle on requests `idx` of one round (OpenMP over requests)."""
+    if mode == "greedy":
+        o.verify_greedy(wl.target[idx], wl.draft_tokens[idx], wl.gamma[idx], nthreads=cores)
+    elif mode == "onehot":
+        o.verify_onehot(wl.target[idx], wl.draft_tokens[idx], wl.gamma[idx], wl.temperature[idx], wl.uniforms[idx],
+                        nthreads=cores)
+    else:
+        o.verify_sample(wl.target[idx], wl.draft[idx], wl.draft_tokens[idx], wl.gamma[idx], wl.temperature[idx],
+                        wl.uniforms[idx], want_signals=True, nthreads=cores)
+
+
+def cpu_baseline(wl, seconds, mode="sample"):
     """The fp64 oracle (test infrastructure, as it stands) on full rounds of the
     same workload, repeated on one input set for about `seconds` of wall time."""
     import oracle
     o = oracle.load()
     cores = os.cpu_count() or 1
-    wl.draft_tokens = tokens.astype(np.int32)
+    idx = np.arange(wl.B)
     t0 = time.perf_counter()
     n = 0
     while n < 1 or time.perf_counter() - t0 < seconds:
-        if mode == "greedy":
-            o.verify_greedy(wl.target, wl.draft_tokens, wl.gamma, nthreads=cores)
-        elif mode == "onehot":
-            o.verify_onehot(wl.target, wl.draft_tokens, wl.gamma, wl.temperature, wl.uniforms, nthreads=cores)
-        else:
-            o.verify_sample(wl.target, wl.draft, wl.draft_tokens, wl.gamma, wl.temperature, wl.uniforms,
-                            want_signals=True, nthreads=cores)
+        oracle_round(o, wl, mode, idx, cores)
         n += 1
     dt = time.perf_counter() - t0
     return {"value": n / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
@@ -462,46 +469,60 @@ def cpu_baseline(wl, tokens, seconds, mode="sample"):
 
 
 def run_reference(args):
+    """The reference arm: the fp64 oracle, as it stands, on the host cores, on
+    the same input sets, draft tokens, metric and config as our arm.  A step
+    verifies `per_step` requests of the rotating rounds (a full round when K
+    rounds fit in about a minute, else a divisor of B sized so they do); the
+    requests of consecutive steps are verified a round at a time (one oracle
+    call, OpenMP over that round's requests), so a step of a few requests
+    costs what it costs inside a full round."""
     rank, world, _ = rank_env()
     if rank != 0:
         return
     import oracle
     o = oracle.load()
     cores = os.cpu_count() or 1
-    wl = W.make(WORKLOAD, rank_round_index(0, 0))
-    B, G, V = wl.B, wl.G, wl.V
-    # draft tokens y ~ q drawn by the oracle's own categorical draw
-    rows = wl.draft.reshape(B * G, V)
-    wl.draft_tokens = o.run(oracle.SAMPLE, target=rows[:, None, :], temperature=np.repeat(wl.temperature, G),
-                            uniforms=wl.draft_aux["uniforms"].reshape(B * G, 1), G=0)["tokens"][:, 0]
-    wl.draft_tokens = wl.draft_tokens.reshape(B, G).astype(np.int32)
+    mode = WORKLOADS[WORKLOAD][0]
 
-    def sub(idx):
-        return dict(target=wl.target[idx], draft=wl.draft[idx], tok=wl.draft_tokens[idx], gamma=wl.gamma[idx],
-                    T=wl.temperature[idx], u=wl.uniforms[idx])
+    def argmax_rows(rows):
+        return o.run(oracle.GREEDY, target=np.ascontiguousarray(rows)[:, None, :], G=0)["tokens"][:, 0]
 
-    # A step is one request of the round (a bounded sample of the workload:
-    # about 25 ms of fp64 work on one core).  The K timed steps run `cores` at a
-    # time, one request per OpenMP thread, so K = 20000 steps take ~30 s.
+    sets = []
+    for s in range(args.sets):
+        wl = W.make(WORKLOAD, rank_round_index(0, s))
+        W.resolve_draft_tokens(wl, argmax_rows)
+        sets.append(wl)
+    B = sets[0].B
+    t0 = time.perf_counter()
+    oracle_round(o, sets[0], mode, np.arange(B), cores)          # one round: size the steps
+    t_round = time.perf_counter() - t0
+    budget_s = args.ref_seconds
+    divisors = [d for d in range(1, B + 1) if B % d == 0]
+    per_step = max([d for d in divisors if args.steps * t_round * d / B <= budget_s] or [1])
+
     def run_steps(k0, n):
-        for j in range(0, n, cores):
-            idx = (np.arange(min(cores, n - j)) + k0 + j) % B
-            s = sub(idx)
-            o.verify_sample(s["target"], s["draft"], s["tok"], s["gamma"], s["T"], s["u"], want_signals=True,
-                            nthreads=min(cores, len(idx)))
-    run_steps(0, args.warmup)
+        """Steps k0 .. k0+n-1: their requests, a round (input set) at a time."""
+        r0, r1 = k0 * per_step, (k0 + n) * per_step             # request counter range
+        while r0 < r1:
+            rnd, off = divmod(r0, B)
+            m = min(B - off, r1 - r0)
+            oracle_round(o, sets[rnd % len(sets)], mode, np.arange(off, off + m), cores)
+            r0 += m
+    run_steps(0, max(args.warmup, 1))
     t0 = time.perf_counter()
     run_steps(args.warmup, args.steps)
     dt = time.perf_counter() - t0
-    value = args.steps / B / dt
-    threads = min(cores, args.steps)
-    sample = (f"each step: 1 of the {B} requests of one round (fp64); the {args.steps} timed steps run "
-              f"{threads} at a time, OpenMP over requests")
+    rounds = args.steps * per_step / B
+    value = rounds / dt
+    F_bytes = all_rows_bytes(sets[0], mode)
+    sample = (f"each step: {per_step} of the {B} requests of a round (fp64 oracle); the {args.steps} timed steps "
+              f"({rounds:g} rounds of {len(sets)} rotating input sets) run a round's requests per call, "
+              f"OpenMP over requests on {cores} threads")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": WORKLOAD_DESC, "B": B, "gamma": G, "V": V},
-            "cpu_baseline": {"kind": "oracle", "cores": threads, "sample": sample, "value": value, "unit": UNIT},
+            "config": config_dict(sets[0], world, len(sets), F_bytes),
+            "cpu_baseline": {"kind": "oracle", "cores": cores, "sample": sample, "value": value, "unit": UNIT},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -515,6 +536,8 @@ def main(argv=None):
     ap.add_argument("--sets", type=int, default=4, help="rotating input sets (L2 flush by footprint)")
     ap.add_argument("--e2e-steps", type=int, default=500)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-seconds", type=float, default=60.0,
+                    help="reference arm: size its steps so the timed ones take about this long")
     ap.add_argument("--min-warmup-s", type=float, default=0.5, help="keep warming up at least this long")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
@@ -530,8 +553,6 @@ def main(argv=None):
         c = W.CONFIGS[WORKLOAD]
         METRIC = (f"verify rounds/s and HBM GB/s (% of 8 TB/s) at B={c['B']}, gamma={c['G']}, V={c['V']} bf16, "
                   f"{WORKLOADS[WORKLOAD][0]}")
-        if args.impl == "reference" and WORKLOADS[WORKLOAD][0] != "sample":
-            ap.error("the reference arm times the full-q workloads (m, c3, c5)")
     if args.impl == "reference":
         run_reference(args)
     else:

@@ -126,6 +126,19 @@ uint64_t spec_launch_count(void);
  * so that call's start-up overlap with the kernel before is lost. */
 int spec_profile_next_call(void* begin_event, void* end_event);
 
+/* Testing aid for the timeout path; the method has no counterpart.  Every
+ * wait inside a call (for a staged piece of a row, another CTA's partial
+ * statistics, a draw's slice sums) gives up after `cycles` SM clock cycles;
+ * the request it served then commits nothing and reports SPEC_ST_TIMEOUT,
+ * and every other role of the call gives up as soon as it sees that.  The
+ * setting applies to calls enqueued afterwards by any host thread;
+ * cycles <= 0 restores the default of 4e9 cycles (about 2 s at 2 GHz), which
+ * no healthy call comes near.  A low value (1) makes most requests of a call
+ * time out; it is meant only for tests of that path.  The wait for a CTA's
+ * own copies in flight before it exits always keeps the default.  Returns
+ * SPEC_OK. */
+int spec_set_wait_limit(long long cycles);
+
 /* Greedy verification (tutorial page, section 3.1).  For i = 0..gamma_b-1:
  * g_i = argmax target row i (lowest index among equal maxima); stop at the
  * first y_i != g_i with k = i and commit g_i; if none, k = gamma_b and commit

@@ -9,7 +9,7 @@ loads the library and fails loudly if it is missing.
 """
 from ._lib import (  # noqa: F401
     BF16, F32, SpecVerifyError, draft_signals, launch_count, lib, profile_next_call, request_status_string,
-    status_string,
+    set_wait_limit, status_string,
     verify_greedy, verify_onehot, verify_sample, workspace, workspace_bytes,
 )
 from ._lib import STATIC_WORKSPACE_BYTES, verify_sample_static  # noqa: F401

@@ -52,6 +52,8 @@ def lib(path: str | None = None) -> ctypes.CDLL:
         L.spec_launch_count.restype = ctypes.c_uint64
         L.spec_profile_next_call.argtypes = [P, P]
         L.spec_profile_next_call.restype = I
+        L.spec_set_wait_limit.argtypes = [ctypes.c_longlong]
+        L.spec_set_wait_limit.restype = I
         L.spec_verify_greedy.argtypes = [P, I, I, I, I, P, P, P, P, P, P, SZ, P]
         L.spec_verify_greedy.restype = I
         L.spec_verify_sample.argtypes = [P, P, I, I, I, I, P, P, P, P, P, P, P, P, P, P, SZ, P]
@@ -79,6 +81,14 @@ def workspace_bytes(B: int, G: int, V: int) -> int:
 
 def launch_count() -> int:
     return int(lib().spec_launch_count())
+
+
+def set_wait_limit(cycles: int) -> None:
+    """Testing aid: internal waits of later calls give up after `cycles` SM
+    cycles (<= 0 restores the default); see spec_set_wait_limit."""
+    rc = lib().spec_set_wait_limit(int(cycles))
+    if rc != OK:
+        raise SpecVerifyError(rc, "spec_set_wait_limit")
 
 
 def profile_next_call(begin, end) -> None:

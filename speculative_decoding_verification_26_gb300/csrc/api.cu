@@ -13,6 +13,7 @@
 // after all earlier work on the stream (which may be producing the inputs).
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 #include <mutex>
 
@@ -23,6 +24,7 @@ using namespace sv;
 namespace {
 
 thread_local uint64_t g_launches = 0;
+std::atomic<long long> g_wait_limit{kWaitLimitCycles};   // spec_set_wait_limit
 thread_local cudaEvent_t g_prof_begin = nullptr, g_prof_end = nullptr;
 
 struct DevState {
@@ -147,6 +149,7 @@ int run(const Call& c) {
   P.defq = reinterpret_cast<tword*>(ws + L.defq);
   P.nrows = L.nrows; P.nch = L.nch; P.nres = L.nres; P.dq_cap = L.dq_cap; P.def_cap = L.def_cap;
   P.aligned_rows = ((size_t)c.V * es) % 16 == 0 && aligned(c.target, 16) && aligned(c.draft, 16);
+  P.wait_limit = g_wait_limit.load(std::memory_order_relaxed);
   // Rows a draw may read again (positions 0 .. keep_pos, both models in the
   // full-q mode) are loaded with an evict-last L2 policy, as long as they
   // fill at most 3/4 of the 129 MB L2 of a GB300; the draw then reads them
@@ -238,6 +241,11 @@ const char* spec_request_status_string(int bit) {
 }
 
 uint64_t spec_launch_count(void) { return g_launches; }
+
+int spec_set_wait_limit(long long cycles) {
+  g_wait_limit.store(cycles > 0 ? cycles : kWaitLimitCycles, std::memory_order_relaxed);
+  return SPEC_OK;
+}
 
 int spec_profile_next_call(void* begin_event, void* end_event) {
   g_prof_begin = static_cast<cudaEvent_t>(begin_event);

@@ -64,12 +64,16 @@ constexpr unsigned long long kWorkspaceMagic = 0x5356455246595631ull;
 // Every bounded wait counts SM clock cycles (clock64 is a register of the SM
 // and costs a few cycles to read; the global timer is read from outside the
 // SM and delays the reading warp by about a microsecond under load).
-// 4e9 cycles: about 2 s at the maximum clock, longer when clocked down.
+// 4e9 cycles: about 2 s at the maximum clock, longer when clocked down.  The
+// limit of a call is Params::wait_limit (this default unless a test lowers
+// it); the wait for a CTA's own bulk copies still in flight before it exits
+// always uses the default, so no copy can land in shared memory after exit.
 constexpr long long kWaitLimitCycles = 4000000000ll;
 
 // ---------------------------------------------------------------------------
-// partial statistics of a run of logits, relative to its own max m:
-//   s = sum 2^{(x-m)c},  t = sum (x-m)c * 2^{(x-m)c}  (entropy numerator),
+// partial statistics of a run of logits, relative to the exponent reference
+// R(m) = fl(m c) of its own max m (see ref_of), with a = fl(x c - R(m)):
+//   s = sum 2^a,  t = sum a 2^a  (entropy numerator),
 //   idx = lowest index attaining m,  bad = a NaN was seen (argmax mode).
 struct alignas(16) Part {
   float m, s, t;
@@ -174,6 +178,7 @@ struct Params {
   int dtype, B, G, V, mode, signals_on;
   int aligned_rows;              // every row starts on a 16-byte boundary
   int keep_pos;                  // rows of positions <= keep_pos are kept in L2 for the draw (-1: none)
+  long long wait_limit;          // SM cycles before a wait gives up (kWaitLimitCycles unless lowered)
   const int32_t* draft_tokens;
   const int32_t* gamma;
   const float* temperature;
@@ -276,16 +281,6 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
   return ok != 0;
 }
 
-// Wait for phase `parity` of `bar` to complete; gives up after kWaitLimitCycles.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const long long c0 = clock64();
-  while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (clock64() - c0 > kWaitLimitCycles) return false;
-  }
-}
-
 // 1-D bulk copy global -> shared, completion counted on `bar` (bytes % 16 == 0,
 // both addresses 16-byte aligned).
 // L2 policies of the bulk copies: rows the draw may read again stay in L2
@@ -370,8 +365,17 @@ __device__ __forceinline__ bool row_ok(const RowStats& r, bool argmax_mode) {
   return isfinite(r.s) && r.s > 0.f;
 }
 
+// The exponent reference of a run of logits with max m at scale c: every
+// term of its sums is 2^{fl(x c - R(m))} with R(m) = fl(m c), rounded once,
+// and every rescale between two runs uses R(m1) - R(m2).  So all sums of a
+// row, the probability of one token and the draw weights refer to the same
+// R(m) of the row max and their ratios do not depend on how m c rounds (at
+// |m c| ~ 500, half an ulp of m c is 3e-5 in the exponent).
+__device__ __forceinline__ float ref_of(float m, float c) { return __fmul_rn(m, c); }
+
 // Merge of two partials of the same row (online-softmax rule):
-//   m = max(m1, m2); s = sum_j s_j 2^{(m_j - m)c}; t = sum_j 2^{d_j}(t_j + d_j s_j).
+//   m = max(m1, m2); s = sum_j s_j 2^{d_j}, d_j = R(m_j) - R(m);
+//   t = sum_j 2^{d_j}(t_j + d_j s_j).
 __device__ __forceinline__ Part merge_parts(const Part& a, const Part& b, float c, bool ent) {
   Part r;
   const float m = fmaxf(a.m, b.m);
@@ -379,15 +383,16 @@ __device__ __forceinline__ Part merge_parts(const Part& a, const Part& b, float 
   if (m == -INFINITY) {          // both empty
     r.s = 0.f; r.t = 0.f;
   } else {
+    const float rm = ref_of(m, c);
     float sa = 0.f, ta = 0.f, sb = 0.f, tb = 0.f;
     if (a.s != 0.f) {
-      const float d = (a.m - m) * c;
+      const float d = __fsub_rn(ref_of(a.m, c), rm);
       const float f = ex2(d);
       sa = a.s * f;
       if (ent) ta = f * fmaf(d, a.s, a.t);
     }
     if (b.s != 0.f) {
-      const float d = (b.m - m) * c;
+      const float d = __fsub_rn(ref_of(b.m, c), rm);
       const float f = ex2(d);
       sb = b.s * f;
       if (ent) tb = f * fmaf(d, b.s, b.t);

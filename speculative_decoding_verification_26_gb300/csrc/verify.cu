@@ -314,6 +314,7 @@ struct __align__(128) VSmem {
   StageDesc desc[kStages];
   ItemDesc item[kItemSlots];
   EpiSlot slot[kEpiSlots];
+  long long wait_limit;             // Params::wait_limit, for the waits that see only S
   int abort;
 };
 
@@ -339,7 +340,7 @@ __device__ __forceinline__ bool wait_bar(VSmem& S, uint64_t* bar, uint32_t parit
   while (true) {
     if (mbar_try_wait_sleep(bar, parity, kSleepHintNs)) return true;
     if (aborted(S)) return false;
-    if (clock64() - c0 > kWaitLimitCycles) return false;
+    if (clock64() - c0 > S.wait_limit) return false;
   }
 }
 
@@ -466,14 +467,15 @@ __device__ __forceinline__ void stage_softmax(RunState& r, uint4 (&w)[kVecPerThr
   constexpr int NP = N / 2;                     // pairs per vector
   const float vm = stage_max<DT, false>(w);
   if (vm > r.m) {
+    const float vmc = ref_of(vm, c);
     if (r.m != -INFINITY) {
-      const float d = (r.m - vm) * c;
+      const float d = __fsub_rn(r.mc, vmc);
       const float f = ex2(d);
       if (ENT) r.t = f * fmaf(d, r.s, r.t);
       r.s *= f;
     }
     r.m = vm;
-    r.mc = vm * c;
+    r.mc = vmc;
   }
   const bool packed_clamp = ENT && DT == SPEC_BF16 && c <= kClampScaleMax;
   if (packed_clamp) {
@@ -516,7 +518,7 @@ __device__ __forceinline__ Part warp_softmax_part(const RunState& r, float c, bo
   for (int off = 16; off >= 1; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
   float s = 0.f, t = 0.f;
   if (r.s != 0.f) {                       // lanes that saw nothing contribute 0
-    const float d = (r.m - m) * c;
+    const float d = __fsub_rn(r.mc, ref_of(m, c));
     const float f = ex2(d);
     s = r.s * f;
     if (ent) t = f * fmaf(d, r.s, r.t);
@@ -561,14 +563,15 @@ __device__ __forceinline__ void run_scalar(RunState& r, float x, int e, float c,
     return;
   }
   if (x > r.m) {
+    const float xc = ref_of(x, c);
     if (r.m != -INFINITY) {
-      const float d = (r.m - x) * c;
+      const float d = __fsub_rn(r.mc, xc);
       const float f = ex2(d);
       if (ent) r.t = f * fmaf(d, r.s, r.t);
       r.s *= f;
     }
     r.m = x;
-    r.mc = x * c;
+    r.mc = xc;
   }
   const float a = fmaf(x, c, -r.mc);
   const float ev = ex2(a);
@@ -592,7 +595,6 @@ __device__ __forceinline__ unsigned ld_relaxed_u32(const unsigned* p) {
   asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
-__device__ __forceinline__ void consumer_bar() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumerThreads) : "memory"); }
 
 // ---------------------------------------------------------------------------
 // device work queue
@@ -798,7 +800,7 @@ __device__ bool stage_dyn_item(const Params& P, VSmem& S, int& stage, uint32_t& 
       ok &= tw_ok(w[j], tag);
     }
     if (ok) break;
-    if (aborted(S) || clock64() - c0 > kWaitLimitCycles) return false;
+    if (aborted(S) || clock64() - c0 > P.wait_limit) return false;
   }
   const unsigned kk = tw_u32(w[DW_KIND]);
   const int kind = (int)(kk & 0xffu), k = (int)(kk >> 8);
@@ -948,17 +950,21 @@ __device__ void producer_role(const Params& P, VSmem& S, unsigned epoch) {
     if (ld_relaxed_u32(&P.hdr->error.v) != 0u) break;
     const long long now = clock64();
     if (idle_since < 0) idle_since = now;
-    else if (now - idle_since > kWaitLimitCycles) { ok = false; break; }
+    else if (now - idle_since > P.wait_limit) { ok = false; break; }
     __nanosleep(sleep_ns);
     if (sleep_ns < 256) sleep_ns *= 2;
   }
   if (ok && wait_bar(S, &S.empty[stage], phase ^ 1u)) {
     S.desc[stage].flags = F_TERM;
     mbar_arrive(&S.full[stage]);
-    return;
+    if (++stage == kStages) { stage = 0; phase ^= 1u; }
+  } else {
+    set_abort(P, S);                 // gave up: tell the other roles
   }
-  // gave up: tell the other roles, then let the copies already in flight land
-  set_abort(P, S);
+  // Let every copy this producer issued land before the CTA can exit: the
+  // latest phase of each ring slot, always with the default limit (a copy of
+  // valid memory completes; a consumer that gave up early under a lowered
+  // limit may have left one in flight).
   for (int s = 0; s < kStages; ++s) {
     const uint32_t par = s < stage ? phase : phase ^ 1u;
     const long long c0 = clock64();
@@ -970,8 +976,12 @@ __device__ void producer_role(const Params& P, VSmem& S, unsigned epoch) {
 // ---------------------------------------------------------------------------
 // consumers
 
-// A direct stage (rows not 16-byte aligned): the consumers copy its elements
-// from global memory into the stage buffer, padding the last vector with -inf.
+// A direct stage (rows not 16-byte aligned): each consumer thread copies the
+// elements of the four vectors it reads itself (load_stage) from global
+// memory into the stage buffer, padding past the row's end with -inf.  No
+// thread reads another thread's vectors, so no barrier between the consumer
+// warps is needed (a warp that gave up on a wait can never leave another
+// waiting at one).
 template <int DT>
 __device__ void fill_direct(const Params& P, VSmem& S, int stage, const StageDesc& d, int tid) {
   constexpr int N = VecT<DT>::N;
@@ -979,17 +989,24 @@ __device__ void fill_direct(const Params& P, VSmem& S, int stage, const StageDes
   const int kind = (d.item >> 4) & 1;
   const unsigned char* tens = kind == KIND_TARGET ? P.target : P.draft;
   const long long src_elem = row_elem_offset(kind, it.b, it.i, P.G, P.V) + d.elem0;
-  const int n = min(stage_elems(DT), P.V - d.elem0), npad = d.nvec * N;
-  if (DT == SPEC_BF16) {
-    unsigned short* dst = reinterpret_cast<unsigned short*>(S.ring[stage]);
-    const unsigned short* src = reinterpret_cast<const unsigned short*>(tens) + src_elem;
-    for (int j = tid; j < npad; j += kConsumerThreads) dst[j] = j < n ? __ldg(src + j) : (unsigned short)0xff80u;
-  } else {
-    float* dst = reinterpret_cast<float*>(S.ring[stage]);
-    const float* src = reinterpret_cast<const float*>(tens) + src_elem;
-    for (int j = tid; j < npad; j += kConsumerThreads) dst[j] = j < n ? __ldg(src + j) : -INFINITY;
+  const int n = min(stage_elems(DT), P.V - d.elem0);
+#pragma unroll
+  for (int r = 0; r < kVecPerThread; ++r) {
+    const int v = tid + r * kConsumerThreads;
+    if (v >= d.nvec) continue;                // load_stage pads these itself
+    if (DT == SPEC_BF16) {
+      unsigned short* dst = reinterpret_cast<unsigned short*>(S.ring[stage]) + v * N;
+      const unsigned short* src = reinterpret_cast<const unsigned short*>(tens) + src_elem + v * N;
+#pragma unroll
+      for (int k = 0; k < N; ++k) dst[k] = v * N + k < n ? __ldg(src + k) : (unsigned short)0xff80u;
+    } else {
+      float* dst = reinterpret_cast<float*>(S.ring[stage]) + v * N;
+      const float* src = reinterpret_cast<const float*>(tens) + src_elem + v * N;
+#pragma unroll
+      for (int k = 0; k < N; ++k) dst[k] = v * N + k < n ? __ldg(src + k) : -INFINITY;
+    }
   }
-  consumer_bar();
+  __syncwarp();   // orders the element stores before the vector loads that read them back
 }
 
 // Residual weight [p - q]_+ of one element pair, p = 2^{x_p c - m_p c} / s_p
@@ -1130,8 +1147,8 @@ __device__ void consumer_role(const Params& P, VSmem& S, int cw, int lane) {
     load_stage<DT>(vec, d.nvec, tid, wt);
     if (resid) load_stage<DT>(vec2, d.nvec, tid, wd);
     ResidW R;
-    R.c = it.c; R.mpc = it.m1 * it.c; R.mqc = it.m2 * it.c; R.rp = 1.f / it.s1; R.nrq = -1.f / it.s2;
-    const float mc = it.m1 * it.c;
+    R.c = it.c; R.mpc = ref_of(it.m1, it.c); R.mqc = ref_of(it.m2, it.c); R.rp = 1.f / it.s1; R.nrq = -1.f / it.s2;
+    const float mc = ref_of(it.m1, it.c);
     const float cd = it.c;
     const int excl = it.y;
     const unsigned dtag = it.tag;
@@ -1238,7 +1255,7 @@ __device__ void epilogue_role(const Params& P, VSmem& S, int lane, int e, unsign
       for (int off = 4; off >= 1; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
       float ss = 0.f, tt = 0.f;
       if (p.s != 0.f) {            // an empty partial contributes 0
-        const float dd = (p.m - m) * c;
+        const float dd = __fsub_rn(ref_of(p.m, c), ref_of(m, c));
         const float f = ex2(dd);
         ss = p.s * f;
         if (ent) tt = f * fmaf(dd, p.s, p.t);
@@ -1267,14 +1284,14 @@ __device__ void epilogue_role(const Params& P, VSmem& S, int lane, int e, unsign
 // first reject (early exit), runs the draw and writes the outputs.  All of a
 // request's decisions are taken in one warp, so they need no atomics.
 
-// A wait of the owner gives up after kWaitLimitCycles, or at once when any
+// A wait of the owner gives up after P.wait_limit cycles, or at once when any
 // role of any CTA has given up (the header error word).
 struct OwnerClock {
   long long c0;
   int polls;
   __device__ __forceinline__ void start() { c0 = clock64(); polls = 0; }
   __device__ __forceinline__ bool expired(const Params& P) {
-    const bool mine = __any_sync(0xffffffffu, clock64() - c0 > kWaitLimitCycles);
+    const bool mine = __any_sync(0xffffffffu, clock64() - c0 > P.wait_limit);
     if (mine) {   // this wait gave up: every other role gives up too
       if ((threadIdx.x & 31) == 0) atomicOr(&P.hdr->error.v, (unsigned)SPEC_ST_TIMEOUT);
       return true;
@@ -1455,7 +1472,7 @@ __device__ __forceinline__ int status_of_code(int code) {
 
 // Acceptance test of position i (tutorial page "5.1 投机解码核心原理",
 // sections 3.1-3.3), in fp32 on the merged row statistics:
-//   p(y) = 2^{(x_y - m_p) c} / s_p,  q(y) likewise (1 for one-hot q),
+//   p(y) = 2^{fl(x_y c - R(m_p))} / s_p,  q(y) likewise (1 for one-hot q),
 //   accept <=> u q(y) < p(y),  a = min(1, p(y)/q(y)).
 // A test closer than 1e-5 (relative) to its threshold is counted; it is not
 // published as an early exit.  Returns the position code (with
@@ -1478,8 +1495,8 @@ __device__ int evaluate_pos(const Params& P, int b, int i, const RowRes& T, cons
     else if (y < 0 || y >= V) code = PC_BAD_TOKEN;
     else if (!(u >= 0.f && u < 1.f)) code = PC_BAD_UNIFORM;
     else {
-      const float py = ex2((T.xy - T.st.m) * c) / T.st.s;
-      const float qy = sample ? ex2((D.xy - D.st.m) * c) / D.st.s : 1.f;
+      const float py = ex2(fmaf(T.xy, c, -ref_of(T.st.m, c))) / T.st.s;
+      const float qy = sample ? ex2(fmaf(D.xy, c, -ref_of(D.st.m, c))) / D.st.s : 1.f;
       const float uq = u * qy;
       code = uq < py ? PC_ACCEPT : PC_REJECT;
       a = qy > 0.f ? fminf(1.f, py / qy) : (py > 0.f ? 1.f : 0.f);
@@ -1649,8 +1666,8 @@ __device__ int draw_round(const Params& P, int b, int kind, int k, int excl, con
   // 3. the token: lane l takes the PER consecutive tokens of vector l of the
   // group (one 16-byte load per row when the rows are 16-byte aligned)
   ResidW R;
-  R.c = c; R.mpc = tr.m * c; R.mqc = dr.m * c; R.rp = 1.f / tr.s; R.nrq = -1.f / dr.s;
-  const float mc = tr.m * c;
+  R.c = c; R.mpc = ref_of(tr.m, c); R.mqc = ref_of(dr.m, c); R.rp = 1.f / tr.s; R.nrq = -1.f / dr.s;
+  const float mc = ref_of(tr.m, c);
   const long long trow = row_elem_offset(KIND_TARGET, b, k, G, V);
   const long long drow = resid ? row_elem_offset(KIND_DRAFT, b, k, G, V) : 0;
   float w[PER];
@@ -1721,7 +1738,7 @@ __device__ int draw_round(const Params& P, int b, int kind, int k, int excl, con
 
 // Outputs of one request (warp-wide): committed tokens y_0..y_{k-1} then z,
 // accept_prob for positions <= k, the SpecKV signals (H_i = log2 s_i -
-// t_i / s_i bits and c_i = 1 / s_i, held by lane i), status; then the
+// t_i / s_i bits and c_i = max_v q_i(v), held by lane i), status; then the
 // request is counted as done.
 __device__ void owner_outputs(const Params& P, int b, int gam, int st, int k, int z, float a_lane, float H_lane,
                               float cf_lane, unsigned epoch, int lane) {
@@ -1789,8 +1806,11 @@ __device__ void serve_request(const Params& P, int b, unsigned epoch, int lane) 
   auto take_draft = [&](int i, const RowRes& D) {
     if (sig) {
       if (lane == i) {
+        // H = log2 s - t/s holds for any exponent reference; the largest
+        // term of s is 2^{fl(m c - R(m))}, not exactly 1, so max q is that
+        // term over s
         H_lane = log2f(D.st.s) - D.st.t / D.st.s;
-        cf_lane = 1.f / D.st.s;
+        cf_lane = ex2(fmaf(D.st.m, c, -ref_of(D.st.m, c))) / D.st.s;
       }
       sig_bad |= !row_ok(D.st, false);
     }
@@ -1969,6 +1989,7 @@ __global__ void __launch_bounds__(kStatsThreads, 2) verify_kernel(Params P) {
       S.slot[e].term = 0;
     }
     S.abort = 0;
+    S.wait_limit = P.wait_limit;
     fence_mbar_init();
   }
   __syncthreads();

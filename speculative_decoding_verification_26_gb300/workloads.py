@@ -10,23 +10,33 @@ synthetic stand-ins with the pages' shapes: draft lengths gamma 2-8 with K = 7
 draft positions (DLite page), concurrency 1-64 and beyond, Qwen-family
 (V = 151936) and Llama-family (V = 128256) vocabularies, temperatures 0.6-1.0.
 
-Recipe (all numpy PCG64, platform independent):
+Recipe (all numpy PCG64, platform independent; every logit row's normals come
+from its own child seed, SeedSequence.spawn, and are drawn on a thread pool, so
+the values do not depend on the number of threads):
   * Zipf-like per-token bias shared by every row of a workload:
     b[v] = -1.1 * ln(1 + pi(v)) with pi a seeded random permutation of 0..V-1,
     so frequent tokens are scattered over the vocabulary;
-  * target logits = bf16_rne(N(0, sigma_t^2) + b)   (fp32 configs: no rounding);
+  * target logits = bf16_rne(N(0, sigma_t^2) + b + shift)   (fp32 configs: no
+    rounding; shift = 0 unless a test asks for an offset, which softmax
+    ignores but fp32 exponent arithmetic does not);
   * draft logits  = bf16_rne(float(target) + N(0, sigma_d^2));
   * uniforms [B, G+1] float32 in [0, 1): u = (bits >> 40) * 2^-24;
-  * draft tokens come from a stand-in drafter, which needs a categorical
-    sampler or an argmax; the caller supplies it (see ``resolve_draft_tokens``):
-      - "sample_q":      y_i ~ q_i (softmax of the draft row at T) driven by an
-                         independent uniform stream;
+  * draft tokens come from a stand-in drafter (see ``resolve_draft_tokens``):
+      - "sample_q":      y_i ~ q_i, the draft model's own sampling law
+                         softmax(x / T), drawn by the Gumbel-max trick:
+                         y = argmax_v (x_v / T + g_v), g_v = -ln(-ln U_v) with
+                         U_v uniform from the row's own seed (an exact draw;
+                         only noise and an argmax, in fp64);
       - "argmax_replace": y_i = argmax of target row i, replaced with
                          probability 0.3 by a uniform random token;
-      - "noisy_argmax":  y_i = argmax of (target row i + N(0, 2^2)).
+      - "noisy_argmax":  y_i = argmax of (target row i + N(0, 2^2));
+    the two argmax kinds take a caller-supplied argmax (lowest index on
+    ties), so that this module computes nothing a verification call does.
 """
 from __future__ import annotations
 
+import os
+from concurrent.futures import ThreadPoolExecutor
 from dataclasses import dataclass, field
 
 import numpy as np
@@ -52,11 +62,35 @@ CONFIGS = {
 _CONFIG_ID = {name: i + 1 for i, name in enumerate(CONFIGS)}
 
 
+def _rows_parallel(n: int, fn) -> None:
+    """fn(lo, hi) over row blocks of [0, n) on a thread pool (numpy releases
+    the GIL in its loops; every row is computed the same way whatever the
+    block)."""
+    nt = max(1, min(32, os.cpu_count() or 1, n))
+    step = (n + nt - 1) // nt
+    if nt == 1:
+        fn(0, n)
+        return
+    with ThreadPoolExecutor(nt) as ex:
+        list(ex.map(lambda lo: fn(lo, min(n, lo + step)), range(0, n, step)))
+
+
 def bf16_rne_bits(x: np.ndarray) -> np.ndarray:
     """float32 -> bf16 bit patterns (uint16), round to nearest even."""
-    b = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
-    r = (b + np.uint32(0x7FFF) + ((b >> np.uint32(16)) & np.uint32(1))) >> np.uint32(16)
-    return r.astype(np.uint16)
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    src = x.reshape(-1, x.shape[-1]) if x.ndim > 1 else x.reshape(1, -1)
+    out = np.empty(src.shape, np.uint16)
+
+    def blk(lo, hi):
+        b = src[lo:hi].view(np.uint32)
+        r = (b >> np.uint32(16)) & np.uint32(1)
+        r += np.uint32(0x7FFF)
+        r += b
+        r >>= np.uint32(16)
+        out[lo:hi] = r
+
+    _rows_parallel(src.shape[0], blk)
+    return out.reshape(x.shape)
 
 
 def bf16_bits_to_f32(h: np.ndarray) -> np.ndarray:
@@ -73,6 +107,23 @@ def uniforms01(rng: np.random.Generator, shape) -> np.ndarray:
 def zipf_bias(V: int, rng: np.random.Generator, s: float = 1.1) -> np.ndarray:
     perm = rng.permutation(V)
     return (-s * np.log1p(perm.astype(np.float64))).astype(np.float32)
+
+
+def normal_rows(ss: np.random.SeedSequence, shape, scale: float) -> np.ndarray:
+    """float32 N(0, scale^2) of `shape`; row j (over the last axis) is drawn
+    from child seed j of `ss`, rows in parallel (numpy releases the GIL)."""
+    V = shape[-1]
+    n = int(np.prod(shape[:-1]))
+    out = np.empty((n, V), np.float32)
+    kids = ss.spawn(n)
+
+    def fill(lo, hi):
+        for j in range(lo, hi):
+            np.random.default_rng(kids[j]).standard_normal(V, dtype=np.float32, out=out[j])
+            out[j] *= np.float32(scale)
+
+    _rows_parallel(n, fill)
+    return out.reshape(shape)
 
 
 @dataclass
@@ -110,10 +161,10 @@ def make(name: str, round_idx: int = 0, *, B: int | None = None, G: int | None =
     k_bias, k_t, k_d, k_u, k_y, k_g = ss.spawn(6)
     # the Zipf permutation is fixed per config (shared by all rounds)
     bias = zipf_bias(V, np.random.default_rng([cid, 11])) if cfg.get("zipf") else np.float32(0)
-    rt = np.random.default_rng(k_t)
-    t32 = rt.standard_normal((B, G + 1, V), dtype=np.float32)
-    t32 *= np.float32(cfg["sigma_t"])
+    t32 = normal_rows(k_t, (B, G + 1, V), cfg["sigma_t"])
     t32 += bias
+    if cfg.get("shift"):
+        t32 += np.float32(cfg["shift"])
     if cfg["dtype"] == BF16:
         target = bf16_rne_bits(t32)
         tf = bf16_bits_to_f32(target)
@@ -122,9 +173,7 @@ def make(name: str, round_idx: int = 0, *, B: int | None = None, G: int | None =
         tf = t32
     draft = None
     if "sigma_d" in cfg and G > 0:
-        rd = np.random.default_rng(k_d)
-        d32 = rd.standard_normal((B, G, V), dtype=np.float32)
-        d32 *= np.float32(cfg["sigma_d"])
+        d32 = normal_rows(k_d, (B, G, V), cfg["sigma_d"])
         d32 += tf[:, :G, :]
         draft = bf16_rne_bits(d32) if cfg["dtype"] == BF16 else d32
     if "gammas" in cfg:
@@ -137,32 +186,49 @@ def make(name: str, round_idx: int = 0, *, B: int | None = None, G: int | None =
     aux = {}
     kind = cfg["draft"]
     if kind == "sample_q":
-        aux["uniforms"] = uniforms01(ry, (B, G))
+        aux["gumbel_key"] = [1000 * cid + round_idx, 17]
     elif kind == "argmax_replace":
         aux["replace"] = ry.random((B, G)) < cfg.get("replace_p", 0.3)
         aux["random_tokens"] = ry.integers(0, V, size=(B, G), dtype=np.int32)
     elif kind == "noisy_argmax":
-        noise = ry.standard_normal((B, G, V), dtype=np.float32) * np.float32(cfg.get("noise", 2.0))
-        aux["proxy"] = tf[:, :G, :] + noise        # float32 [B, G, V]
+        noise = normal_rows(np.random.SeedSequence([1000 * cid + round_idx, 13]), (B, G, V), cfg.get("noise", 2.0))
+        noise += tf[:, :G, :]
+        aux["proxy"] = noise                       # float32 [B, G, V]
     return Workload(name, B, G, V, cfg["dtype"], target, draft, gamma.astype(np.int32),
                     temperature, uniforms, kind, aux)
 
 
-def resolve_draft_tokens(wl: Workload, sample_rows, argmax_rows) -> np.ndarray:
-    """Fill ``wl.draft_tokens`` using caller-supplied primitives.
+def gumbel_max_tokens(key, rows: np.ndarray, temps: np.ndarray) -> np.ndarray:
+    """One draw per row from softmax(row / T) by the Gumbel-max trick:
+    argmax_v (x_v / T - ln(-ln U_v)); row j's uniforms come from child seed j
+    of SeedSequence(key).  rows: [n, V] float32, float64 or bf16 bits."""
+    n, V = rows.shape
+    kids = np.random.SeedSequence(key).spawn(n)
+    out = np.empty(n, np.int32)
 
-    sample_rows(logits [n, V], temperature [n], u [n]) -> tokens [n]
-        a categorical draw from softmax(logits / T) driven by u;
-    argmax_rows(logits [n, V]) -> tokens [n]   (lowest index on ties).
-    """
+    def blk(lo, hi):
+        with np.errstate(divide="ignore"):
+            for j in range(lo, hi):
+                x = bf16_bits_to_f32(rows[j]) if rows.dtype == np.uint16 else rows[j]
+                u = np.random.default_rng(kids[j]).random(V)
+                out[j] = int(np.argmax(x.astype(np.float64) / np.float64(temps[j]) - np.log(-np.log(u))))
+
+    _rows_parallel(n, blk)
+    return out
+
+
+def resolve_draft_tokens(wl: Workload, argmax_rows=None) -> np.ndarray:
+    """Fill ``wl.draft_tokens`` from the workload's stand-in drafter (drawn
+    from the current draft rows, so a test that replaces them redraws).
+
+    argmax_rows(logits [n, V]) -> tokens [n] (lowest index on ties) serves
+    the two argmax drafters."""
     B, G, V = wl.B, wl.G, wl.V
     if G == 0:
         wl.draft_tokens = np.zeros((B, 0), np.int32)
         return wl.draft_tokens
     if wl.draft_kind == "sample_q":
-        rows = wl.draft.reshape(B * G, V)
-        temps = np.repeat(wl.temperature, G)
-        y = np.asarray(sample_rows(rows, temps, wl.draft_aux["uniforms"].reshape(-1)), np.int32)
+        y = gumbel_max_tokens(wl.draft_aux["gumbel_key"], wl.draft.reshape(B * G, V), np.repeat(wl.temperature, G))
     elif wl.draft_kind == "argmax_replace":
         rows = wl.target[:, :G, :].reshape(B * G, V)
         y = np.asarray(argmax_rows(rows), np.int32)
