@@ -89,7 +89,9 @@ enum {
     SPEC_ST_BAD_TOKEN = 2,       /* draft token outside [0, V)              */
     SPEC_ST_BAD_GAMMA = 4,       /* gamma_b outside [0, G]                  */
     SPEC_ST_ZERO_RESIDUAL = 8,   /* residual mass rounded to 0: drew from p */
-    SPEC_ST_GUARDED = 16,        /* reserved: never set by this version     */
+    SPEC_ST_GUARDED = 16,        /* informational: a near-tie draw was taken
+                                    again in extended precision; the outputs
+                                    are valid                                */
     SPEC_ST_TIMEOUT = 32,        /* an internal wait hit its time limit     */
     SPEC_ST_BAD_TEMPERATURE = 64,/* temperature <= 0 or not finite          */
     SPEC_ST_BAD_UNIFORM = 128    /* a uniform that was used is not in [0,1) */
@@ -97,7 +99,8 @@ enum {
 
 /* Limits checked by the host: 1 <= B <= 65535, 0 <= G <= 31, 2 <= V < 2^28,
  * and the internal work and queue counts (B (2G+1) ceil(V / 16384) chunks,
- * B (2 ceil(V / 4096) + 2) draw entries) below 2^31; no device could hold
+ * B (4 ceil(V / 4096) + 2 G ceil(V / 16384) + 2) dynamic-queue entries)
+ * below 2^31; no device could hold
  * the logits of sizes past those. */
 #define SPEC_MAX_B 65535
 #define SPEC_MAX_G 31
@@ -185,7 +188,7 @@ int spec_draft_signals(const void* draft_logits, int dtype, int B, int G, int V,
 
 /* Size of the library-owned scratch used by spec_verify_sample_static: 8 MiB.
  * It holds the workspace of spec_workspace_bytes(B, G, V) <= this value, e.g.
- * B <= 509 at G = 8, V = 151936, or B <= 527 at G = 7, V = 151936. */
+ * B <= 268 at G = 8, V = 151936, or B <= 276 at G = 7, V = 151936. */
 #define SPEC_STATIC_WORKSPACE_BYTES (8u << 20)
 
 /* spec_verify_sample without a caller workspace.  The pages have no

@@ -16,7 +16,7 @@ CSRC = os.path.join(HERE, "csrc")
 OBJ = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libspec_verify.so")
 SOURCES = ["api.cu", "verify.cu"]
-HEADERS = ["common.cuh", os.path.join("..", "..", "include", "spec_verify.h")]
+HEADERS = ["common.cuh", "exp2_table.cuh", os.path.join("..", "..", "include", "spec_verify.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          "--expt-relaxed-constexpr", "-Xptxas", "-warn-spills"]

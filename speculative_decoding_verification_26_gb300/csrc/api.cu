@@ -75,8 +75,7 @@ bool sizes_ok(int B, int G, int V) {
   const long long ce = chunk_elems(SPEC_F32), se = stage_elems(SPEC_F32);
   const long long rows = (long long)B * (2 * G + 1);
   const long long nch = (V + ce - 1) / ce, nres = (V + se - 1) / se;
-  return rows * nch < (1ll << 31) && (long long)B * (2 * nres + 2) < (1ll << 31) &&
-         (long long)B * G * nch < (1ll << 31);
+  return rows * nch < (1ll << 31) && (long long)B * (kMaxDrawRounds * nres + 2 * G * nch + 2) < (1ll << 31);
 }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -138,6 +137,8 @@ int run(const Call& c) {
   P.known_reject = reinterpret_cast<int*>(ws + L.known_reject);
   P.row_list = reinterpret_cast<int*>(ws + L.row_list);
   P.req_scale = reinterpret_cast<float*>(ws + L.req_scale);
+  P.req_scale_lo = reinterpret_cast<float*>(ws + L.req_scale_lo);
+  P.req_ks = reinterpret_cast<float*>(ws + L.req_ks);
   P.req_gam = reinterpret_cast<int*>(ws + L.req_gam);
   P.req_status = reinterpret_cast<int*>(ws + L.req_status);
   P.req_fin = reinterpret_cast<unsigned*>(ws + L.req_fin);
@@ -146,8 +147,17 @@ int run(const Call& c) {
   P.gsum = reinterpret_cast<tword*>(ws + L.gsum);
   P.dd = reinterpret_cast<tword*>(ws + L.dd);
   P.dq = reinterpret_cast<tword*>(ws + L.dq);
+  P.claim = reinterpret_cast<tword*>(ws + L.claim);
   P.defq = reinterpret_cast<tword*>(ws + L.defq);
   P.nrows = L.nrows; P.nch = L.nch; P.nres = L.nres; P.dq_cap = L.dq_cap; P.def_cap = L.def_cap;
+  // Lookahead: greedy and sample calls read every row in position-major order
+  // and skip the rows past a decided reject (a dependency per position, a
+  // read issued only once the position before is accepted, would put a full
+  // pipeline latency on every step of a long chain).  A one-hot call reads
+  // the target rows of positions 0 and 1 up front and the row of position
+  // i + 2 once position i is accepted (its drafts are rejected early: most
+  // later rows are not needed).
+  P.lookahead = c.mode == MODE_ONEHOT ? 2 : c.G + 1;
   P.aligned_rows = ((size_t)c.V * es) % 16 == 0 && aligned(c.target, 16) && aligned(c.draft, 16);
   P.wait_limit = g_wait_limit.load(std::memory_order_relaxed);
   // Rows a draw may read again (positions 0 .. keep_pos, both models in the
@@ -231,7 +241,7 @@ const char* spec_request_status_string(int bit) {
     case SPEC_ST_BAD_TOKEN: return "draft token outside [0, V)";
     case SPEC_ST_BAD_GAMMA: return "gamma outside [0, G]";
     case SPEC_ST_ZERO_RESIDUAL: return "residual mass rounded to zero; drew from p";
-    case SPEC_ST_GUARDED: return "reserved (never set)";
+    case SPEC_ST_GUARDED: return "near-tie draw taken again in extended precision (informational)";
     case SPEC_ST_TIMEOUT: return "internal wait timed out";
     case SPEC_ST_BAD_TEMPERATURE: return "temperature not positive and finite";
     case SPEC_ST_BAD_UNIFORM: return "uniform outside [0, 1)";

@@ -33,9 +33,18 @@ enum ItemType : int {
   IT_DSUM = 2,     // one 16 KB slice of the draw's weights: group sums
 };
 
-// draw kinds: the residual [p_k - q_k]_+ (rows k of both models), or p of
-// target row k (bonus draw; one-hot residual with the draft token removed)
-enum DrawKind : int { DK_RESID = 1, DK_P = 2 };
+// draw kinds (one round of a draw each):
+//   DK_RESID   the residual [p_k - q_k]_+ (rows k of both models) with fp32
+//              weights and the streaming row sums;
+//   DK_P       2^{a} of target row k in extended precision (bonus draw;
+//              one-hot residual with the draft token removed);
+//   DK_SUMS    the extended-precision row sums S_p, S_q of rows k (first
+//              round of a residual draw taken again in extended precision);
+//   DK_PRESID  [p_k - q_k]_+ in extended precision with S_p, S_q from DK_SUMS;
+//   DK_PF      2^{a} of target row k with fp32 weights (first round of a
+//              bonus or one-hot draw; taken again as DK_P near a tie).
+enum DrawKind : int { DK_RESID = 1, DK_P = 2, DK_SUMS = 3, DK_PRESID = 4, DK_PF = 5 };
+constexpr int kMaxDrawRounds = 4;   // residual, sums, extended residual, p after zero mass
 
 
 // ---------------------------------------------------------------------------
@@ -43,19 +52,21 @@ enum DrawKind : int { DK_RESID = 1, DK_P = 2 };
 
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
-constexpr int kEpiWarps = 2;                           // epilogue warps (items alternate)
-constexpr int kStatsThreads = kConsumerThreads + 32 * (2 + kEpiWarps);   // + producer, epilogue, owner warps
+constexpr int kEpiWarps = 1;                           // epilogue warps (items alternate)
+constexpr int kStatsThreads = kConsumerThreads + 32 * (3 + kEpiWarps);   // + producer, scheduler, epilogue, owner warps
 constexpr int kStageBytes = 16384;                      // one bulk copy
-constexpr int kStages = 6;                              // ring depth per CTA
+constexpr int kStages = 4;                              // ring depth per CTA
 constexpr int kChunkBytes = 4 * kStageBytes;            // one work item of a row
 constexpr int kEpiSlots = 12;                           // consumer -> epilogue ring (multiple of kEpiWarps)
 constexpr int kGroupVecs = 32;                          // draw group: one warp's 32 vectors (256 bf16 / 128 fp32 tokens)
 constexpr int kGroupsPerStage = kStageBytes / 16 / kGroupVecs;   // 32
 constexpr int kPartWords = 3;                           // tagged words of a chunk partial: m, s (argmax: idx), t
-constexpr int kDrawWords = 8;                           // tagged words of a draw descriptor
+constexpr int kDrawWords = 12;                          // tagged words of a draw descriptor
+constexpr int kSliceWords = 4;                          // tagged words of a draw slice's sums (two fp64)
+constexpr int kGroupWords = 2;                          // tagged words of a draw group sum (one fp64)
 constexpr int kNoReject = 0x7fffffff;
-constexpr unsigned kEpochMax = 0x3ffffff0u;             // tags come from 4 * epoch + kind (kind < 4)
-// Tags are (4 * epoch + kind) * kTagMul: an odd multiplier is a bijection of
+constexpr unsigned kEpochMax = 0x1ffffff0u;             // tags come from 8 * epoch + kind (kind < 8)
+// Tags are (8 * epoch + kind) * kTagMul: an odd multiplier is a bijection of
 // the 32-bit integers that maps 0 to 0 only, and sends the small integers an
 // epoch starts from to values that stale data (counts, indices, tokens) does
 // not hold.
@@ -72,7 +83,7 @@ constexpr long long kWaitLimitCycles = 4000000000ll;
 
 // ---------------------------------------------------------------------------
 // partial statistics of a run of logits, relative to the exponent reference
-// R(m) = fl(m c) of its own max m (see ref_of), with a = fl(x c - R(m)):
+// R(m) = fl(m c) of its own max m (see ref_of), with a = stretch(fl(x c - R(m)), k):
 //   s = sum 2^a,  t = sum a 2^a  (entropy numerator),
 //   idx = lowest index attaining m,  bad = a NaN was seen (argmax mode).
 struct alignas(16) Part {
@@ -90,12 +101,12 @@ struct alignas(16) RowStats {
 // workspace layout (offsets in bytes, 256-aligned)
 
 struct Layout {
-  size_t hdr, req_flags, known_reject, row_list, req_scale, req_gam, req_status, req_fin, cparts, dsum, gsum, dd, dq,
-      defq, total;
+  size_t hdr, req_flags, known_reject, row_list, req_scale, req_scale_lo, req_ks, req_gam, req_status, req_fin, cparts,
+      dsum, gsum, dd, dq, claim, defq, total;
   int nrows;      // B*(G+1) + B*G row ids
   int nch;        // statistics chunks per row
   int nres;       // draw slices per row (one stage each)
-  int dq_cap;     // dynamic queue capacity
+  int dq_cap;     // dynamic queue capacity: every draw round and lookahead row
   int def_cap;    // deferred queue capacity (statistics items of draft rows)
 };
 
@@ -114,19 +125,23 @@ struct Header {
   Counter def_tail;     // deferred static items reserved
   Counter done;         // requests whose outputs are written
   Counter error;        // SPEC_ST_TIMEOUT when any wait gave up
-  Counter misc;         // n_items, n_valid, exited, n_uncertain, epoch, magic (rarely written)
+  Counter misc;         // n_items, n_valid, exited, n_uncertain, epoch, n_front, magic, generation, owner (rarely written)
 };
 #define HDR_N_ITEMS(h) ((h)->misc.pad[0])
 #define HDR_N_VALID(h) ((h)->misc.pad[1])
 #define HDR_EXITED(h) ((h)->misc.pad[2])
 #define HDR_UNCERTAIN(h) ((h)->misc.pad[3])
 #define HDR_EPOCH(h) ((h)->misc.pad[4])
+#define HDR_N_FRONT(h) ((h)->misc.pad[5])   // static items of the first positions
 #define HDR_MAGIC(h) (*reinterpret_cast<unsigned long long*>(&(h)->misc.pad[7]))   // byte offset 32: 8-aligned
 #define HDR_GEN(h) (*reinterpret_cast<unsigned long long*>(&(h)->misc.pad[9]))     // byte offset 40: 8-aligned
+// the address of the call counter of the library copy that last used the
+// workspace (two copies of the library in one process count calls apart)
+#define HDR_OWNER(h) (*reinterpret_cast<unsigned long long*>(&(h)->misc.pad[11]))   // byte offset 48: 8-aligned
 
 // Data that crosses CTAs travels in tagged 64-bit words: payload in the high
-// 32 bits, the tag in the low 32 bits: (4 * epoch) * kTagMul for chunk
-// partials and queue entries, (4 * epoch + 1 + round) * kTagMul for the words
+// 32 bits, the tag in the low 32 bits: (8 * epoch) * kTagMul for chunk
+// partials and queue entries, (8 * epoch + 1 + round) * kTagMul for the words
 // of a draw round (one tag space per kind of word).  An aligned 64-bit
 // relaxed access is single-copy atomic, so a reader that sees the current tag
 // has the payload written in this call, whatever the order in which words
@@ -148,7 +163,9 @@ __host__ inline Layout make_layout(int B, int G, int V, int dtype) {
   L.nrows = nrows;
   L.nch = (V + ce - 1) / ce;
   L.nres = (V + se - 1) / se;
-  L.dq_cap = B * (2 * L.nres + 2);   // a draw restarted once after zero mass
+  // every round of every draw, and the chunks of every lookahead row (target
+  // rows 2..G and, without signals, draft rows 2..G-1 of each request)
+  L.dq_cap = B * (kMaxDrawRounds * L.nres + 2 * G * L.nch + 2);
   L.def_cap = B * G * L.nch;
   size_t o = 0;
   L.hdr = o;          o = align256(o + sizeof(Header));
@@ -156,14 +173,17 @@ __host__ inline Layout make_layout(int B, int G, int V, int dtype) {
   L.known_reject = o; o = align256(o + sizeof(int) * B);
   L.row_list = o;     o = align256(o + sizeof(int) * nrows);
   L.req_scale = o;    o = align256(o + sizeof(float) * B);
+  L.req_scale_lo = o; o = align256(o + sizeof(float) * B);
+  L.req_ks = o;       o = align256(o + sizeof(float) * B);
   L.req_gam = o;      o = align256(o + sizeof(int) * B);
   L.req_status = o;   o = align256(o + sizeof(int) * B);
   L.req_fin = o;      o = align256(o + sizeof(unsigned) * B);
   L.cparts = o;       o = align256(o + sizeof(tword) * (size_t)nrows * L.nch * kPartWords);
-  L.dsum = o;         o = align256(o + sizeof(tword) * 2 * (size_t)B * L.nres);
-  L.gsum = o;         o = align256(o + sizeof(tword) * (size_t)B * L.nres * kGroupsPerStage);
+  L.dsum = o;         o = align256(o + sizeof(tword) * kSliceWords * (size_t)B * L.nres);
+  L.gsum = o;         o = align256(o + sizeof(tword) * (size_t)B * L.nres * kGroupsPerStage * kGroupWords);
   L.dd = o;           o = align256(o + sizeof(tword) * kDrawWords * (size_t)B);
   L.dq = o;           o = align256(o + sizeof(tword) * 2 * (size_t)L.dq_cap);
+  L.claim = o;        o = align256(o + sizeof(tword) * (size_t)B * G * L.nch);
   L.defq = o;         o = align256(o + sizeof(tword) * (size_t)L.def_cap);
   L.total = o;
   return L;
@@ -194,17 +214,21 @@ struct Params {
   int* req_flags;                // error bits found by the plan kernel
   int* known_reject;             // earliest decided reject (early exit), relaxed
   int* row_list;                 // position-major row schedule
-  float* req_scale;              // log2(e) / T_b (plan kernel)
+  float* req_scale;              // log2(e) / T_b rounded to fp32 (plan kernel)
+  float* req_scale_lo;           // log2(e) / T_b - req_scale, rounded to fp32 (extended-precision draws)
+  float* req_ks;                 // scale_k(req_scale, req_scale_lo): the exponent stretch (see ref_of)
   int* req_gam;                  // gamma_b (plan kernel)
   int* req_status;               // kFinished: settled by the plan kernel
   unsigned* req_fin;             // tag of the call whose outputs were written
   tword* cparts;                 // [nrows][nch][kPartWords] chunk partials
-  tword* dsum;                   // [B][nres][2] draw slice sums (fp64 as hi, lo)
-  tword* gsum;                   // [B][nres][kGroupsPerStage] draw group sums (fp32)
+  tword* dsum;                   // [B][nres][kSliceWords] draw slice sums (one or two fp64 as hi, lo words)
+  tword* gsum;                   // [B][nres][kGroupsPerStage][kGroupWords] draw group sums (fp64)
   tword* dd;                     // [B][kDrawWords] draw descriptors
-  tword* dq;                     // [dq_cap][2] dynamic work queue
-  tword* defq;                   // [def_cap] deferred statistics items (item index)
+  tword* dq;                     // [dq_cap][2] dynamic work queue (draw slices, lookahead row chunks)
+  tword* claim;                  // [B][G][nch] draft-row chunks taken (a static item and a lookahead entry race for them)
+  tword* defq;                   // [def_cap] deferred static items (main-queue index): signal-only draft rows
   int nrows, nch, nres, dq_cap, def_cap;
+  int lookahead;                 // target rows of positions >= lookahead are read once position - lookahead is accepted
 };
 
 // row ids: target rows first, then draft rows
@@ -352,8 +376,9 @@ __device__ __forceinline__ float load_logit(const unsigned char* base, int dtype
   return __ldg(reinterpret_cast<const float*>(base) + elem);
 }
 
-// log2(e) / T, rounded once to fp32 (the scale used by every kernel)
-__device__ __forceinline__ float scale_of(float T) { return (float)(1.4426950408889634 / (double)T); }
+// log2(e) / T rounded toward zero to fp32 (the scale used by every kernel;
+// the remainder, >= 0, is carried separately: see ref_of)
+__device__ __forceinline__ float scale_of(float T) { return __double2float_rz(1.4426950408889634 / (double)T); }
 
 __device__ __forceinline__ bool temperature_ok(float T) { return T > 0.f && isfinite(T); }
 
@@ -366,17 +391,27 @@ __device__ __forceinline__ bool row_ok(const RowStats& r, bool argmax_mode) {
 }
 
 // The exponent reference of a run of logits with max m at scale c: every
-// term of its sums is 2^{fl(x c - R(m))} with R(m) = fl(m c), rounded once,
-// and every rescale between two runs uses R(m1) - R(m2).  So all sums of a
-// row, the probability of one token and the draw weights refer to the same
-// R(m) of the row max and their ratios do not depend on how m c rounds (at
-// |m c| ~ 500, half an ulp of m c is 3e-5 in the exponent).
+// term of its sums is 2^a with a = fl(a0 + a0 k), a0 = fl(x c - R(m)),
+// R(m) = fl(m c).  c is log2(e) / T rounded toward zero to fp32 and
+// c (1 + k) = c + c_lo is that scale to about 48 bits: a0 (1 + k) =
+// x (c + c_lo) - R(m) (1 + k), so k corrects the fp32 rounding of c (which
+// would otherwise temper every row by up to 1e-7 of its exponents) up to a
+// constant of the row.  Every rescale between two runs uses
+// d (1 + k), d = R(m1) - R(m2).  So all sums of a row, the probability of one
+// token and the draw weights refer to the same reference of the row max (a
+// common offset of every exponent of the row, which cancels in every ratio)
+// and do not depend on how m c rounds (at |m c| ~ 500, half an ulp of m c is
+// 3e-5 in the exponent).  k > 0, so a logit of -inf keeps the exponent -inf.
 __device__ __forceinline__ float ref_of(float m, float c) { return __fmul_rn(m, c); }
+__device__ __forceinline__ float scale_k(float c, float c_lo) {
+  return c > 0.f ? fmaxf(__fdiv_rn(c_lo, c), 1e-30f) : 0.f;
+}
+__device__ __forceinline__ float stretch(float a, float k) { return __fmaf_rn(a, k, a); }
 
 // Merge of two partials of the same row (online-softmax rule):
-//   m = max(m1, m2); s = sum_j s_j 2^{d_j}, d_j = R(m_j) - R(m);
+//   m = max(m1, m2); s = sum_j s_j 2^{d_j}, d_j = (R(m_j) - R(m)) (1 + k);
 //   t = sum_j 2^{d_j}(t_j + d_j s_j).
-__device__ __forceinline__ Part merge_parts(const Part& a, const Part& b, float c, bool ent) {
+__device__ __forceinline__ Part merge_parts(const Part& a, const Part& b, float c, float k, bool ent) {
   Part r;
   const float m = fmaxf(a.m, b.m);
   r.m = m;
@@ -386,13 +421,13 @@ __device__ __forceinline__ Part merge_parts(const Part& a, const Part& b, float 
     const float rm = ref_of(m, c);
     float sa = 0.f, ta = 0.f, sb = 0.f, tb = 0.f;
     if (a.s != 0.f) {
-      const float d = __fsub_rn(ref_of(a.m, c), rm);
+      const float d = stretch(__fsub_rn(ref_of(a.m, c), rm), k);
       const float f = ex2(d);
       sa = a.s * f;
       if (ent) ta = f * fmaf(d, a.s, a.t);
     }
     if (b.s != 0.f) {
-      const float d = __fsub_rn(ref_of(b.m, c), rm);
+      const float d = stretch(__fsub_rn(ref_of(b.m, c), rm), k);
       const float f = ex2(d);
       sb = b.s * f;
       if (ent) tb = f * fmaf(d, b.s, b.t);

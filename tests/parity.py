@@ -104,12 +104,14 @@ class Tally:
         self.decisions = 0
         self.flagged = 0
         self.disagree = 0
+        self.guarded = 0           # draws taken again in extended precision (GPU status bit)
         self.notes = []
 
     def __repr__(self):
         n = max(self.decisions, 1)
         return (f"decisions={self.decisions} flagged={self.flagged} ({self.flagged / n:.3%}) "
-                f"disagreements={self.disagree} ({self.disagree / n:.4%}, budget {BUDGET:.2%})"
+                f"disagreements={self.disagree} ({self.disagree / n:.4%}, budget {BUDGET:.2%}) "
+                f"guarded={self.guarded}"
                 + (f" {self.notes[:3]}" if self.notes else ""))
 
     def within_budget(self):
@@ -120,6 +122,7 @@ def compare(o, mode, wl, g, ref, tally: Tally, *, check_signals=True, gamma=True
     """Compare GPU outputs g with oracle outputs ref; raises AssertionError on
     any difference the comparison rule does not allow."""
     B, G = wl.B, wl.G
+    tally.guarded += int(np.count_nonzero(g["status"] & GUARDED))
     st_g = g["status"] & ~GUARDED
     np.testing.assert_array_equal(st_g, ref["status"], err_msg="status")
     alt_probe = np.full(B, -1, np.int32)

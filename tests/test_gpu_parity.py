@@ -264,8 +264,8 @@ def test_single_request(o, dev):
 def test_stale_words_in_reused_memory(o, dev):
     """Memory a workspace takes over may hold small integers left by earlier
     tensors or calls.  Here every word after the header is overwritten with a
-    value whose low half is 4 * (e + 1) (+ 0..3), the tag an epoch counted per
-    workspace would use on the next call, and a payload of 1 (in range as a
+    value whose low half is 8 * (e + 1) (+ 0..7), the unscrambled tag an epoch
+    counted per workspace would use on the next call, and a payload of 1 (in range as a
     request, slice, item or chunk index, so a word taken by mistake reads no
     memory out of bounds); the next call must not take any of them for its
     own partials, queue entries or draw words (tags are scrambled and epochs
@@ -286,7 +286,7 @@ def test_stale_words_in_reused_memory(o, dev):
         epoch = int(ws[7 * 128 + 4 * 5: 7 * 128 + 4 * 6].view(torch.int32).item())
         words = ws[1024:(ws.numel() // 8) * 8].view(torch.int64)
         idx = torch.arange(words.numel(), device=dev, dtype=torch.int64)
-        words.copy_((1 << 32) | (4 * (epoch + 1) + (idx % 4)))
+        words.copy_((1 << 32) | (8 * (epoch + 1) + (idx % 8)))
         r = sv.verify_sample(*args, signals=True, accept_prob=True, ws=ws)
         torch.cuda.synchronize()
         g = {k: v.cpu().numpy() for k, v in r.items()}
