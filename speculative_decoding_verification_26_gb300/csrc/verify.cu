@@ -50,8 +50,8 @@ constexpr int kFinished = 1 << 30;                 // req_status: outputs writte
 // move a bucket edge by a few 1e-8 W (modelled on the kernel's roundings of
 // the residual for the bench workloads: at most 5e-8 W with the scale carried
 // as c + c_lo; a p draw has the same exponent and fewer roundings); the
-// guard is six times that.
-constexpr float kDrawGuard = 3e-7f;
+// guard is three times that.
+constexpr float kDrawGuard = 1.5e-7f;
 
 __device__ __forceinline__ float qnan() { return __int_as_float(0x7fc00000); }
 
@@ -346,10 +346,10 @@ struct WorkEntry {
   int rid, chunk;                   // WT_ROW: row id, chunk; WT_DRAW: request b, slice
   float c, ks;                      // WT_ROW: the request's scale and stretch
   unsigned tag;                     // WT_DRAW: the round's tag
+  int urgent;                       // WT_DRAW: a round after the first (a retake)
   unsigned v[kDrawWords];           // WT_DRAW: the round's descriptor words
 };
 constexpr int kFifo = 1;            // row chunks handed over ahead of the producer (claimed late: a decided reject skips more)
-constexpr int kDeferMax = 64;       // deferred items per CTA (more are read in place)
 
 struct __align__(128) VSmem {
   unsigned char ring[kStages][kStageBytes];
@@ -363,7 +363,6 @@ struct __align__(128) VSmem {
   float2 exp2tab[256];              // 2^{i/256} as hi, lo (extended-precision draws)
   WorkEntry fifo[kFifo];            // scheduler -> producer: row chunks (and the end marker)
   WorkEntry prio;                   // scheduler -> producer: one draw slice
-  int defer[kDeferMax];             // this CTA's deferred static items (main-queue index)
   int fifo_head, fifo_tail, prio_full;
   long long wait_limit;             // Params::wait_limit, for the waits that see only S
   int abort;
@@ -871,7 +870,9 @@ __device__ __forceinline__ void st_vol(int* p, int v) { *reinterpret_cast<volati
 // one draw slice) and issues the bulk copies into the ring.  It never waits
 // on global memory, so the ring stays full.  Draw slices and row chunks take
 // turns: the rows of the positions still open are the longest chain of the
-// call, while a draw started early has time to spare.
+// call, while a draw started early has time to spare.  A retake round (a
+// draw taken again near a tie) goes first, also between the stages of a row
+// chunk: it is on the critical path of its request.
 template <int DT, bool GREEDY>
 __device__ __forceinline__ void producer_role(const Params& P, VSmem& S) {
   int stage = 0;
@@ -889,7 +890,7 @@ __device__ __forceinline__ void producer_role(const Params& P, VSmem& S) {
   bool last_row = true;
   while (ok) {
     const bool rows = ld_vol(&S.fifo_tail) != head;
-    if (ld_vol(&S.prio_full) && (last_row || !rows)) {
+    if (ld_vol(&S.prio_full) && (last_row || !rows || ld_vol(&S.prio.urgent))) {
       take_prio();
       last_row = false;
       idle_since = -1;
@@ -904,7 +905,9 @@ __device__ __forceinline__ void producer_role(const Params& P, VSmem& S) {
       r.rid = e.rid; r.chunk = e.chunk; r.c = e.c; r.ks = e.ks;
       __threadfence_block();
       st_vol(&S.fifo_head, ++head);
-      ok = stage_row_item<DT, GREEDY>(P, S, stage, phase, r, islot++ & (kItemSlots - 1), [&]() {});
+      ok = stage_row_item<DT, GREEDY>(P, S, stage, phase, r, islot++ & (kItemSlots - 1), [&]() {
+        if (ok && ld_vol(&S.prio_full) && ld_vol(&S.prio.urgent)) take_prio();
+      });
       idle_since = -1;
       continue;
     }
@@ -938,9 +941,9 @@ __device__ __forceinline__ void producer_role(const Params& P, VSmem& S) {
 // an atomic: a dynamic entry at its ticket (a draw slice goes to the
 // priority slot with its round's descriptor, a lookahead row chunk to the
 // FIFO), else a static item (position-major main queue; a decided reject
-// voids the row, and a draft row that only the signals still need is
-// deferred to the end, in this CTA's list, so the rows of live requests go
-// first), else the deferred items.  It ends the producer with a WT_TERM entry
+// voids the row, and a draft row that only the signals still need goes to
+// the deferred queue, shared by all CTAs, so the rows of live requests go
+// first), else a deferred item.  It ends the producer with a WT_TERM entry
 // once no work can come any more.
 template <int DT, bool GREEDY>
 __device__ __forceinline__ void scheduler_role(const Params& P, VSmem& S, unsigned epoch) {
@@ -952,7 +955,7 @@ __device__ __forceinline__ void scheduler_role(const Params& P, VSmem& S, unsign
   const bool defer_on = dyn && P.mode == MODE_SAMPLE && P.signals_on;
   unsigned ticket = dyn ? atomicAdd(&P.hdr->dq_head.v, 1u) : 0xffffffffu;
   bool main_done = n_items == 0u;
-  int n_def = 0, def_next = 0;
+  unsigned dticket = 0xffffffffu;     // deferred-queue ticket whose entry is not seen yet
   int tail = 0;
   bool ok = true;
   auto room = [&]() { return tail - ld_vol(&S.fifo_head) < kFifo; };
@@ -1003,7 +1006,7 @@ __device__ __forceinline__ void scheduler_role(const Params& P, VSmem& S, unsign
             if (aborted(S) || clock64() - c0 > P.wait_limit) { ok = false; break; }
           }
           if (!ok) break;
-          e.type = WT_DRAW; e.rid = b; e.chunk = slice; e.tag = tag;
+          e.type = WT_DRAW; e.rid = b; e.chunk = slice; e.tag = tag; e.urgent = round > 0;
           __threadfence_block();
           st_vol(&S.prio_full, 1);
           ticket = atomicAdd(&P.hdr->dq_head.v, 1u);
@@ -1023,20 +1026,34 @@ __device__ __forceinline__ void scheduler_role(const Params& P, VSmem& S, unsign
           decode_row(rid, P.B, P.G, kind, b, i);
           bool take = true;
           if (ld_relaxed(P.known_reject + b) < i) {    // decided reject: the signals may still need the row
-            if (!(kind == KIND_DRAFT && P.signals_on)) take = false;
-            else if (defer_on && n_def < kDeferMax) { S.defer[n_def++] = (int)q; take = false; }
+            if (!(kind == KIND_DRAFT && P.signals_on)) {
+              take = false;
+            } else if (defer_on) {                       // to the deferred queue (all CTAs share it)
+              const unsigned slot = atomicAdd(&P.hdr->def_tail.v, 1u);
+              if (slot < (unsigned)P.def_cap) {
+                st_tw(P.defq + slot, tw_make(q, ptag));
+                take = false;
+              }
+            }
           }
           if (take && claim_chunk(P, kind, b, i, chunk, ptag)) push_row(rid, chunk);
           did = true;
         }
       }
-      if (!did && main_done && def_next < n_def) {
-        const unsigned q = (unsigned)S.defer[def_next++];
-        const int rid = __ldg(P.row_list + q / (unsigned)P.nch), chunk = (int)(q % (unsigned)P.nch);
-        int kind, b, i;
-        decode_row(rid, P.B, P.G, kind, b, i);
-        if (claim_chunk(P, kind, b, i, chunk, ptag)) push_row(rid, chunk);
-        did = true;
+      if (!did && main_done && defer_on) {
+        if (dticket == 0xffffffffu) dticket = atomicAdd(&P.hdr->def_head.v, 1u);
+        if (dticket < (unsigned)P.def_cap) {
+          const tword w = ld_tw(P.defq + dticket);
+          if (tw_ok(w, ptag)) {
+            const unsigned q = tw_u32(w);
+            dticket = 0xffffffffu;
+            const int rid = __ldg(P.row_list + q / (unsigned)P.nch), chunk = (int)(q % (unsigned)P.nch);
+            int kind, b, i;
+            decode_row(rid, P.B, P.G, kind, b, i);
+            if (claim_chunk(P, kind, b, i, chunk, ptag)) push_row(rid, chunk);
+            did = true;
+          }
+        }
       }
     }
     if (did) {
@@ -1046,7 +1063,7 @@ __device__ __forceinline__ void scheduler_role(const Params& P, VSmem& S, unsign
     }
     // 3. nothing to hand over right now: finished, or dynamic items are
     // still to come (calls without them are finished with the static items)
-    if (main_done && def_next >= n_def && (!dyn || ld_relaxed_u32(&P.hdr->done.v) >= n_valid)) break;
+    if (main_done && (!dyn || ld_relaxed_u32(&P.hdr->done.v) >= n_valid)) break;
     if (ld_relaxed_u32(&P.hdr->error.v) != 0u || aborted(S)) break;
     const long long now = clock64();
     if (idle_since < 0) idle_since = now;
@@ -2332,32 +2349,38 @@ __device__ void serve_request(const Params& P, int b, unsigned epoch, int lane) 
     if (GREEDY || y < 0 || y >= P.V) return qnan();
     return load_logit(kind == KIND_TARGET ? P.target : P.draft, DT, row_elem_offset(kind, b, i, G, P.V) + y);
   };
+  // the draft tokens and x_y of every position, loaded once (lane i holds
+  // position i; G <= 31): no step of the position loop waits on them
+  int y_lane = -1;
+  float xt_lane = qnan(), xd_lane = qnan();
+  if (P.mode != MODE_SIGNALS && lane < gam) {
+    y_lane = P.draft_tokens[(size_t)b * G + lane];
+    xt_lane = logit_at(KIND_TARGET, lane, y_lane);
+    if (sample) xd_lane = logit_at(KIND_DRAFT, lane, y_lane);
+  }
   bool bonus = false;                         // the bonus row is merged (into rt)
   if (P.mode != MODE_SIGNALS && P.nch <= 8) {
     // position i, and position i+1 (or the bonus row) too when its rows are
     // already complete: an owner behind the stream catches up two at a time
     for (int i = 0; i < gam;) {
       const int i1 = i + 1;
-      const int y0 = P.draft_tokens[(size_t)b * G + i];
-      const int y1 = i1 < gam ? P.draft_tokens[(size_t)b * G + i1] : -1;
+      const int y0 = __shfl_sync(0xffffffffu, y_lane, i);
+      const int y1 = __shfl_sync(0xffffffffu, y_lane, i1 & 31);
       const int seg = lane >> 3;
       int rid = -1;
       if (seg == 0) rid = target_row_id(b, i, G);
       else if (seg == 1) rid = sample ? draft_row_id(b, i, B, G) : -1;
       else if (seg == 2) rid = i1 <= gam ? target_row_id(b, i1, G) : -1;
       else rid = (sample && i1 < gam) ? draft_row_id(b, i1, B, G) : -1;
-      // x_y of the four rows, in flight while the partials are polled
-      float xl = qnan();
-      if (lane == 0) xl = logit_at(KIND_TARGET, i, y0);
-      else if (lane == 1 && sample) xl = logit_at(KIND_DRAFT, i, y0);
-      else if (lane == 2 && i1 < gam) xl = logit_at(KIND_TARGET, i1, y1);
-      else if (lane == 3 && sample && i1 < gam) xl = logit_at(KIND_DRAFT, i1, y1);
+      // x_y of the four rows (positions i, i + 1 of target and draft)
+      const float xt0 = __shfl_sync(0xffffffffu, xt_lane, i), xd0 = __shfl_sync(0xffffffffu, xd_lane, i);
+      const float xt1 = __shfl_sync(0xffffffffu, xt_lane, i1 & 31), xd1 = __shfl_sync(0xffffffffu, xd_lane, i1 & 31);
       Part pm;
       const int ready = merge_rows4<GREEDY>(P, rid, (seg & 1) && sig, 3u, c, ks, epoch, lane, pm);
       if (ready < 0) { failed = true; break; }
       auto row_xy = [&](int s2) {
         RowRes o = row_of(pm, s2);
-        o.xy = __shfl_sync(0xffffffffu, xl, s2);
+        o.xy = s2 == 0 ? xt0 : s2 == 1 ? xd0 : s2 == 2 ? xt1 : xd1;
         return o;
       };
       if (!decide(i, y0, row_xy(0), row_xy(1))) break;
@@ -2371,9 +2394,9 @@ __device__ void serve_request(const Params& P, int b, unsigned epoch, int lane) 
     }
   } else if (P.mode != MODE_SIGNALS) {
     for (int i = 0; i < gam; ++i) {
-      const int y = P.draft_tokens[(size_t)b * G + i];
+      const int y = __shfl_sync(0xffffffffu, y_lane, i);
       RowRes T, D{};
-      const float xt = logit_at(KIND_TARGET, i, y), xd = sample ? logit_at(KIND_DRAFT, i, y) : qnan();
+      const float xt = __shfl_sync(0xffffffffu, xt_lane, i), xd = __shfl_sync(0xffffffffu, xd_lane, i);
       if (sample && 2 * P.nch <= 32) {
         if (!merge_pair(P, target_row_id(b, i, G), draft_row_id(b, i, B, G), c, ks, sig, epoch, lane, T, D)) {
           failed = true;
