@@ -414,7 +414,11 @@ def run_ours(args):
             "config": config_dict(sets[0]["host"], world, nsets, F_bytes),
             "roofline": {"bound": "hbm", "kernel": "verify_kernel", "achieved": achieved, "peak": hbm_peak,
                          "unit": "GB/s", "frac": achieved / hbm_peak, "peak_kind": peak_kind,
-                         "traffic": traffic, "algorithmic_bytes_per_launch": N_bytes,
+                         "frac_label": f"of {peak_kind} peak ({hbm_peak:.0f} GB/s copy bandwidth)",
+                         "frac_of_8tbs": achieved / 8000.0, "target_frac": 0.70,
+                         "traffic": traffic,
+                         "dram_gbs": (traffic / t_kern / 1e9) if traffic else None,
+                         "algorithmic_bytes_per_launch": N_bytes,
                          "kernel_ms": t_kern * 1e3},
             "gpu_launches": int(launches),
             "clocks": clocks,
