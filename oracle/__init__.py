@@ -49,6 +49,11 @@ PLANTS = {
     "probe_next_bucket": 13,
     "margin_one_sided": 14,
     "accept_margin_unnormalised": 15,
+    "divergence_nats": 16,
+    "divergence_kl_swapped": 17,
+    "divergence_l1_half": 18,
+    "divergence_a_max": 19,
+    "divergence_entropy_of_q": 20,
 }
 
 _lock = threading.Lock()
@@ -100,6 +105,9 @@ class Oracle:
         f.restype = ctypes.c_int
         self.lib.oracle_plant_id.restype = ctypes.c_int
         self.plant = self.lib.oracle_plant_id()
+        g = self.lib.oracle_divergence
+        g.argtypes = [P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P, P, P, ctypes.c_int]
+        g.restype = ctypes.c_int
 
     def run(self, mode, target=None, draft=None, draft_tokens=None, gamma=None,
             temperature=None, uniforms=None, *, B=None, G=None, V=None,
@@ -172,6 +180,30 @@ class Oracle:
     def draft_signals(self, draft, gamma, temperature, **kw):
         kw.setdefault("want_signals", True)
         return self.run(SIGNALS, draft=draft, gamma=gamma, temperature=temperature, **kw)
+
+    def divergence_stats(self, target, draft, gamma, temperature, *, nthreads=None):
+        """Per-position divergence statistics: target [B, G+1, V] (rows 0..G-1
+        are used), draft [B, G, V]; returns {"stats": [B, G, 5] (A, L1,
+        KL(p||q), KL(q||p), H(p), bits), "status": [B]}."""
+        target = np.ascontiguousarray(target)
+        draft = np.ascontiguousarray(draft)
+        B, G, V = draft.shape
+        if target.shape != (B, G + 1, V):
+            raise ValueError("target must be [B, G+1, V] for draft [B, G, V]")
+        dt = _dtype_code(target)
+        if _dtype_code(draft) != dt:
+            raise TypeError("target and draft dtypes differ")
+        gamma = None if gamma is None else np.ascontiguousarray(gamma, dtype=np.int32)
+        temperature = np.ascontiguousarray(temperature, dtype=np.float32)
+        stats = np.zeros((B, G, 5), np.float64)
+        status = np.zeros(B, np.int32)
+        nthreads = nthreads or os.cpu_count() or 1
+        rc = self.lib.oracle_divergence(_ptr(target, ctypes.c_char), _ptr(draft, ctypes.c_char), dt, B, G, V,
+                                        _ptr(gamma, ctypes.c_int32), _ptr(temperature, ctypes.c_float),
+                                        _ptr(stats, ctypes.c_double), _ptr(status, ctypes.c_int32), int(nthreads))
+        if rc != 0:
+            raise ValueError("oracle_divergence rejected its arguments")
+        return {"stats": stats, "status": status}
 
 
 def load(plant: int = 0, out_dir: str | None = None) -> Oracle:

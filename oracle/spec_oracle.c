@@ -62,6 +62,10 @@
  *   - accept_prob: pinned through A = 1 - TV(p, q) (section 4.3);
  *   - signals: pinned by closed forms (uniform, two-way tie, near one-hot rows)
  *     and by scipy's entropy on random rows;
+ *   - divergence statistics (oracle_divergence): pinned by scipy's entropy
+ *     and relative entropy on random rows, the identities A = 1 - TV and
+ *     L1 = 2 TV, the acceptance probability of the verify path averaged over
+ *     y ~ q, p = q and closed forms (tests);
  *   - the decision margins: accept_margin = |u_i - a_i| (the distance of the
  *     acceptance test of section 3.2 from its threshold), draw_margin (the
  *     distance of t = u W from the nearer edge of the drawn bucket, over W)
@@ -99,6 +103,11 @@
 #define PLANT_PROBE_NEXT_BUCKET 13   /* probe distance to the bucket after it  */
 #define PLANT_MARGIN_ONE_SIDED 14    /* draw margin to the upper edge only     */
 #define PLANT_ACCEPT_MARGIN_UNNORM 15 /* accept margin |u q(y) - p(y)|         */
+#define PLANT_DIV_NATS 16            /* divergence KL and H in nats            */
+#define PLANT_DIV_KL_SWAPPED 17      /* KL(p||q) slot holds KL(q||p)           */
+#define PLANT_DIV_L1_HALF 18         /* L1 slot holds TV = L1 / 2              */
+#define PLANT_DIV_A_MAX 19           /* A = sum max(p, q)                      */
+#define PLANT_DIV_H_DRAFT 20         /* entropy of q instead of p              */
 
 /* dtype codes of the input logits */
 #define ORACLE_F32 0
@@ -536,6 +545,117 @@ int oracle_run(int mode, const void* target, const void* draft, int dtype,
 #pragma omp for schedule(dynamic, 1)
         for (int b = 0; b < B; ++b) {
             if (buf) run_request(&J, b, buf, buf + V, buf + 2 * (size_t)V, buf + 3 * (size_t)V);
+        }
+        free(buf);
+    }
+    return failed ? -1 : 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* per-position divergence statistics                                        */
+
+/* The statistics of one position from its two normalised rows p (target)
+ * and q (draft), sums in ascending token order:
+ *   out[0] = A   = sum_v min(p(v), q(v))  (= 1 - TV(p, q), the expected
+ *                acceptance of the position: tutorial page section 4.3);
+ *   out[1] = L1  = sum_v |p(v) - q(v)|    (= 2 TV; the L1 distance of the
+ *                DLite page's TV loss and of the DDTE page's selector inputs);
+ *   out[2] = KL(p||q) = sum_{p(v)>0} p(v) log2(p(v)/q(v))  (forward KL of the
+ *                DLite page; +inf if some q(v) = 0 < p(v));
+ *   out[3] = KL(q||p), likewise (the DDTE page's "bidirectional KL");
+ *   out[4] = H(p) = -sum_v p(v) log2 p(v)  (target entropy, DDTE page).
+ * Reading: information quantities in bits, as the SpecKV signals. */
+static void divergence_row(const double* p, const double* q, int V, double* out)
+{
+    double A = 0.0, L1 = 0.0, kpq = 0.0, kqp = 0.0, H = 0.0;
+    for (int v = 0; v < V; ++v) {
+        const double a = p[v], b = q[v];
+#if ORACLE_PLANT == PLANT_DIV_A_MAX
+        A += a > b ? a : b;
+#else
+        A += a < b ? a : b;
+#endif
+        L1 += fabs(a - b);
+#if ORACLE_PLANT == PLANT_DIV_NATS
+        if (a > 0.0) kpq += a * log(a / b);
+        if (b > 0.0) kqp += b * log(b / a);
+        if (a > 0.0) H -= a * log(a);
+#else
+        if (a > 0.0) kpq += a * log2(a / b);
+        if (b > 0.0) kqp += b * log2(b / a);
+#if ORACLE_PLANT == PLANT_DIV_H_DRAFT
+        if (b > 0.0) H -= b * log2(b);
+#else
+        if (a > 0.0) H -= a * log2(a);
+#endif
+#endif
+    }
+#if ORACLE_PLANT == PLANT_DIV_L1_HALF
+    L1 *= 0.5;
+#endif
+    out[0] = A;
+    out[1] = L1;
+#if ORACLE_PLANT == PLANT_DIV_KL_SWAPPED
+    out[2] = kqp;
+    out[3] = kpq;
+#else
+    out[2] = kpq;
+    out[3] = kqp;
+#endif
+    out[4] = H;
+}
+
+/* Per-position divergence statistics (the five of divergence_row) of the
+ * target row i and the draft row i of every request, for i < gamma_b, at the
+ * request's temperature; stats [B, G, 5] (NaN past gamma_b, for a position
+ * whose rows are not usable, and for every position of a request with a bad
+ * gamma or temperature); status [B] or NULL: OST_BAD_GAMMA,
+ * OST_BAD_TEMPERATURE, OST_NONFINITE (any position's row unusable).
+ * Layouts as oracle_run.  Returns 0, or -1 on a bad argument or allocation
+ * failure. */
+int oracle_divergence(const void* target, const void* draft, int dtype, int B, int G, int V,
+                      const int32_t* gamma, const float* temperature, double* stats,
+                      int32_t* status, int nthreads)
+{
+    if (B < 0 || G < 0 || V < 1 || dtype < 0 || dtype > 2 || !stats || !temperature) return -1;
+    if (G > 0 && (!target || !draft)) return -1;
+    int failed = 0;
+    if (nthreads < 1) nthreads = 1;
+#pragma omp parallel num_threads(nthreads)
+    {
+        double* buf = (double*)malloc(sizeof(double) * (size_t)V * 3);
+        if (!buf) {
+#pragma omp atomic write
+            failed = 1;
+        }
+#pragma omp for schedule(dynamic, 1)
+        for (int b = 0; b < B; ++b) {
+            if (!buf) continue;
+            double* x = buf;
+            double* p = buf + V;
+            double* q = buf + 2 * (size_t)V;
+            int st = 0;
+            const int gam = gamma ? gamma[b] : G;
+            const double T = (double)temperature[b];
+            if (gam < 0 || gam > G) st |= OST_BAD_GAMMA;
+            if (!(T > 0.0 && isfinite(T))) st |= OST_BAD_TEMPERATURE;
+            for (int i = 0; i < G; ++i) {
+                double* o = stats + ((size_t)b * G + i) * 5;
+                for (int k = 0; k < 5; ++k) o[k] = NAN;
+                if (st != 0 || i >= gam) continue;
+                load_row(target, dtype, (size_t)b * (G + 1) + i, V, x);
+                const int okp = softmax_t(x, V, T, p);
+                load_row(draft, dtype, (size_t)b * G + i, V, x);
+                const int okq = softmax_t(x, V, T, q);
+                if (!okp || !okq) {
+                    st |= OST_NONFINITE;
+                    continue;
+                }
+                divergence_row(p, q, V, o);
+            }
+            if (st & (OST_BAD_GAMMA | OST_BAD_TEMPERATURE))
+                for (int k = 0; k < G * 5; ++k) stats[(size_t)b * G * 5 + k] = NAN;
+            if (status) status[b] = st;
         }
         free(buf);
     }

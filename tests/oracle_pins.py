@@ -493,6 +493,72 @@ def pin_decision_margins(o):
     assert abs(r["accept_margin"][0, 0] - 0.2) < 1e-12
 
 
+def pin_divergence(o):
+    """Per-position divergence statistics (A = sum min(p, q) = 1 - TV(p, q):
+    tutorial section 4.3; L1 and forward KL: the DLite page's distillation
+    losses; bidirectional KL and entropies: the DDTE page's selector inputs),
+    in bits, against facts that do not restate the oracle's sums:
+      - the worked example of section 7: A = 0.6 and L1 = 0.8 by hand, KL both
+        ways and H(p) by scipy's (relative) entropy;
+      - random rows at T = 0.7: KL both ways and H(p) by scipy, A + L1 / 2 = 1
+        (TV = L1 / 2), and A equal to the expected acceptance of the verify
+        path, sum_y q(y) min(1, p(y)/q(y)), from the oracle's accept_prob for
+        every draft token y (a different code path: the acceptance test);
+      - p = q: A = 1, L1 = 0, KL = 0; a uniform target row: H = log2 V;
+      - a draft row with a -inf logit where p > 0: KL(p||q) = +inf, KL(q||p)
+        finite; positions past gamma and bad gamma / temperature: NaN."""
+    g = golden("worked_example.json")
+    pw, qw = np.array(g["p"]), np.array(g["q"])
+    tg = _f64_logits(np.stack([pw, pw]))[None]
+    dr = _f64_logits(qw[None])[None]
+    r = o.divergence_stats(tg, dr, None, np.ones(1, np.float32))
+    st = r["stats"][0, 0]
+    assert abs(st[0] - 0.6) < 1e-12 and abs(st[1] - 0.8) < 1e-12, st
+    assert abs(st[2] - stats.entropy(pw, qw, base=2)) < 1e-12, st
+    assert abs(st[3] - stats.entropy(qw, pw, base=2)) < 1e-12, st
+    assert abs(st[4] - stats.entropy(pw, base=2)) < 1e-12, st
+    # random rows at T = 0.7
+    rng = np.random.default_rng(11)
+    V, T = 40, float(np.float32(0.7))          # the oracle takes T as float32
+    xt = rng.normal(0.0, 2.0, V)
+    xd = xt + rng.normal(0.0, 1.0, V)
+    p = special.softmax(xt / T)
+    q = special.softmax(xd / T)
+    r = o.divergence_stats(np.stack([xt, xt])[None], xd[None, None], None, np.full(1, T, np.float32))
+    st = r["stats"][0, 0]
+    assert abs(st[2] - stats.entropy(p, q, base=2)) < 1e-12, (st[2], stats.entropy(p, q, base=2))
+    assert abs(st[3] - stats.entropy(q, p, base=2)) < 1e-12
+    assert abs(st[4] - stats.entropy(p, base=2)) < 1e-12
+    assert abs(st[0] + st[1] / 2 - 1.0) < 1e-12, st
+    # A against the acceptance test: one request per draft token y
+    ys = np.arange(V, dtype=np.int32)[:, None]
+    acc = o.run(O.SAMPLE, target=np.broadcast_to(np.stack([xt, xt])[None], (V, 2, V)),
+                draft=np.broadcast_to(xd[None, None], (V, 1, V)), draft_tokens=ys,
+                temperature=np.full(V, T, np.float32), uniforms=np.full((V, 2), 0.5, np.float32))["accept_prob"][:, 0]
+    assert abs(st[0] - float(np.dot(q, acc))) < 1e-12, (st[0], float(np.dot(q, acc)))
+    # p = q and a uniform target row
+    r = o.divergence_stats(np.stack([xd, xd])[None], xd[None, None], None, np.full(1, T, np.float32))
+    st = r["stats"][0, 0]
+    assert abs(st[0] - 1.0) < 1e-12 and abs(st[1]) < 1e-12 and abs(st[2]) < 1e-12 and abs(st[3]) < 1e-12, st
+    z = np.zeros(V)
+    st = o.divergence_stats(np.stack([z, z])[None], xd[None, None], None, np.ones(1, np.float32))["stats"][0, 0]
+    assert abs(st[4] - math.log2(V)) < 1e-12, st
+    # a draft zero under target mass
+    xd2 = xd.copy()
+    xd2[3] = -np.inf
+    st = o.divergence_stats(np.stack([xt, xt])[None], xd2[None, None], None, np.ones(1, np.float32))["stats"][0, 0]
+    assert st[2] == np.inf and np.isfinite(st[3]), st
+    # gamma and temperature handling
+    tg3 = np.broadcast_to(np.stack([xt, xt, xt])[None], (3, 3, V))
+    dr3 = np.broadcast_to(np.stack([xd, xd])[None], (3, 2, V))
+    r = o.divergence_stats(tg3, dr3, np.array([1, 3, 2], np.int32), np.array([1.0, 1.0, -1.0], np.float32))
+    s3 = r["stats"]
+    assert np.isfinite(s3[0, 0]).all() and np.isnan(s3[0, 1]).all(), s3[0]
+    assert np.isnan(s3[1]).all() and r["status"][1] == 4, r["status"]
+    assert np.isnan(s3[2]).all() and r["status"][2] == 64, r["status"]
+    assert r["status"][0] == 0
+
+
 ALL_PINS = [
     pin_worked_example,
     pin_worked_example_onehot,
@@ -510,4 +576,5 @@ ALL_PINS = [
     pin_bf16_inputs,
     pin_status_semantics,
     pin_decision_margins,
+    pin_divergence,
 ]
