@@ -642,7 +642,7 @@ int oracle_divergence(const void* target, const void* draft, int dtype, int B, i
             for (int i = 0; i < G; ++i) {
                 double* o = stats + ((size_t)b * G + i) * 5;
                 for (int k = 0; k < 5; ++k) o[k] = NAN;
-                if (st != 0 || i >= gam) continue;
+                if ((st & (OST_BAD_GAMMA | OST_BAD_TEMPERATURE)) || i >= gam) continue;
                 load_row(target, dtype, (size_t)b * (G + 1) + i, V, x);
                 const int okp = softmax_t(x, V, T, p);
                 load_row(draft, dtype, (size_t)b * G + i, V, x);

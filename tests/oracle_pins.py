@@ -557,6 +557,11 @@ def pin_divergence(o):
     assert np.isnan(s3[1]).all() and r["status"][1] == 4, r["status"]
     assert np.isnan(s3[2]).all() and r["status"][2] == 64, r["status"]
     assert r["status"][0] == 0
+    # a row with no finite maximum voids its own position only
+    tg4 = np.stack([xt, xt, xt])[None].copy()
+    tg4[0, 0, :] = -np.inf
+    r = o.divergence_stats(tg4, np.stack([xd, xd])[None], None, np.ones(1, np.float32))
+    assert r["status"][0] == 1 and np.isnan(r["stats"][0, 0]).all() and np.isfinite(r["stats"][0, 1]).all(), r
 
 
 ALL_PINS = [
