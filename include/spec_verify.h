@@ -186,6 +186,34 @@ int spec_draft_signals(const void* draft_logits, int dtype, int B, int G, int V,
                        float* signals, float* row_signals, int32_t* status,
                        void* workspace, size_t workspace_bytes, spec_stream_t stream);
 
+/* Per-position divergence statistics of a draft chain.  For each request b
+ * and position i < gamma_b, with p = softmax(target row i / T_b) and
+ * q = softmax(draft row i / T_b), five fp32 values at stats[(b G + i) 5 + k]:
+ *   k = 0: A = sum_v min(p(v), q(v)), = 1 - TV(p, q), the expected acceptance
+ *          of the position (tutorial page section 4.3);
+ *   k = 1: L1 = sum_v |p(v) - q(v)| (the L1 / TV distance of the DLite page's
+ *          distillation loss and of the DDTE page's selector inputs);
+ *   k = 2: KL(p||q) = sum p log2(p/q)  (forward KL, DLite page), +inf when
+ *          some q(v) = 0 < p(v) (a draft logit of -inf);
+ *   k = 3: KL(q||p) (with k = 2, the DDTE page's bidirectional KL);
+ *   k = 4: H(p) = -sum p log2 p, the target entropy (DDTE page).
+ * All in bits, as the draft signals.  Positions i >= gamma_b give NaN.
+ *   target_logits  [B, G+1, V] (rows 0..G-1 are read), draft_logits [B, G, V],
+ *                  dtype SPEC_F32 or SPEC_BF16, device, caller-owned, read
+ *                  only;
+ *   gamma          [B] int32 or NULL (= G); temperature [B] fp32 (required);
+ *   stats          [B, G, 5] fp32 (required when G > 0), written;
+ *   status         [B] int32 or NULL: zeroed, then SPEC_ST_BAD_GAMMA or
+ *                  SPEC_ST_BAD_TEMPERATURE (every position of the request is
+ *                  NaN) and SPEC_ST_NONFINITE (a position with NaN, +inf or no
+ *                  finite maximum in either row is NaN; the others are valid).
+ * Every row of positions < gamma_b is read twice (the second read mostly
+ * from L2).  No workspace.  Host errors: SPEC_ERR_INVALID_ARG (sizes, dtype,
+ * NULL required pointers, misalignment), SPEC_ERR_CUDA, SPEC_ERR_UNSUPPORTED. */
+int spec_divergence_stats(const void* target_logits, const void* draft_logits, int dtype,
+                          int B, int G, int V, const int32_t* gamma, const float* temperature,
+                          float* stats, int32_t* status, spec_stream_t stream);
+
 /* Size of the library-owned scratch used by spec_verify_sample_static: 8 MiB.
  * It holds the workspace of spec_workspace_bytes(B, G, V) <= this value, e.g.
  * B <= 268 at G = 8, V = 151936, or B <= 276 at G = 7, V = 151936. */

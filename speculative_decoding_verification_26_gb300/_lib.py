@@ -61,6 +61,8 @@ def lib(path: str | None = None) -> ctypes.CDLL:
         L.spec_verify_onehot.argtypes = [P, I, I, I, I, P, P, P, P, P, P, P, P, P, SZ, P]
         L.spec_verify_onehot.restype = I
         L.spec_draft_signals.argtypes = [P, I, I, I, I, P, P, P, P, P, P, SZ, P]
+        L.spec_divergence_stats.argtypes = [P, P, I, I, I, I, P, P, P, P, P]
+        L.spec_divergence_stats.restype = I
         L.spec_draft_signals.restype = I
         if path is None:
             _lib = L
@@ -242,6 +244,29 @@ def verify_onehot(target, draft_tokens, gamma, temperature, uniforms, *, accept_
     if ap is not None:
         r["accept_prob"] = ap
     return r
+
+
+def divergence_stats(target, draft, gamma, temperature, *, out=None):
+    """Per-position divergence statistics.  target [B, G+1, V], draft [B, G, V];
+    returns {"stats": [B, G, 5] (A, L1, KL(p||q), KL(q||p), H(p), bits),
+    "status": [B]}."""
+    torch = _torch()
+    B, G, V = draft.shape
+    dev = draft.device
+    _check(target, "target", shape=(B, G + 1, V), device=dev)
+    _check(draft, "draft", device=dev)
+    if target.dtype != draft.dtype:
+        raise TypeError("target and draft dtypes differ")
+    _check(gamma, "gamma", torch.int32, (B,), dev)
+    _check(temperature, "temperature", torch.float32, (B,), dev)
+    o = out or {}
+    stats = _out(o, "stats", lambda: torch.empty(B, G, 5, dtype=torch.float32, device=dev))
+    st = _out(o, "status", lambda: torch.empty(B, dtype=torch.int32, device=dev))
+    rc = lib().spec_divergence_stats(_ptr(target), _ptr(draft), _dtype_code(draft), B, G, V, _ptr(gamma),
+                                     _ptr(temperature), _ptr(stats), _ptr(st), _stream(dev))
+    if rc != OK:
+        raise SpecVerifyError(rc, "spec_divergence_stats")
+    return {"stats": stats, "status": st}
 
 
 def draft_signals(draft, gamma, temperature, *, row_signals=False, ws=None, out=None):

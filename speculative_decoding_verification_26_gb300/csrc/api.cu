@@ -310,6 +310,39 @@ int spec_verify_onehot(const void* target_logits, int dtype, int B, int G, int V
   return run(c);
 }
 
+int spec_divergence_stats(const void* target_logits, const void* draft_logits, int dtype, int B, int G, int V,
+                          const int32_t* gamma, const float* temperature, float* stats, int32_t* status,
+                          spec_stream_t stream) {
+  if (!sizes_ok(B, G, V) || (dtype != SPEC_F32 && dtype != SPEC_BF16)) return SPEC_ERR_INVALID_ARG;
+  const size_t es = dtype == SPEC_BF16 ? 2 : 4;
+  if (!temperature || (G > 0 && (!target_logits || !draft_logits || !stats))) return SPEC_ERR_INVALID_ARG;
+  if (!aligned(target_logits, es) || !aligned(draft_logits, es)) return SPEC_ERR_INVALID_ARG;
+  const void* ptrs4[] = {gamma, temperature, stats, status};
+  for (const void* p : ptrs4)
+    if (!aligned(p, 4)) return SPEC_ERR_INVALID_ARG;
+  int ctas = 0;
+  const int ds = device_state(&ctas);
+  if (ds != SPEC_OK) return ds;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (status && cudaMemsetAsync(status, 0, sizeof(int32_t) * (size_t)B, s) != cudaSuccess) return SPEC_ERR_CUDA;
+  if (G == 0) return SPEC_OK;
+  int dev = 0, nsm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return SPEC_ERR_CUDA;
+  DivParams P{};
+  P.target = static_cast<const unsigned char*>(target_logits);
+  P.draft = static_cast<const unsigned char*>(draft_logits);
+  P.dtype = dtype; P.B = B; P.G = G; P.V = V;
+  P.aligned = ((size_t)V * es) % 16 == 0 && aligned(target_logits, 16) && aligned(draft_logits, 16);
+  P.gamma = gamma; P.temperature = temperature; P.stats = stats; P.status = status;
+  const long long pairs = (long long)B * G;
+  const int grid = (int)(pairs < (long long)nsm ? pairs : (long long)nsm);
+  if (launch_divergence(P, grid, s) != cudaSuccess) return SPEC_ERR_CUDA;
+  ++g_launches;
+  return SPEC_OK;
+}
+
 int spec_draft_signals(const void* draft_logits, int dtype, int B, int G, int V, const int32_t* gamma,
                        const float* temperature, float* signals, float* row_signals, int32_t* status,
                        void* workspace, size_t workspace_bytes, spec_stream_t stream) {

@@ -495,6 +495,19 @@ __device__ __forceinline__ Part empty_part() {
 
 // Host-side launchers (defined in verify.cu).  `pdl` enables programmatic
 // dependent launch on the caller's stream.
+// Parameters of the divergence-statistics kernel (divergence.cu).
+struct DivParams {
+  const unsigned char* target;   // [B, G+1, V]
+  const unsigned char* draft;    // [B, G, V]
+  int dtype, B, G, V;
+  int aligned;                   // every row starts on a 16-byte boundary (vector loads)
+  const int32_t* gamma;          // [B] or null (= G)
+  const float* temperature;      // [B]
+  float* stats;                  // [B, G, 5]
+  int32_t* status;               // [B] or null (zeroed by the host before the launch)
+};
+cudaError_t launch_divergence(const DivParams& P, int grid, cudaStream_t s);
+
 cudaError_t launch_plan(const Params& P, cudaStream_t s);
 cudaError_t launch_verify(const Params& P, int grid, cudaStream_t s, bool pdl);
 cudaError_t configure_kernels();   // dynamic shared-memory limit, current device

@@ -84,3 +84,15 @@ def test_host_rejects_bad_arguments(L):
     assert L.spec_verify_onehot(fake, 1, 4, 4, 1024, fake, None, fake, None, fake, fake, None, None, fake, ws,
                                 None) == 1
     assert L.spec_draft_signals(fake, 1, 4, 4, 1024, None, fake, None, None, None, fake, ws, None) == 1
+
+
+def test_divergence_stats_rejects_bad_arguments(L):
+    P = ctypes.c_void_p
+    fake = P(0x7f0000000000)       # never dereferenced: the host checks fail first
+    # no temperature, no stats, no draft, bad dtype, bad sizes, misaligned logits
+    assert L.spec_divergence_stats(fake, fake, 1, 4, 4, 1024, None, None, fake, None, None) == 1
+    assert L.spec_divergence_stats(fake, fake, 1, 4, 4, 1024, None, fake, None, None, None) == 1
+    assert L.spec_divergence_stats(fake, None, 1, 4, 4, 1024, None, fake, fake, None, None) == 1
+    assert L.spec_divergence_stats(fake, fake, 5, 4, 4, 1024, None, fake, fake, None, None) == 1
+    assert L.spec_divergence_stats(fake, fake, 1, 0, 4, 1024, None, fake, fake, None, None) == 1
+    assert L.spec_divergence_stats(P(0x7f0000000001), fake, 1, 4, 4, 1024, None, fake, fake, None, None) == 1
