@@ -54,6 +54,10 @@ PLANTS = {
     "divergence_l1_half": 18,
     "divergence_a_max": 19,
     "divergence_entropy_of_q": 20,
+    "gamma_select_no_relu": 21,
+    "gamma_select_no_gamma_factor": 22,
+    "gamma_select_tie_high": 23,
+    "gamma_select_feature_order": 24,
 }
 
 _lock = threading.Lock()
@@ -105,6 +109,9 @@ class Oracle:
         f.restype = ctypes.c_int
         self.lib.oracle_plant_id.restype = ctypes.c_int
         self.plant = self.lib.oracle_plant_id()
+        h = self.lib.oracle_gamma_select
+        h.argtypes = [P, P, P, ctypes.c_int, P, P]
+        h.restype = ctypes.c_int
         g = self.lib.oracle_divergence
         g.argtypes = [P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P, P, P, ctypes.c_int]
         g.restype = ctypes.c_int
@@ -180,6 +187,25 @@ class Oracle:
     def draft_signals(self, draft, gamma, temperature, **kw):
         kw.setdefault("want_signals", True)
         return self.run(SIGNALS, draft=draft, gamma=gamma, temperature=temperature, **kw)
+
+    def gamma_select(self, signals, comp, model):
+        """SpecKV gamma selection: signals [B, 4] (mean H, max H, mean c, min c),
+        comp [B] or None, model [141] (mu, sd, W1 [16, 6], b1, w2, b2); returns
+        {"gamma": [B] int32 (-1: non-finite features), "expected": [B, 4]}."""
+        signals = np.ascontiguousarray(signals, dtype=np.float64)
+        B = signals.shape[0]
+        comp = None if comp is None else np.ascontiguousarray(comp, dtype=np.float64)
+        model = np.ascontiguousarray(model, dtype=np.float64)
+        if model.shape != (141,):
+            raise ValueError("model must hold 141 values")
+        gam = np.zeros(B, np.int32)
+        exp_ = np.zeros((B, 4), np.float64)
+        rc = self.lib.oracle_gamma_select(_ptr(signals, ctypes.c_double), _ptr(comp, ctypes.c_double),
+                                          _ptr(model, ctypes.c_double), B, _ptr(gam, ctypes.c_int32),
+                                          _ptr(exp_, ctypes.c_double))
+        if rc != 0:
+            raise ValueError("oracle_gamma_select rejected its arguments")
+        return {"gamma": gam, "expected": exp_}
 
     def divergence_stats(self, target, draft, gamma, temperature, *, nthreads=None):
         """Per-position divergence statistics: target [B, G+1, V] (rows 0..G-1

@@ -62,6 +62,9 @@
  *   - accept_prob: pinned through A = 1 - TV(p, q) (section 4.3);
  *   - signals: pinned by closed forms (uniform, two-way tie, near one-hot rows)
  *     and by scipy's entropy on random rows;
+ *   - gamma selection (oracle_gamma_select): pinned by scikit-learn's MLP
+ *     regressor on the same weights, hand-built selectors with a known
+ *     argmax, ties and non-finite features (tests);
  *   - divergence statistics (oracle_divergence): pinned by scipy's entropy
  *     and relative entropy on random rows, the identities A = 1 - TV and
  *     L1 = 2 TV, the acceptance probability of the verify path averaged over
@@ -108,6 +111,10 @@
 #define PLANT_DIV_L1_HALF 18         /* L1 slot holds TV = L1 / 2              */
 #define PLANT_DIV_A_MAX 19           /* A = sum max(p, q)                      */
 #define PLANT_DIV_H_DRAFT 20         /* entropy of q instead of p              */
+#define PLANT_GSEL_NO_RELU 21        /* gamma selector: hidden layer linear    */
+#define PLANT_GSEL_NO_GAMMA_FACTOR 22 /* selector maximises f + 1, not f g + 1 */
+#define PLANT_GSEL_TIE_HIGH 23       /* selector ties go to the larger gamma   */
+#define PLANT_GSEL_FEATURE_ORDER 24  /* features in the library's signal order */
 
 /* dtype codes of the input logits */
 #define ORACLE_F32 0
@@ -660,6 +667,84 @@ int oracle_divergence(const void* target, const void* draft, int dtype, int B, i
         free(buf);
     }
     return failed ? -1 : 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* the SpecKV gamma selector                                                 */
+
+/* The SpecKV page ("接受率预测与 gamma 选择", acceptance prediction and gamma
+ * selection): with the context x = [mean H, mean c, max H, min c, comp] of a
+ * request, a regressor f(x, gamma) predicts the acceptance rate; the expected
+ * tokens of a step are f(x, gamma) gamma + 1, and the policy takes
+ * gamma* = argmax over gamma in {2, 4, 6, 8}.  The regressor is an MLP with
+ * 16 hidden units.  Readings: its inputs are [x, gamma], standardised as
+ * (z - mu) / sd; one ReLU hidden layer; an identity output; ties go to the
+ * smallest gamma.
+ * Model layout (141 values): mu[6], sd[6], W1[16][6] (row h: the weights of
+ * hidden unit h), b1[16], w2[16], b2.
+ * signals [B, 4] in the library's order (mean H, max H, mean c, min c);
+ * comp [B] or NULL (= 0).  Outputs: gamma_star [B] (-1 when a feature is not
+ * finite), expected [B, 4] (f gamma + 1 for gamma = 2, 4, 6, 8). */
+static double gsel_f(const double* model, const double* x5, double g)
+{
+    const double* mu = model;
+    const double* sd = model + 6;
+    const double* W1 = model + 12;
+    const double* b1 = model + 108;
+    const double* w2 = model + 124;
+    const double b2 = model[140];
+    double z[6];
+    for (int k = 0; k < 5; ++k) z[k] = x5[k];
+    z[5] = g;
+    for (int k = 0; k < 6; ++k) z[k] = (z[k] - mu[k]) / sd[k];
+    double f = b2;
+    for (int h = 0; h < 16; ++h) {
+        double a = b1[h];
+        for (int k = 0; k < 6; ++k) a += W1[h * 6 + k] * z[k];
+#if ORACLE_PLANT != PLANT_GSEL_NO_RELU
+        if (a < 0.0) a = 0.0;
+#endif
+        f += w2[h] * a;
+    }
+    return f;
+}
+
+int oracle_gamma_select(const double* signals, const double* comp, const double* model, int B,
+                        int32_t* gamma_star, double* expected)
+{
+    if (B < 0 || !signals || !model || !gamma_star) return -1;
+    static const int cand[4] = {2, 4, 6, 8};
+    for (int b = 0; b < B; ++b) {
+        const double* s = signals + (size_t)b * 4;
+#if ORACLE_PLANT == PLANT_GSEL_FEATURE_ORDER
+        const double x5[5] = {s[0], s[1], s[2], s[3], comp ? comp[b] : 0.0};
+#else
+        const double x5[5] = {s[0], s[2], s[1], s[3], comp ? comp[b] : 0.0};   /* [mean H, mean c, max H, min c, comp] */
+#endif
+        int finite = 1;
+        for (int k = 0; k < 5; ++k) finite &= isfinite(x5[k]);
+        int best = -1;
+        double bestE = -INFINITY;
+        for (int j = 0; j < 4; ++j) {
+            double E = NAN;
+            if (finite) {
+                const double f = gsel_f(model, x5, (double)cand[j]);
+#if ORACLE_PLANT == PLANT_GSEL_NO_GAMMA_FACTOR
+                E = f + 1.0;
+#else
+                E = f * cand[j] + 1.0;
+#endif
+#if ORACLE_PLANT == PLANT_GSEL_TIE_HIGH
+                if (E >= bestE) { bestE = E; best = cand[j]; }
+#else
+                if (E > bestE) { bestE = E; best = cand[j]; }
+#endif
+            }
+            if (expected) expected[(size_t)b * 4 + j] = E;
+        }
+        gamma_star[b] = finite ? best : -1;
+    }
+    return 0;
 }
 
 /* Which planted mistake this build carries (0 = none). */

@@ -564,6 +564,67 @@ def pin_divergence(o):
     assert r["status"][0] == 1 and np.isnan(r["stats"][0, 0]).all() and np.isfinite(r["stats"][0, 1]).all(), r
 
 
+def pin_gamma_select(o):
+    """The SpecKV gamma selector (SpecKV page, acceptance prediction and gamma
+    selection): E[tokens] = f(x, gamma) gamma + 1 with x = [mean H, mean c,
+    max H, min c, comp], gamma* = argmax over {2, 4, 6, 8}; f an MLP with 16
+    hidden units on the standardised inputs [x, gamma].
+      - f against scikit-learn's MLPRegressor (ReLU hidden layer, identity
+        output) fitted on random data, its scaler and weights copied into the
+        141-value model;
+      - a hand-built selector f = a - b gamma, whose expected tokens
+        a gamma - b gamma^2 + 1 peak at gamma = a / (2b): an exact tie between
+        4 and 6 (a = 1.25, b = 1/8: the smaller is taken), and a peak at 7.1
+        (8 is taken);
+      - a non-finite feature gives -1."""
+    pytest_sklearn = __import__("importlib").util.find_spec("sklearn")
+    rng = np.random.default_rng(21)
+    sig = np.column_stack([rng.uniform(0.5, 6, 50), rng.uniform(2, 12, 50),        # mean H, max H
+                           rng.uniform(0.2, 0.9, 50), rng.uniform(0.05, 0.5, 50)])  # mean c, min c
+    comp = rng.integers(0, 3, 50).astype(np.float64)
+    if pytest_sklearn is not None:
+        from sklearn.neural_network import MLPRegressor
+        from sklearn.preprocessing import StandardScaler
+        X = np.column_stack([rng.uniform(0.5, 6, 400), rng.uniform(0.2, 0.9, 400), rng.uniform(2, 12, 400),
+                             rng.uniform(0.05, 0.5, 400), rng.integers(0, 3, 400), rng.choice([2, 4, 6, 8], 400)])
+        y = rng.uniform(0, 1, 400)
+        sc = StandardScaler().fit(X)
+        mlp = MLPRegressor(hidden_layer_sizes=(16,), activation="relu", max_iter=300, random_state=0).fit(
+            sc.transform(X), y)
+        model = np.concatenate([sc.mean_, sc.scale_, mlp.coefs_[0].T.ravel(), mlp.intercepts_[0],
+                                mlp.coefs_[1][:, 0], mlp.intercepts_[1]])
+        r = o.gamma_select(sig, comp, model)
+        for j, g in enumerate((2, 4, 6, 8)):
+            xin = np.column_stack([sig[:, 0], sig[:, 2], sig[:, 1], sig[:, 3], comp, np.full(50, g)])
+            want = mlp.predict(sc.transform(xin)) * g + 1.0
+            assert np.allclose(r["expected"][:, j], want, rtol=1e-12, atol=1e-12), (g, r["expected"][:5, j], want[:5])
+        assert np.array_equal(r["gamma"], np.array((2, 4, 6, 8))[np.argmax(r["expected"], axis=1)])
+    # f = a - b gamma: one hidden unit passes gamma (mu 0, sd 1), a second
+    # one is off (ReLU of -gamma) unless the hidden layer were linear
+    def selector(a, b):
+        m = np.zeros(141)
+        m[6:12] = 1.0                      # sd
+        W1 = np.zeros((16, 6))
+        W1[0, 5] = 1.0
+        W1[1, 5] = -1.0
+        m[12:108] = W1.ravel()
+        w2 = np.zeros(16)
+        w2[0] = -b
+        w2[1] = 0.3
+        m[124:140] = w2
+        m[140] = a
+        return m
+    one = np.array([[1.0, 2.0, 0.6, 0.3]])
+    r = o.gamma_select(one, None, selector(1.25, 0.125))
+    assert r["gamma"][0] == 4, r               # E(4) = E(6) = 4 exactly: the smaller gamma
+    assert np.array_equal(r["expected"][0], [3.0, 4.0, 4.0, 3.0]), r["expected"]
+    r = o.gamma_select(one, None, selector(1.0, 0.07))
+    assert r["gamma"][0] == 8, r               # peak at 7.1: E(6) = 4.48 < E(8) = 4.52
+    bad = np.array([[np.nan, 2.0, 0.6, 0.3]])
+    r = o.gamma_select(bad, None, selector(1.25, 0.125))
+    assert r["gamma"][0] == -1 and np.isnan(r["expected"][0]).all()
+
+
 ALL_PINS = [
     pin_worked_example,
     pin_worked_example_onehot,
@@ -582,4 +643,5 @@ ALL_PINS = [
     pin_status_semantics,
     pin_decision_margins,
     pin_divergence,
+    pin_gamma_select,
 ]
