@@ -214,6 +214,32 @@ int spec_divergence_stats(const void* target_logits, const void* draft_logits, i
                           int B, int G, int V, const int32_t* gamma, const float* temperature,
                           float* stats, int32_t* status, spec_stream_t stream);
 
+/* The SpecKV gamma selector (SpecKV page, acceptance prediction and gamma
+ * selection).  For each request, with the context
+ * x = [mean H, mean c, max H, min c, comp] (the signals of spec_verify_sample
+ * or spec_draft_signals, taken in that order, and a compression level), an
+ * MLP f(x, gamma) with 16 hidden units predicts the acceptance rate; the
+ * expected tokens of a step are f(x, gamma) gamma + 1 and
+ * gamma* = argmax over gamma in {2, 4, 6, 8}, ties to the smaller gamma.
+ * The MLP takes [x, gamma] standardised as (z - mu) / sd, has one ReLU hidden
+ * layer and an identity output.
+ *   signals     [B, 4] fp32 (mean H, max H, mean c, min c: the library's
+ *               signal layout), device, read only;
+ *   comp        [B] fp32 or NULL (= 0): the compression level feature;
+ *   model       SPEC_GAMMA_MODEL_FLOATS fp32, device: mu[6], sd[6],
+ *               W1[16][6] (row h holds hidden unit h's weights), b1[16],
+ *               w2[16], b2;
+ *   gamma_star  [B] int32, written: 2, 4, 6 or 8; -1 when a feature is not
+ *               finite (a request with gamma_b = 0 or an error);
+ *   expected    [B, 4] fp32 or NULL: f gamma + 1 for gamma = 2, 4, 6, 8 (NaN
+ *               for a non-finite feature).
+ * No workspace.  Host errors: SPEC_ERR_INVALID_ARG (B outside [1, 65535], NULL
+ * signals, model or gamma_star, misalignment: signals 16-byte, the others
+ * 4-byte), SPEC_ERR_CUDA, SPEC_ERR_UNSUPPORTED. */
+#define SPEC_GAMMA_MODEL_FLOATS 141
+int spec_gamma_select(const float* signals, const float* comp, const float* model, int B,
+                      int32_t* gamma_star, float* expected, spec_stream_t stream);
+
 /* Size of the library-owned scratch used by spec_verify_sample_static: 8 MiB.
  * It holds the workspace of spec_workspace_bytes(B, G, V) <= this value, e.g.
  * B <= 268 at G = 8, V = 151936, or B <= 276 at G = 7, V = 151936. */

@@ -63,6 +63,8 @@ def lib(path: str | None = None) -> ctypes.CDLL:
         L.spec_draft_signals.argtypes = [P, I, I, I, I, P, P, P, P, P, P, SZ, P]
         L.spec_divergence_stats.argtypes = [P, P, I, I, I, I, P, P, P, P, P]
         L.spec_divergence_stats.restype = I
+        L.spec_gamma_select.argtypes = [P, P, P, I, P, P, P]
+        L.spec_gamma_select.restype = I
         L.spec_draft_signals.restype = I
         if path is None:
             _lib = L
@@ -267,6 +269,28 @@ def divergence_stats(target, draft, gamma, temperature, *, out=None):
     if rc != OK:
         raise SpecVerifyError(rc, "spec_divergence_stats")
     return {"stats": stats, "status": st}
+
+
+GAMMA_MODEL_FLOATS = 141
+
+
+def gamma_select(signals, model, comp=None, *, out=None):
+    """SpecKV gamma selection.  signals [B, 4] fp32 (mean H, max H, mean c,
+    min c), model [141] fp32, comp [B] fp32 or None; returns {"gamma": [B]
+    int32 (2, 4, 6, 8; -1 for non-finite features), "expected": [B, 4]}."""
+    torch = _torch()
+    B = signals.shape[0]
+    dev = signals.device
+    _check(signals, "signals", torch.float32, (B, 4), dev)
+    _check(model, "model", torch.float32, (GAMMA_MODEL_FLOATS,), dev)
+    _check(comp, "comp", torch.float32, (B,), dev)
+    o = out or {}
+    g = _out(o, "gamma", lambda: torch.empty(B, dtype=torch.int32, device=dev))
+    e = _out(o, "expected", lambda: torch.empty(B, 4, dtype=torch.float32, device=dev))
+    rc = lib().spec_gamma_select(_ptr(signals), _ptr(comp), _ptr(model), B, _ptr(g), _ptr(e), _stream(dev))
+    if rc != OK:
+        raise SpecVerifyError(rc, "spec_gamma_select")
+    return {"gamma": g, "expected": e}
 
 
 def draft_signals(draft, gamma, temperature, *, row_signals=False, ws=None, out=None):

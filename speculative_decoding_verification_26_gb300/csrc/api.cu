@@ -343,6 +343,23 @@ int spec_divergence_stats(const void* target_logits, const void* draft_logits, i
   return SPEC_OK;
 }
 
+int spec_gamma_select(const float* signals, const float* comp, const float* model, int B, int32_t* gamma_star,
+                      float* expected, spec_stream_t stream) {
+  if (B < 1 || B > SPEC_MAX_B || !signals || !model || !gamma_star) return SPEC_ERR_INVALID_ARG;
+  if (!aligned(signals, 16)) return SPEC_ERR_INVALID_ARG;
+  const void* ptrs4[] = {comp, model, gamma_star, expected};
+  for (const void* p : ptrs4)
+    if (!aligned(p, 4)) return SPEC_ERR_INVALID_ARG;
+  int ctas = 0;
+  const int ds = device_state(&ctas);
+  if (ds != SPEC_OK) return ds;
+  if (launch_gamma_select(signals, comp, model, B, gamma_star, expected, reinterpret_cast<cudaStream_t>(stream)) !=
+      cudaSuccess)
+    return SPEC_ERR_CUDA;
+  ++g_launches;
+  return SPEC_OK;
+}
+
 int spec_draft_signals(const void* draft_logits, int dtype, int B, int G, int V, const int32_t* gamma,
                        const float* temperature, float* signals, float* row_signals, int32_t* status,
                        void* workspace, size_t workspace_bytes, spec_stream_t stream) {

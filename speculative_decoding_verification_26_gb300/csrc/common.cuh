@@ -508,6 +508,11 @@ struct DivParams {
 };
 cudaError_t launch_divergence(const DivParams& P, int grid, cudaStream_t s);
 
+// The SpecKV gamma selector (gamma.cu): model of SPEC_GAMMA_MODEL_FLOATS values.
+constexpr int kGammaModelFloats = SPEC_GAMMA_MODEL_FLOATS;
+cudaError_t launch_gamma_select(const float* signals, const float* comp, const float* model, int B,
+                                int32_t* gamma_star, float* expected, cudaStream_t s);
+
 cudaError_t launch_plan(const Params& P, cudaStream_t s);
 cudaError_t launch_verify(const Params& P, int grid, cudaStream_t s, bool pdl);
 cudaError_t configure_kernels();   // dynamic shared-memory limit, current device

@@ -96,3 +96,13 @@ def test_divergence_stats_rejects_bad_arguments(L):
     assert L.spec_divergence_stats(fake, fake, 5, 4, 4, 1024, None, fake, fake, None, None) == 1
     assert L.spec_divergence_stats(fake, fake, 1, 0, 4, 1024, None, fake, fake, None, None) == 1
     assert L.spec_divergence_stats(P(0x7f0000000001), fake, 1, 4, 4, 1024, None, fake, fake, None, None) == 1
+
+
+def test_gamma_select_rejects_bad_arguments(L):
+    P = ctypes.c_void_p
+    fake = P(0x7f0000000000)       # never dereferenced: the host checks fail first
+    assert L.spec_gamma_select(None, None, fake, 4, fake, None, None) == 1
+    assert L.spec_gamma_select(fake, None, None, 4, fake, None, None) == 1
+    assert L.spec_gamma_select(fake, None, fake, 4, None, None, None) == 1
+    assert L.spec_gamma_select(fake, None, fake, 0, fake, None, None) == 1
+    assert L.spec_gamma_select(P(0x7f0000000004), None, fake, 4, fake, None, None) == 1   # signals not 16-byte aligned
