@@ -58,6 +58,10 @@ PLANTS = {
     "gamma_select_no_gamma_factor": 22,
     "gamma_select_tie_high": 23,
     "gamma_select_feature_order": 24,
+    "filter_topk_strict": 25,
+    "filter_topp_exclusive": 26,
+    "filter_topp_before_topk": 27,
+    "filter_no_temperature": 28,
 }
 
 _lock = threading.Lock()
@@ -109,6 +113,9 @@ class Oracle:
         f.restype = ctypes.c_int
         self.lib.oracle_plant_id.restype = ctypes.c_int
         self.plant = self.lib.oracle_plant_id()
+        fl = self.lib.oracle_filter
+        fl.argtypes = [P, ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P, P, P, P, P, ctypes.c_int]
+        fl.restype = ctypes.c_int
         h = self.lib.oracle_gamma_select
         h.argtypes = [P, P, P, ctypes.c_int, P, P]
         h.restype = ctypes.c_int
@@ -187,6 +194,27 @@ class Oracle:
     def draft_signals(self, draft, gamma, temperature, **kw):
         kw.setdefault("want_signals", True)
         return self.run(SIGNALS, draft=draft, gamma=gamma, temperature=temperature, **kw)
+
+    def filter_logits(self, logits, top_k=None, top_p=None, temperature=None, *, nthreads=None):
+        """Top-k / top-p filtering of rows [n, V] (f32, bf16 bits or f64);
+        returns {"logits": [n, V] fp64 filtered, "status": [n], "margin": [n]}."""
+        logits = np.ascontiguousarray(logits)
+        n, V = logits.shape
+        dt = _dtype_code(logits)
+        top_k = None if top_k is None else np.ascontiguousarray(top_k, dtype=np.int32)
+        top_p = None if top_p is None else np.ascontiguousarray(top_p, dtype=np.float32)
+        temperature = None if temperature is None else np.ascontiguousarray(temperature, dtype=np.float32)
+        out = np.zeros((n, V), np.float64)
+        st = np.zeros(n, np.int32)
+        mg = np.zeros(n, np.float64)
+        nthreads = nthreads or os.cpu_count() or 1
+        rc = self.lib.oracle_filter(_ptr(logits, ctypes.c_char), dt, n, V, _ptr(top_k, ctypes.c_int32),
+                                    _ptr(top_p, ctypes.c_float), _ptr(temperature, ctypes.c_float),
+                                    _ptr(out, ctypes.c_double), _ptr(st, ctypes.c_int32), _ptr(mg, ctypes.c_double),
+                                    int(nthreads))
+        if rc != 0:
+            raise ValueError("oracle_filter rejected its arguments")
+        return {"logits": out, "status": st, "margin": mg}
 
     def gamma_select(self, signals, comp, model):
         """SpecKV gamma selection: signals [B, 4] (mean H, max H, mean c, min c),

@@ -62,6 +62,9 @@
  *   - accept_prob: pinned through A = 1 - TV(p, q) (section 4.3);
  *   - signals: pinned by closed forms (uniform, two-way tie, near one-hot rows)
  *     and by scipy's entropy on random rows;
+ *   - top-k / top-p filtering (oracle_filter): pinned by hand-computed rows
+ *     (ties, the crossing value, top-k then top-p, temperature) and by a
+ *     brute-force search over thresholds on random rows (tests);
  *   - gamma selection (oracle_gamma_select): pinned by scikit-learn's MLP
  *     regressor on the same weights, hand-built selectors with a known
  *     argmax, ties and non-finite features (tests);
@@ -115,6 +118,10 @@
 #define PLANT_GSEL_NO_GAMMA_FACTOR 22 /* selector maximises f + 1, not f g + 1 */
 #define PLANT_GSEL_TIE_HIGH 23       /* selector ties go to the larger gamma   */
 #define PLANT_GSEL_FEATURE_ORDER 24  /* features in the library's signal order */
+#define PLANT_FILT_TOPK_STRICT 25    /* top-k keeps x > k-th value, not >=     */
+#define PLANT_FILT_TOPP_EXCLUSIVE 26 /* top-p stops before the crossing value  */
+#define PLANT_FILT_TOPP_BEFORE_TOPK 27 /* top-p mass over the unfiltered row   */
+#define PLANT_FILT_NO_TEMPERATURE 28 /* top-p mass at T = 1                     */
 
 /* dtype codes of the input logits */
 #define ORACLE_F32 0
@@ -745,6 +752,126 @@ int oracle_gamma_select(const double* signals, const double* comp, const double*
         gamma_star[b] = finite ? best : -1;
     }
     return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* top-k / top-p filtering before verification                               */
+
+static int cmp_desc(const void* a, const void* b)
+{
+    const double x = *(const double*)a, y = *(const double*)b;
+    return (x < y) - (x > y);
+}
+
+/* Filter one row of logits x[0..V) in place (tutorial page, section 2.1: p
+ * and q are the distributions actually sampled from, "temperature / top-k /
+ * top-p already applied, if used").  Readings (by value, so ties are kept
+ * together):
+ *   top-k (k >= 1 and k < V): keep x >= the k-th largest value;
+ *   top-p (0 < top_p < 1), on the distribution left by top-k at temperature T:
+ *     with the kept values in descending order, t* = the largest value v such
+ *     that the mass of {x >= v} is >= top_p; keep x >= t*;
+ *   a removed token becomes -inf.
+ * margin (optional): for top-p, the distance of top_p from the nearer of the
+ * masses of {x >= t*} and {x > t*} (a decision within rounding of its
+ * threshold can come out either way in fp32).  Returns 0 if the row holds NaN
+ * or +inf or has no finite maximum (left unchanged), else 1. */
+static int filter_row(double* x, int V, int k, double top_p, double T, double* sorted, double* margin)
+{
+    double m;
+    if (!row_max(x, V, &m)) return 0;
+    if (margin) *margin = INFINITY;
+    memcpy(sorted, x, sizeof(double) * (size_t)V);
+    qsort(sorted, (size_t)V, sizeof(double), cmp_desc);
+    double thr = -INFINITY;
+    if (k >= 1 && k < V) {
+        thr = sorted[k - 1];
+#if ORACLE_PLANT == PLANT_FILT_TOPK_STRICT
+        for (int v = 0; v < V; ++v) if (!(x[v] > thr)) x[v] = -INFINITY;
+        thr = -INFINITY;
+        memcpy(sorted, x, sizeof(double) * (size_t)V);
+        qsort(sorted, (size_t)V, sizeof(double), cmp_desc);
+#endif
+    }
+    if (top_p > 0.0 && top_p < 1.0) {
+#if ORACLE_PLANT == PLANT_FILT_TOPP_BEFORE_TOPK
+        const double lim = -INFINITY;
+#else
+        const double lim = thr;
+#endif
+#if ORACLE_PLANT == PLANT_FILT_NO_TEMPERATURE
+        T = 1.0;
+#endif
+        double S = 0.0;
+        for (int v = 0; v < V; ++v)
+            if (sorted[v] >= lim) S += exp((sorted[v] - m) / T);
+        double C = 0.0, Cprev = 0.0;
+        double tstar = -INFINITY;
+        for (int v = 0; v < V && sorted[v] >= lim;) {
+            int w = v;
+            double mass = 0.0;
+            while (w < V && sorted[w] == sorted[v]) { mass += exp((sorted[w] - m) / T); ++w; }
+            Cprev = C;
+            C += mass;
+            if (C / S >= top_p) {
+#if ORACLE_PLANT == PLANT_FILT_TOPP_EXCLUSIVE
+                tstar = v > 0 ? sorted[v - 1] : sorted[v];
+#else
+                tstar = sorted[v];
+#endif
+                if (margin) {
+                    const double d1 = C / S - top_p, d0 = top_p - Cprev / S;
+                    *margin = d0 < d1 ? d0 : d1;
+                }
+                break;
+            }
+            v = w;
+        }
+        if (tstar > thr) thr = tstar;
+    }
+    for (int v = 0; v < V; ++v)
+        if (x[v] < thr) x[v] = -INFINITY;
+    return 1;
+}
+
+/* Filter n rows [n, V] of logits (dtype 0 f32, 1 bf16 as uint16 bits, 2 f64)
+ * into out [n, V] fp64 (a row with NaN, +inf or no finite maximum is copied
+ * unchanged and gets status OST_NONFINITE).  top_k [n] int32 or NULL (no
+ * top-k), top_p [n] or NULL (no top-p), temperature [n] or NULL (= 1; only
+ * top-p uses it; an invalid temperature with top-p in use gives status
+ * OST_BAD_TEMPERATURE and the row unchanged); margin [n] or NULL.
+ * Returns 0, or -1 on a bad argument or allocation failure. */
+int oracle_filter(const void* logits, int dtype, int n, int V, const int32_t* top_k, const float* top_p,
+                  const float* temperature, double* out, int32_t* status, double* margin, int nthreads)
+{
+    if (n < 0 || V < 1 || dtype < 0 || dtype > 2 || !logits || !out) return -1;
+    int failed = 0;
+    if (nthreads < 1) nthreads = 1;
+#pragma omp parallel num_threads(nthreads)
+    {
+        double* buf = (double*)malloc(sizeof(double) * (size_t)V);
+        if (!buf) {
+#pragma omp atomic write
+            failed = 1;
+        }
+#pragma omp for schedule(dynamic, 1)
+        for (int r = 0; r < n; ++r) {
+            if (!buf) continue;
+            double* x = out + (size_t)r * V;
+            load_row(logits, dtype, (size_t)r, V, x);
+            const double pp = top_p ? (double)top_p[r] : 1.0;
+            const double T = temperature ? (double)temperature[r] : 1.0;
+            int st = 0;
+            double mg = INFINITY;
+            if (pp > 0.0 && pp < 1.0 && !(T > 0.0 && isfinite(T))) st = OST_BAD_TEMPERATURE;
+            else if (!filter_row(x, V, top_k ? top_k[r] : 0, pp, T, buf, &mg)) st = OST_NONFINITE;
+            if (st) load_row(logits, dtype, (size_t)r, V, x);
+            if (status) status[r] = st;
+            if (margin) margin[r] = mg;
+        }
+        free(buf);
+    }
+    return failed ? -1 : 0;
 }
 
 /* Which planted mistake this build carries (0 = none). */

@@ -625,6 +625,54 @@ def pin_gamma_select(o):
     assert r["gamma"][0] == -1 and np.isnan(r["expected"][0]).all()
 
 
+def pin_filter(o):
+    """Top-k / top-p filtering before verification (tutorial page, section
+    2.1: p and q already include temperature / top-k / top-p when used),
+    read by value: top-k keeps x >= the k-th largest logit; top-p, on the
+    distribution left by top-k at temperature T, keeps x >= t*, the largest
+    value whose upper mass {x >= t*} reaches top_p.  Checked on rows of exact
+    binary fractions by hand, and against a brute-force search over every
+    candidate threshold on small random rows with ties."""
+    one = np.ones(1, np.float32)
+    x = np.log(np.array([[0.5, 0.25, 0.125, 0.0625, 0.0625]]))
+
+    def kept(k, p, T=1.0, row=x):
+        r = o.filter_logits(row, None if k is None else np.array([k]), None if p is None else np.array([p]),
+                            np.array([T], np.float32))
+        return np.isfinite(r["logits"][0]).astype(int).tolist()
+    assert kept(None, 0.7) == [1, 1, 0, 0, 0]      # 0.5, 0.75 >= 0.7
+    assert kept(None, 0.75) == [1, 1, 0, 0, 0]     # the crossing value is kept (mass >= top_p)
+    assert kept(None, 0.76) == [1, 1, 1, 0, 0]
+    assert kept(None, 0.95) == [1, 1, 1, 1, 1]     # the tie group {1/16, 1/16} together
+    assert kept(3, None) == [1, 1, 1, 0, 0]
+    assert kept(4, None) == [1, 1, 1, 1, 1]        # the 4th largest is tied with the 5th
+    assert kept(3, 0.8) == [1, 1, 0, 0, 0]         # after top-k: 4/7, 6/7 >= 0.8
+    assert kept(0, 1.0) == [1, 1, 1, 1, 1] and kept(5, None) == [1, 1, 1, 1, 1]
+    # T = 2 flattens p to [0.354, 0.25, 0.177, 0.125, 0.125] / 1.030: 0.5 takes 2 tokens
+    assert kept(None, 0.5, T=2.0) == [1, 1, 0, 0, 0] and kept(None, 0.5) == [1, 0, 0, 0, 0]
+    # brute force: every candidate threshold of the row, in fp64
+    rng = np.random.default_rng(31)
+    for trial in range(300):
+        V = int(rng.integers(2, 12))
+        row = np.round(rng.normal(0, 2, V), 1)           # rounding makes ties
+        k = int(rng.integers(0, V + 1))
+        p = float(np.float32(rng.uniform(0.05, 1.0)))
+        T = float(np.float32(rng.uniform(0.3, 2.0)))
+        got = np.isfinite(o.filter_logits(row[None], np.array([k]), np.array([p]), np.array([T]))["logits"][0])
+        cand = np.sort(np.unique(row))[::-1]
+        keep = row >= np.sort(row)[::-1][k - 1] if 1 <= k < V else np.ones(V, bool)
+        if p < 1.0:
+            w = special.softmax(row[keep] / T)
+            vals = row[keep]
+            tstar = None
+            for v in cand:                                  # descending candidate thresholds
+                if (vals >= v).any() and w[vals >= v].sum() >= p:
+                    tstar = v
+                    break
+            keep = keep & (row >= tstar)
+        assert np.array_equal(got, keep), (row, k, p, T, got, keep)
+
+
 ALL_PINS = [
     pin_worked_example,
     pin_worked_example_onehot,
@@ -644,4 +692,5 @@ ALL_PINS = [
     pin_decision_margins,
     pin_divergence,
     pin_gamma_select,
+    pin_filter,
 ]
