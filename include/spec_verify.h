@@ -214,6 +214,34 @@ int spec_divergence_stats(const void* target_logits, const void* draft_logits, i
                           int B, int G, int V, const int32_t* gamma, const float* temperature,
                           float* stats, int32_t* status, spec_stream_t stream);
 
+/* Top-k / top-p filtering of logit rows before verification (tutorial page
+ * section 2.1: p and q are the distributions actually sampled from, with
+ * temperature, top-k and top-p already applied when used).  Row r of
+ * logits [n, V] is filtered in place, by value (ties stay together):
+ *   top-k, when 1 <= top_k[r] < V: keep x >= the k-th largest logit;
+ *   top-p, when 0 < top_p[r] < 1, on the distribution left by top-k at
+ *   temperature[r]: keep x >= t*, the largest value whose upper mass
+ *   sum_{x >= t*} softmax(x / T) reaches top_p;
+ *   a removed logit becomes -inf.
+ *   logits       [n, V], dtype SPEC_F32 or SPEC_BF16, device, caller-owned,
+ *                read and written;
+ *   top_k        [n] int32 or NULL (no top-k); top_p [n] fp32 or NULL (no
+ *                top-p); temperature [n] fp32 or NULL (= 1; used by top-p);
+ *   status       [n] int32 or NULL: 0, SPEC_ST_NONFINITE (a NaN or +inf, or
+ *                no finite logit: the row is left unchanged) or
+ *                SPEC_ST_BAD_TEMPERATURE (top-p with a temperature <= 0 or not
+ *                finite: unchanged).
+ * The top-p decision compares masses that fp32 weights carry to ~1e-6: a row
+ * whose mass at t* lies within that of top_p can keep one value group more or
+ * less than an exact computation.  Results are deterministic.  Filtering a
+ * target and a draft row with the same settings gives the p and q the
+ * verification calls then use.  No workspace.  Host errors:
+ * SPEC_ERR_INVALID_ARG (n < 1, V outside [2, 2^28), dtype, NULL logits,
+ * misalignment), SPEC_ERR_CUDA, SPEC_ERR_UNSUPPORTED. */
+int spec_filter_top_k_top_p(void* logits, int dtype, int n, int V, const int32_t* top_k,
+                            const float* top_p, const float* temperature, int32_t* status,
+                            spec_stream_t stream);
+
 /* The SpecKV gamma selector (SpecKV page, acceptance prediction and gamma
  * selection).  For each request, with the context
  * x = [mean H, mean c, max H, min c, comp] (the signals of spec_verify_sample

@@ -8,7 +8,7 @@ entry points (``_lib.py``) and the seeded synthetic workloads
 loads the library and fails loudly if it is missing.
 """
 from ._lib import (  # noqa: F401
-    BF16, F32, GAMMA_MODEL_FLOATS, SpecVerifyError, divergence_stats, draft_signals, gamma_select, launch_count, lib, profile_next_call, request_status_string,
+    BF16, F32, GAMMA_MODEL_FLOATS, SpecVerifyError, divergence_stats, draft_signals, filter_top_k_top_p, gamma_select, launch_count, lib, profile_next_call, request_status_string,
     set_wait_limit, status_string,
     verify_greedy, verify_onehot, verify_sample, workspace, workspace_bytes,
 )

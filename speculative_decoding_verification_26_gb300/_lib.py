@@ -64,6 +64,8 @@ def lib(path: str | None = None) -> ctypes.CDLL:
         L.spec_divergence_stats.argtypes = [P, P, I, I, I, I, P, P, P, P, P]
         L.spec_divergence_stats.restype = I
         L.spec_gamma_select.argtypes = [P, P, P, I, P, P, P]
+        L.spec_filter_top_k_top_p.argtypes = [P, I, I, I, P, P, P, P, P]
+        L.spec_filter_top_k_top_p.restype = I
         L.spec_gamma_select.restype = I
         L.spec_draft_signals.restype = I
         if path is None:
@@ -269,6 +271,26 @@ def divergence_stats(target, draft, gamma, temperature, *, out=None):
     if rc != OK:
         raise SpecVerifyError(rc, "spec_divergence_stats")
     return {"stats": stats, "status": st}
+
+
+def filter_top_k_top_p(logits, top_k=None, top_p=None, temperature=None, *, status=None):
+    """Top-k / top-p filtering of the rows of `logits` ([..., V], contiguous,
+    fp32 or bf16) in place; top_k [n] int32, top_p [n] fp32, temperature [n]
+    fp32, each optional (n = rows).  Returns the per-row status tensor."""
+    torch = _torch()
+    V = logits.shape[-1]
+    n = logits.numel() // V
+    dev = logits.device
+    _check(logits, "logits", device=dev)
+    _check(top_k, "top_k", torch.int32, (n,), dev)
+    _check(top_p, "top_p", torch.float32, (n,), dev)
+    _check(temperature, "temperature", torch.float32, (n,), dev)
+    st = status if status is not None else torch.empty(n, dtype=torch.int32, device=dev)
+    rc = lib().spec_filter_top_k_top_p(_ptr(logits), _dtype_code(logits), n, V, _ptr(top_k), _ptr(top_p),
+                                       _ptr(temperature), _ptr(st), _stream(dev))
+    if rc != OK:
+        raise SpecVerifyError(rc, "spec_filter_top_k_top_p")
+    return st
 
 
 GAMMA_MODEL_FLOATS = 141

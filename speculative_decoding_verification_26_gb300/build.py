@@ -15,7 +15,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OBJ = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libspec_verify.so")
-SOURCES = ["api.cu", "verify.cu", "divergence.cu", "gamma.cu"]
+SOURCES = ["api.cu", "verify.cu", "divergence.cu", "gamma.cu", "filter.cu"]
 HEADERS = ["common.cuh", "exp2_table.cuh", os.path.join("..", "..", "include", "spec_verify.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",

@@ -343,6 +343,29 @@ int spec_divergence_stats(const void* target_logits, const void* draft_logits, i
   return SPEC_OK;
 }
 
+int spec_filter_top_k_top_p(void* logits, int dtype, int n, int V, const int32_t* top_k, const float* top_p,
+                            const float* temperature, int32_t* status, spec_stream_t stream) {
+  if (n < 1 || V < 2 || V >= (1 << 28) || !logits || (dtype != SPEC_F32 && dtype != SPEC_BF16))
+    return SPEC_ERR_INVALID_ARG;
+  const size_t es = dtype == SPEC_BF16 ? 2 : 4;
+  if (!aligned(logits, es)) return SPEC_ERR_INVALID_ARG;
+  const void* ptrs4[] = {top_k, top_p, temperature, status};
+  for (const void* p : ptrs4)
+    if (!aligned(p, 4)) return SPEC_ERR_INVALID_ARG;
+  int ctas = 0;
+  const int ds = device_state(&ctas);
+  if (ds != SPEC_OK) return ds;
+  FiltParams P{};
+  P.logits = static_cast<unsigned char*>(logits);
+  P.dtype = dtype; P.n = n; P.V = V;
+  P.top_k = top_k; P.top_p = top_p; P.temperature = temperature; P.status = status;
+  const int grid = n < 4 * ctas ? n : 4 * ctas;
+  if (launch_filter(P, grid > 0 ? grid : 1, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return SPEC_ERR_CUDA;
+  ++g_launches;
+  return SPEC_OK;
+}
+
 int spec_gamma_select(const float* signals, const float* comp, const float* model, int B, int32_t* gamma_star,
                       float* expected, spec_stream_t stream) {
   if (B < 1 || B > SPEC_MAX_B || !signals || !model || !gamma_star) return SPEC_ERR_INVALID_ARG;

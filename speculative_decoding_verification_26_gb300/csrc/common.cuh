@@ -508,6 +508,17 @@ struct DivParams {
 };
 cudaError_t launch_divergence(const DivParams& P, int grid, cudaStream_t s);
 
+// Parameters of the top-k / top-p filter (filter.cu).
+struct FiltParams {
+  unsigned char* logits;         // [n, V], filtered in place
+  int dtype, n, V;
+  const int32_t* top_k;          // [n] or null
+  const float* top_p;            // [n] or null
+  const float* temperature;      // [n] or null (= 1)
+  int32_t* status;               // [n] or null
+};
+cudaError_t launch_filter(const FiltParams& P, int grid, cudaStream_t s);
+
 // The SpecKV gamma selector (gamma.cu): model of SPEC_GAMMA_MODEL_FLOATS values.
 constexpr int kGammaModelFloats = SPEC_GAMMA_MODEL_FLOATS;
 cudaError_t launch_gamma_select(const float* signals, const float* comp, const float* model, int B,

@@ -106,3 +106,13 @@ def test_gamma_select_rejects_bad_arguments(L):
     assert L.spec_gamma_select(fake, None, fake, 4, None, None, None) == 1
     assert L.spec_gamma_select(fake, None, fake, 0, fake, None, None) == 1
     assert L.spec_gamma_select(P(0x7f0000000004), None, fake, 4, fake, None, None) == 1   # signals not 16-byte aligned
+
+
+def test_filter_rejects_bad_arguments(L):
+    P = ctypes.c_void_p
+    fake = P(0x7f0000000000)       # never dereferenced: the host checks fail first
+    assert L.spec_filter_top_k_top_p(None, 1, 4, 1024, None, None, None, None, None) == 1
+    assert L.spec_filter_top_k_top_p(fake, 3, 4, 1024, None, None, None, None, None) == 1
+    assert L.spec_filter_top_k_top_p(fake, 1, 0, 1024, None, None, None, None, None) == 1
+    assert L.spec_filter_top_k_top_p(fake, 1, 4, 1, None, None, None, None, None) == 1
+    assert L.spec_filter_top_k_top_p(P(0x7f0000000001), 1, 4, 1024, None, None, None, None, None) == 1
