@@ -359,7 +359,7 @@ int spec_filter_top_k_top_p(void* logits, int dtype, int n, int V, const int32_t
   P.logits = static_cast<unsigned char*>(logits);
   P.dtype = dtype; P.n = n; P.V = V;
   P.top_k = top_k; P.top_p = top_p; P.temperature = temperature; P.status = status;
-  const int grid = n < 4 * ctas ? n : 4 * ctas;
+  const int grid = n < ctas ? n : ctas;   // one row per resident CTA at a time (two per SM)
   if (launch_filter(P, grid > 0 ? grid : 1, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
     return SPEC_ERR_CUDA;
   ++g_launches;

@@ -147,3 +147,26 @@ def test_filtered_rows_feed_the_verification(o, dev):
     r = PT.run_oracle(o, "sample", wl, signals=True)
     assert np.array_equal(g["accept_len"], r["accept_len"])
     assert np.array_equal(g["tokens"], r["tokens"])
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_top_ties_overflow_the_candidate_list(o, dev, dtype):
+    """Rows whose top value is shared by more logits than the candidate list
+    holds (20000 of 30000): the bound from the threads' maxima keeps them all,
+    so the kernel falls back to counting the row; ties stay together.  Row 6
+    takes the same fallback with top-p alone; row 7 (nearly flat, top-p 0.99
+    alone) gives a list that fits but carries too little mass, the other
+    fallback of top-p alone."""
+    rng = np.random.default_rng(11)
+    n, V = 8, 30000
+    rows = rng.normal(-4, 1, (n, V)).astype(np.float32)
+    for r in range(7):
+        rows[r, rng.choice(V, 20000, replace=False)] = 1.0
+    rows[5, :] = 1.0                                   # every logit tied
+    rows[7] = rng.normal(0, 0.01, V).astype(np.float32)
+    k = np.array([1, 5, 300, 512, 20001, 3, 0, 0], np.int32)
+    p = np.array([1.0, 0.9, 0.5, 1.0, 0.99, 0.2, 0.9, 0.99], np.float32)
+    T = np.full(n, 0.8, np.float32)
+    if dtype == "bf16":
+        rows = W.bf16_rne_bits(rows)
+    check(o, dev, rows, dtype == "bf16", k, p, T, f"top ties {dtype}")
