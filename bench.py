@@ -532,6 +532,101 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+# ----------------------------------------------------------------------------
+# the calls beside the verification, timed on the headline shapes
+
+def run_op(args):
+    """--op divergence|filter|gamma: one JSON line per case, not the headline.
+    CUDA events on the current stream, inputs resident in HBM; divergence
+    rotates --sets input sets (L2 flush by footprint); filter restores its rows
+    between calls outside the timed events (the call filters in place)."""
+    import torch
+
+    import speculative_decoding_verification_26_gb300 as sv
+    sv.lib()
+    dev = torch.device("cuda:0")
+    peak, peak_kind = peaks()
+    steps, warm = min(args.steps, 400), max(args.warmup, 3)
+
+    def bf16_dev(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    def emit(case, us, algo_bytes, extra):
+        gbs = algo_bytes / (us * 1e-6) / 1e9 if algo_bytes else None
+        line = {"op": args.op, "case": case, "metric": f"{args.op} us per call", "value": round(us, 2),
+                "unit": "us", "higher_is_better": False, "steps": steps, "warmup": warm,
+                "algorithmic_bytes": algo_bytes, "achieved_gbs": round(gbs, 1) if gbs else None,
+                "frac": round(gbs / peak, 4) if gbs else None, "frac_label": f"of {peak_kind} {peak:.1f} GB/s",
+                "data": "synthetic", **extra}
+        print(json.dumps(line), flush=True)
+
+    if args.op == "divergence":
+        sets = []
+        for k in range(args.sets):
+            wl = W.make("m", k)
+            sets.append((bf16_dev(wl.target), bf16_dev(wl.draft), torch.from_numpy(wl.gamma).to(dev),
+                         torch.from_numpy(wl.temperature).to(dev)))
+        pairs = int(wl.gamma.sum())
+        for i in range(warm):
+            sv.divergence_stats(*sets[i % len(sets)])
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for i in range(steps):
+            sv.divergence_stats(*sets[i % len(sets)])
+        e1.record()
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / steps
+        emit("b64_g7_v151936", us, pairs * 2 * wl.V * 2,
+             {"config": {"workload": "divergence statistics of 64 requests, gamma 7, V 151936 bf16",
+                         "pairs": pairs, "l2": f"{args.sets} rotating input sets"}})
+    elif args.op == "filter":
+        wl = W.make("m", 0)
+        base = bf16_dev(wl.target).reshape(-1, wl.V)
+        n = base.shape[0]
+        work = base.clone()
+        T = torch.full((n,), 0.7, dtype=torch.float32, device=dev)
+        for case, k, p in (("top_k50", 50, None), ("top_p0.9", None, 0.9), ("top_k50_top_p0.9", 50, 0.9)):
+            kt = None if k is None else torch.full((n,), k, dtype=torch.int32, device=dev)
+            pt = None if p is None else torch.full((n,), p, dtype=torch.float32, device=dev)
+            for _ in range(warm):
+                work.copy_(base)
+                sv.filter_top_k_top_p(work, kt, pt, T)
+            torch.cuda.synchronize()
+            changed = int((work.view(torch.int16).reshape(n, -1, 8) != base.view(torch.int16).reshape(n, -1, 8))
+                          .any(-1).sum())
+            tot = 0.0
+            for _ in range(steps):
+                work.copy_(base)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                sv.filter_top_k_top_p(work, kt, pt, T)
+                e1.record()
+                torch.cuda.synchronize()
+                tot += e0.elapsed_time(e1)
+            kept = int(torch.isfinite(work.float()).sum())
+            emit(case, tot * 1e3 / steps, n * wl.V * 2 + changed * 16,
+                 {"config": {"workload": f"top-k/top-p filtering of {n} rows of V {wl.V} bf16 at T 0.7",
+                             "rows": n, "kept_per_row": round(kept / n, 2), "changed_16B_vectors": changed}})
+    else:
+        for B in (64, 4096):
+            g = torch.Generator().manual_seed(B)
+            sig = torch.rand(B, 4, generator=g).to(dev)
+            model = (torch.randn(141, generator=g) * 0.3).to(dev)
+            model[6:12] = 1.0                                  # standard deviations
+            for _ in range(warm):
+                sv.gamma_select(sig, model)
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(steps):
+                sv.gamma_select(sig, model)
+            e1.record()
+            torch.cuda.synchronize()
+            emit(f"b{B}", e0.elapsed_time(e1) * 1e3 / steps, None,
+                 {"config": {"workload": f"SpecKV gamma selector, {B} requests", "B": B}})
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -546,6 +641,8 @@ def main(argv=None):
     ap.add_argument("--min-warmup-s", type=float, default=0.5, help="keep warming up at least this long")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--op", choices=["verify", "divergence", "filter", "gamma"], default="verify",
+                    help="verify (default) is the headline step; the others time the calls beside it")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="m",
                     help="m (default) is the headline; c2..c5 time the other configurations")
     args = ap.parse_args(argv)
@@ -558,7 +655,9 @@ def main(argv=None):
         c = W.CONFIGS[WORKLOAD]
         METRIC = (f"verify rounds/s and HBM GB/s (% of 8 TB/s) at B={c['B']}, gamma={c['G']}, V={c['V']} bf16, "
                   f"{WORKLOADS[WORKLOAD][0]}")
-    if args.impl == "reference":
+    if args.op != "verify":
+        run_op(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

@@ -59,8 +59,8 @@ def compare(gs, gst, os_, ost, what):
     inf_g, inf_o = np.isinf(gs), np.isinf(os_)
     assert np.array_equal(inf_g, inf_o), (what, np.argwhere(inf_g != inf_o)[:5])
     fin = np.isfinite(os_)
-    err = np.abs(gs - os_)
-    tol = REL * np.abs(os_) + FLOOR
+    err = np.where(fin, np.abs(np.where(fin, gs, 0.0) - np.where(fin, os_, 0.0)), 0.0)   # inf - inf unasked
+    tol = REL * np.abs(np.where(fin, os_, 0.0)) + FLOOR
     bad = fin & ~(err <= tol)
     assert not bad.any(), (what, np.argwhere(bad)[:5], gs[bad][:5], os_[bad][:5])
     return int(fin.sum())
