@@ -28,13 +28,14 @@
 // are compared and maxed as packed bf16x2, so a pass costs a few instructions
 // per element):
 //   A: the row max and the non-finite check;
-//   C (top-k, k <= 512): the k-th largest of the 512 threads' own maxima is a
-//      lower bound of the k-th largest logit (k threads each hold an element
-//      that large), so the logits at or above it -- about k of them -- are
-//      copied to shared memory, and every level, top-k's and top-p's, runs on
-//      that list.  For larger k, or when the list would pass kCap, the first
-//      top-k level counts the whole row, and its keys at or above the chosen
-//      bucket are copied instead when they fit;
+//   S + C (top-k, k <= 512): over a quarter of the row, the k-th largest of the
+//      512 threads' own maxima is a lower bound of the k-th largest logit (k
+//      threads each hold an element that large), so pass A also copies the
+//      logits at or above it -- a few times k of them -- to shared memory, and
+//      every level, top-k's and top-p's, runs on that list.  For larger k, or
+//      when the list would pass kCap, the first top-k level counts the whole
+//      row, and its keys at or above the chosen bucket are copied instead when
+//      they fit;
 //   C (top-p alone): the same pass sums the whole row's mass in registers
 //      (a compensated fp32 sum per thread, reduced in fp64 in a fixed order:
 //      ~1e-7 relative, deterministic) and copies the logits at or above the
@@ -43,7 +44,9 @@
 //      list;
 //   else one pass per remaining level (a packed range test first, the exact
 //      key test on the few elements inside);
-//   K: the removed logits become -inf (a 16-byte store where any changed).
+//   K: the removed logits become -inf: on a list, -inf stores over the whole
+//      row (no read) and the list's kept logits put back at their indices;
+//      else a 16-byte store where any element changed.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -56,10 +59,10 @@ namespace {
 
 constexpr int kFiltThreads = 512;
 constexpr int kUnroll = 4;                                 // 16-byte loads in flight per thread
-constexpr int kCap = 8192;                                 // candidate list (raw values)
+constexpr int kCap = 4096;                                 // candidate list (index << 32 | raw)
 constexpr int kRankP = 384;                                // top-p alone: the list's bound, a thread-max rank
 constexpr int kHistWords = 256 * 32;                       // [bucket][lane] copies
-constexpr int kFiltSmem = kHistWords * 8 + kCap * 4;       // 96 KB dynamic
+constexpr int kFiltSmem = kHistWords * 8 + kCap * 8;       // 96 KB dynamic
 
 __device__ __forceinline__ __nv_bfloat162 as_bf2(uint32_t w) {
   __nv_bfloat162 v;
@@ -136,29 +139,37 @@ struct Span {
   }
 };
 
-// fe(raw) for each element of the head and tail, fw(word) for each 32-bit
-// word of the body (one fp32 element, or two bf16 elements, the lower index in
-// the low half), in no particular order.
+// fe(raw, v) for each element v of the head and tail, fw(word, v) for each
+// 32-bit word of the body (one fp32 element, or two bf16 elements, element v
+// in the low half and v + 1 in the high half), in no particular order.
 template <int DT, class FE, class FW>
-__device__ __forceinline__ void each_word(const unsigned char* row, int V, FE&& fe, FW&& fw) {
+__device__ __forceinline__ void each_word_at(const unsigned char* row, int V, FE&& fe, FW&& fw) {
   using K = Keys<DT>;
+  constexpr int PER = 16 / K::kES, WS = PER / 4;         // elements per vector / per word
   const Span<DT> sp(row, V);
   const int tid = threadIdx.x;
-  if (tid < sp.head) fe(K::raw(row, tid));
+  if (tid < sp.head) fe(K::raw(row, tid), tid);
   const uint4* body = reinterpret_cast<const uint4*>(row + (size_t)sp.head * K::kES);
+  auto vec = [&](const uint4& w, int i) {
+    const int v = sp.head + i * PER;
+    fw(w.x, v); fw(w.y, v + WS); fw(w.z, v + 2 * WS); fw(w.w, v + 3 * WS);
+  };
   int i = tid;
   for (; i + (kUnroll - 1) * kFiltThreads < sp.nvec; i += kUnroll * kFiltThreads) {
     uint4 w[kUnroll];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) w[u] = body[i + u * kFiltThreads];
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) { fw(w[u].x); fw(w[u].y); fw(w[u].z); fw(w[u].w); }
+    for (int u = 0; u < kUnroll; ++u) vec(w[u], i + u * kFiltThreads);
   }
-  for (; i < sp.nvec; i += kFiltThreads) {
-    const uint4 w = body[i];
-    fw(w.x); fw(w.y); fw(w.z); fw(w.w);
-  }
-  for (int v = sp.tail0 + tid; v < V; v += kFiltThreads) fe(K::raw(row, v));
+  for (; i < sp.nvec; i += kFiltThreads) vec(body[i], i);
+  for (int v = sp.tail0 + tid; v < V; v += kFiltThreads) fe(K::raw(row, v), v);
+}
+
+// The same without the element indices.
+template <int DT, class FE, class FW>
+__device__ __forceinline__ void each_word(const unsigned char* row, int V, FE&& fe, FW&& fw) {
+  each_word_at<DT>(row, V, [&](uint32_t h, int) { fe(h); }, [&](uint32_t w, int) { fw(w); });
 }
 
 // f(raw) for every element of the row, in no particular order.
@@ -171,27 +182,55 @@ __device__ __forceinline__ void each_raw(const unsigned char* row, int V, F&& f)
   }
 }
 
-// f(raw) for every element x with lo <= x <= hi (and perhaps a few more: a
+// f(raw, v) for every element v of the row, in no particular order.
+template <int DT, class F>
+__device__ __forceinline__ void each_raw_at(const unsigned char* row, int V, F&& f) {
+  if constexpr (DT == SPEC_BF16) {
+    each_word_at<DT>(row, V, f, [&](uint32_t w, int v) { f(w & 0xFFFFu, v); f(w >> 16, v + 1); });
+  } else {
+    each_word_at<DT>(row, V, f, f);
+  }
+}
+
+// f(raw, v) for every element x with lo <= x <= hi (and perhaps a few more: a
 // packed range test on bf16 pairs, which f must follow with its exact test).
 template <int DT, class F>
-__device__ __forceinline__ void each_in_range(const unsigned char* row, int V, float lo, float hi, F&& f) {
+__device__ __forceinline__ void each_in_range_at(const unsigned char* row, int V, float lo, float hi, F&& f) {
   using K = Keys<DT>;
-  auto fe = [&](uint32_t h) {
+  auto fe = [&](uint32_t h, int v) {
     const float x = K::value(h);
-    if (x >= lo && x <= hi) f(h);
+    if (x >= lo && x <= hi) f(h, v);
   };
   if constexpr (DT == SPEC_BF16) {
     const __nv_bfloat162 lo2 = __float2bfloat162_rn(lo), hi2 = __float2bfloat162_rn(hi);
-    each_word<DT>(row, V, fe, [&](uint32_t w) {
+    each_word_at<DT>(row, V, fe, [&](uint32_t w, int v) {
       const uint32_t in = __hge2_mask(as_bf2(w), lo2) & __hle2_mask(as_bf2(w), hi2);
       if (in) {
-        if (in & 0xFFFFu) f(w & 0xFFFFu);
-        if (in >> 16) f(w >> 16);
+        if (in & 0xFFFFu) f(w & 0xFFFFu, v);
+        if (in >> 16) f(w >> 16, v + 1);
       }
     });
   } else {
-    each_word<DT>(row, V, fe, fe);
+    each_word_at<DT>(row, V, fe, fe);
   }
+}
+
+template <int DT, class F>
+__device__ __forceinline__ void each_in_range(const unsigned char* row, int V, float lo, float hi, F&& f) {
+  each_in_range_at<DT>(row, V, lo, hi, [&](uint32_t h, int) { f(h); });
+}
+
+// Every logit of the row becomes -inf (stores only: the row is not read).
+template <int DT>
+__device__ __forceinline__ void fill_neg_inf(unsigned char* row, int V) {
+  using K = Keys<DT>;
+  const Span<DT> sp(row, V);
+  const int tid = threadIdx.x;
+  if (tid < sp.head) K::kill(row, tid);
+  constexpr uint32_t w = DT == SPEC_BF16 ? K::kNegInf * 0x00010001u : K::kNegInf;
+  uint4* body = reinterpret_cast<uint4*>(row + (size_t)sp.head * K::kES);
+  for (int i = tid; i < sp.nvec; i += kFiltThreads) body[i] = make_uint4(w, w, w, w);
+  for (int v = sp.tail0 + tid; v < V; v += kFiltThreads) K::kill(row, v);
 }
 
 // Every logit below t becomes -inf.
@@ -292,7 +331,7 @@ __global__ void __launch_bounds__(kFiltThreads, 2) filter_kernel(const __grid_co
   constexpr int kKeyBits = 8 * K::kES;
   extern __shared__ __align__(16) unsigned long long s_h[];   // [256 buckets][32 lanes], then the list
   uint32_t* const s_cnt = reinterpret_cast<uint32_t*>(s_h);
-  uint32_t* const s_cand = reinterpret_cast<uint32_t*>(s_h + kHistWords);
+  unsigned long long* const s_cand = s_h + kHistWords;       // (element index << 32) | raw
   __shared__ unsigned long long s_b[256];                      // bucket totals
   __shared__ __align__(16) float s_tmax[kFiltThreads];         // each thread's own max
   __shared__ float s_max[kFiltThreads / 32];
@@ -368,6 +407,65 @@ __global__ void __launch_bounds__(kFiltThreads, 2) filter_kernel(const __grid_co
         mt = fmaxf(mt, x);
         atomicAdd(&s_cnt[((K::key(h) >> sh0) & 255u) * 32 + lane], 1u);
       });
+    } else if (by_sample) {
+      // pass S: each thread's max over a quarter of the row (every fourth
+      // block of kFiltThreads vectors: any subset's k-th largest thread max
+      // bounds the row's k-th largest logit from below) ...
+      float ms = -INFINITY;
+      {
+        const Span<DT> sp(row, V);
+        const uint4* body = reinterpret_cast<const uint4*>(row + (size_t)sp.head * K::kES);
+#pragma unroll 4
+        for (int i = tid; i < sp.nvec; i += 4 * kFiltThreads) {
+          const uint4 w = body[i];
+          if constexpr (DT == SPEC_BF16) {
+            __nv_bfloat162 a = __hmax2(__hmax2(as_bf2(w.x), as_bf2(w.y)), __hmax2(as_bf2(w.z), as_bf2(w.w)));
+            const uint32_t b = bf2_bits(a);
+            ms = fmaxf(ms, fmaxf(K::value(b & 0xFFFFu), K::value(b >> 16)));
+          } else {
+            ms = fmaxf(ms, fmaxf(fmaxf(__uint_as_float(w.x), __uint_as_float(w.y)),
+                                 fmaxf(__uint_as_float(w.z), __uint_as_float(w.w))));
+          }
+        }
+      }
+      const float lb = rank_bound(ms, k);
+      if (tid == 0) s_n = 0;
+      __syncthreads();
+      // ... then pass A with C: the max, the non-finite check, and every logit
+      // >= lb to the list
+      auto put = [&](uint32_t h, int v) {
+        const int slot = atomicAdd(&s_n, 1);
+        if (slot < kCap) s_cand[slot] = ((unsigned long long)v << 32) | h;
+      };
+      if constexpr (DT == SPEC_BF16) {
+        __nv_bfloat162 mx = as_bf2(K::kNegInf * 0x00010001u);
+        const __nv_bfloat162 lb2 = __float2bfloat162_rn(lb);
+        each_word_at<DT>(
+            row, V,
+            [&](uint32_t h, int v) {
+              mx = __hmax2_nan(mx, as_bf2(h * 0x00010001u));
+              if (K::value(h) >= lb) put(h, v);
+            },
+            [&](uint32_t w, int v) {
+              mx = __hmax2_nan(mx, as_bf2(w));
+              const uint32_t in = __hge2_mask(as_bf2(w), lb2);
+              if (in) {
+                if (in & 0xFFFFu) put(w & 0xFFFFu, v);
+                if (in >> 16) put(w >> 16, v + 1);
+              }
+            });
+        const uint32_t b = bf2_bits(mx);
+        const float lo = K::value(b & 0xFFFFu), hi = K::value(b >> 16);
+        bad = (lo != lo) || (hi != hi) || lo == INFINITY || hi == INFINITY;
+        mt = fmaxf(lo, hi);
+      } else {
+        each_raw_at<DT>(row, V, [&](uint32_t h, int v) {
+          const float x = K::value(h);
+          bad |= (x != x) || x == INFINITY;
+          mt = fmaxf(mt, x);
+          if (x >= lb) put(h, v);
+        });
+      }
     } else if constexpr (DT == SPEC_BF16) {
       __nv_bfloat162 mx = as_bf2(K::kNegInf * 0x00010001u);
       each_word<DT>(row, V, [&](uint32_t h) { mx = __hmax2_nan(mx, as_bf2(h * 0x00010001u)); },
@@ -398,7 +496,7 @@ __global__ void __launch_bounds__(kFiltThreads, 2) filter_kernel(const __grid_co
     int n_list = 0;
     auto each_key = [&](auto&& f) {
       if (on_list) {
-        for (int i = tid; i < n_list; i += kFiltThreads) f(s_cand[i]);
+        for (int i = tid; i < n_list; i += kFiltThreads) f((uint32_t)s_cand[i]);
       } else {
         each_raw<DT>(row, V, f);
       }
@@ -406,10 +504,10 @@ __global__ void __launch_bounds__(kFiltThreads, 2) filter_kernel(const __grid_co
     auto collect = [&](float lo) {   // pass C: every logit >= lo, to the list (any order)
       if (tid == 0) s_n = 0;
       __syncthreads();
-      each_in_range<DT>(row, V, lo, INFINITY, [&](uint32_t h) {
+      each_in_range_at<DT>(row, V, lo, INFINITY, [&](uint32_t h, int v) {
         if (K::value(h) >= lo) {
           const int slot = atomicAdd(&s_n, 1);
-          if (slot < kCap) s_cand[slot] = h;
+          if (slot < kCap) s_cand[slot] = ((unsigned long long)v << 32) | h;
         }
       });
       __syncthreads();
@@ -445,7 +543,10 @@ __global__ void __launch_bounds__(kFiltThreads, 2) filter_kernel(const __grid_co
         prefix |= (uint32_t)s_d << (kKeyBits - 8 * (lv + 1));
         above = s_cum;
       };
-      if (by_sample) collect(rank_bound(mt, k));   // the k-th largest of the threads' maxima
+      if (by_sample && s_n <= kCap) {   // the list pass A filled
+        on_list = true;
+        n_list = s_n;
+      }
       if (!on_list) {
         if (!hist_in_a) count_level(0);
         pick(0);
@@ -479,7 +580,7 @@ __global__ void __launch_bounds__(kFiltThreads, 2) filter_kernel(const __grid_co
         if (tid == 0) { s_n = 0; s_sum = 0ull; }
         __syncthreads();
         float sf = 0.f, cf = 0.f;                              // compensated (Kahan) fp32 sum
-        each_raw<DT>(row, V, [&](uint32_t h) {
+        each_raw_at<DT>(row, V, [&](uint32_t h, int v) {
           const float x = K::value(h);
           const float y = ex2(stretch(fmaf(x, c, nr), ks)) - cf;
           const float t = sf + y;
@@ -487,7 +588,7 @@ __global__ void __launch_bounds__(kFiltThreads, 2) filter_kernel(const __grid_co
           sf = t;
           if (x >= lb) {
             const int slot = atomicAdd(&s_n, 1);
-            if (slot < kCap) s_cand[slot] = h;
+            if (slot < kCap) s_cand[slot] = ((unsigned long long)v << 32) | h;
           }
         });
         double dv = (double)sf - (double)cf;                   // fixed-order fp64 reduction
@@ -504,7 +605,7 @@ __global__ void __launch_bounds__(kFiltThreads, 2) filter_kernel(const __grid_co
           __syncthreads();
           const int nl = s_n;
           unsigned long long lm = 0ull;
-          for (int i = tid; i < nl; i += kFiltThreads) lm += weight(K::value(s_cand[i]));
+          for (int i = tid; i < nl; i += kFiltThreads) lm += weight(K::value((uint32_t)s_cand[i]));
           if ((double)block_sum(lm) >= want) {
             on_list = true;
             n_list = nl;
@@ -555,8 +656,23 @@ __global__ void __launch_bounds__(kFiltThreads, 2) filter_kernel(const __grid_co
       if (prefix > thr) thr = prefix;
     }
 
-    // pass K: the removed logits become -inf
-    if (thr > 0u) kill_below<DT>(row, V, value_of<DT>(thr));
+    // pass K: the removed logits become -inf.  On the list every kept logit is
+    // known with its index: fill the row, then put those back (no row read).
+    if (on_list) {
+      fill_neg_inf<DT>(row, V);
+      __syncthreads();
+      for (int i = tid; i < n_list; i += kFiltThreads) {
+        const unsigned long long e = s_cand[i];
+        const uint32_t h = (uint32_t)e;
+        if (K::key(h) >= thr) {
+          const int v = (int)(e >> 32);
+          if constexpr (DT == SPEC_BF16) reinterpret_cast<uint16_t*>(row)[v] = (uint16_t)h;
+          else reinterpret_cast<uint32_t*>(row)[v] = h;
+        }
+      }
+    } else if (thr > 0u) {
+      kill_below<DT>(row, V, value_of<DT>(thr));
+    }
     if (tid == 0 && P.status) P.status[r] = 0;
     __syncthreads();
   }
