@@ -36,12 +36,17 @@
 //      when the list would pass kCap, the first top-k level counts the whole
 //      row, and its keys at or above the chosen bucket are copied instead when
 //      they fit;
-//   C (top-p alone): the same pass sums the whole row's mass in registers
-//      (a compensated fp32 sum per thread, reduced in fp64 in a fixed order:
-//      ~1e-7 relative, deterministic) and copies the logits at or above the
-//      384th largest thread maximum; when those carry at least top_p of the
-//      total in exact fixed point, t* is among them and the levels run on the
-//      list;
+//   S + C (top-p alone): the sample's max m_s is a provisional reference, so
+//      pass A also sums the whole row's mass on it in registers (each 16-byte
+//      vector's weights by a fixed tree, then a compensated fp32 sum per
+//      thread, reduced in fp64 in a fixed order: ~2e-7 relative,
+//      deterministic), rescaled to the row max by 2^{(R(m_s) - R(m))(1 + k)},
+//      and copies the logits above the 256th largest sampled thread maximum;
+//      when those carry at least top_p of the total in exact fixed point (on
+//      the row max), t* is among them and the levels run on the list.  A
+//      weight that overflows on m_s voids the list (the exact path runs);
+//      with no finite m_s, pass A takes the max alone and a pass C does the
+//      rest on the row max;
 //   else one pass per remaining level (a packed range test first, the exact
 //      key test on the few elements inside);
 //   K: the removed logits become -inf: on a list, -inf stores over the whole
@@ -61,6 +66,7 @@ constexpr int kFiltThreads = 512;
 constexpr int kUnroll = 4;                                 // 16-byte loads in flight per thread
 constexpr int kCap = 4096;                                 // candidate list (index << 32 | raw)
 constexpr int kRankP = 384;                                // top-p alone: the list's bound, a thread-max rank
+constexpr int kRankPS = 256;                               // the same over a quarter-row sample
 constexpr int kHistWords = 256 * 32;                       // [bucket][lane] copies
 constexpr int kFiltSmem = kHistWords * 8 + kCap * 8;       // 96 KB dynamic
 
@@ -163,6 +169,28 @@ __device__ __forceinline__ void each_word_at(const unsigned char* row, int V, FE
     for (int u = 0; u < kUnroll; ++u) vec(w[u], i + u * kFiltThreads);
   }
   for (; i < sp.nvec; i += kFiltThreads) vec(body[i], i);
+  for (int v = sp.tail0 + tid; v < V; v += kFiltThreads) fe(K::raw(row, v), v);
+}
+
+// fe(raw, v) for each element v of the head and tail, fv(vector, v) for each
+// 16-byte vector of the body (its first element is v), in no particular order.
+template <int DT, class FE, class FV>
+__device__ __forceinline__ void each_vec_at(const unsigned char* row, int V, FE&& fe, FV&& fv) {
+  using K = Keys<DT>;
+  constexpr int PER = 16 / K::kES;
+  const Span<DT> sp(row, V);
+  const int tid = threadIdx.x;
+  if (tid < sp.head) fe(K::raw(row, tid), tid);
+  const uint4* body = reinterpret_cast<const uint4*>(row + (size_t)sp.head * K::kES);
+  int i = tid;
+  for (; i + (kUnroll - 1) * kFiltThreads < sp.nvec; i += kUnroll * kFiltThreads) {
+    uint4 w[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) w[u] = body[i + u * kFiltThreads];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) fv(w[u], sp.head + (i + u * kFiltThreads) * PER);
+  }
+  for (; i < sp.nvec; i += kFiltThreads) fv(body[i], sp.head + i * PER);
   for (int v = sp.tail0 + tid; v < V; v += kFiltThreads) fe(K::raw(row, v), v);
 }
 
@@ -376,6 +404,17 @@ __global__ void __launch_bounds__(kFiltThreads, 2) filter_kernel(const __grid_co
     return t;
   };
 
+  auto block_dsum = [&](double v) -> double {   // fixed-order fp64 sum over the CTA
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    if (lane == 0) s_dsum[warp] = v;
+    __syncthreads();
+    double t = 0.0;
+    for (int w = 0; w < kFiltThreads / 32; ++w) t += s_dsum[w];
+    __syncthreads();
+    return t;
+  };
+
   for (int r = blockIdx.x; r < P.n; r += gridDim.x) {
     unsigned char* row = P.logits + (size_t)r * V * K::kES;
     const int k = P.top_k ? P.top_k[r] : 0;
@@ -396,8 +435,47 @@ __global__ void __launch_bounds__(kFiltThreads, 2) filter_kernel(const __grid_co
     constexpr int sh0 = kKeyBits - 8;
     const bool by_sample = use_k && k <= kFiltThreads;
     const bool hist_in_a = use_k && !by_sample;
+    const bool p_alone = use_p && !use_k;
+    // top-p's scale: log2(e)/T as c + c_lo, applied as a stretch by ks
+    float c = 0.f, ks = 0.f, unit = 0.f;
+    if (use_p) {
+      c = scale_of(T);
+      const float c_lo = (float)(1.4426950408889634 / (double)T - (double)c);
+      ks = scale_k(c, c_lo);
+      int lg = 0;
+      while ((1 << lg) < V) ++lg;
+      unit = __int_as_float((127 + 61 - lg) << 23);        // 2^(61 - ceil(log2 V))
+    }
+    // pass S: each thread's max over a quarter of the row (every fourth block
+    // of kFiltThreads vectors).  Any subset's k-th largest thread max bounds
+    // the row's k-th largest logit from below; the CTA's max of it is a
+    // provisional reference for top-p's weights.
+    float ms = -INFINITY;
+    if (by_sample || p_alone) {
+      const Span<DT> sp(row, V);
+      const uint4* body = reinterpret_cast<const uint4*>(row + (size_t)sp.head * K::kES);
+#pragma unroll 4
+      for (int i = tid; i < sp.nvec; i += 4 * kFiltThreads) {
+        const uint4 w = body[i];
+        if constexpr (DT == SPEC_BF16) {
+          __nv_bfloat162 a = __hmax2(__hmax2(as_bf2(w.x), as_bf2(w.y)), __hmax2(as_bf2(w.z), as_bf2(w.w)));
+          const uint32_t b = bf2_bits(a);
+          ms = fmaxf(ms, fmaxf(K::value(b & 0xFFFFu), K::value(b >> 16)));
+        } else {
+          ms = fmaxf(ms, fmaxf(fmaxf(__uint_as_float(w.x), __uint_as_float(w.y)),
+                               fmaxf(__uint_as_float(w.z), __uint_as_float(w.w))));
+        }
+      }
+    }
+    const float m_s = p_alone ? block_max(ms) : -INFINITY;
+    const bool fused_p = p_alone && m_s > -INFINITY && m_s < INFINITY;
+    auto put = [&](uint32_t h, int v) {   // onto the list
+      const int slot = atomicAdd(&s_n, 1);
+      if (slot < kCap) s_cand[slot] = ((unsigned long long)v << 32) | h;
+    };
     float mt = -INFINITY;                                      // this thread's max
     int bad = 0;
+    double tot_s = 0.0;                                        // top-p alone: the mass on m_s
     if (hist_in_a) {
       zero_hist(kHistWords / 2);
       __syncthreads();
@@ -408,35 +486,11 @@ __global__ void __launch_bounds__(kFiltThreads, 2) filter_kernel(const __grid_co
         atomicAdd(&s_cnt[((K::key(h) >> sh0) & 255u) * 32 + lane], 1u);
       });
     } else if (by_sample) {
-      // pass S: each thread's max over a quarter of the row (every fourth
-      // block of kFiltThreads vectors: any subset's k-th largest thread max
-      // bounds the row's k-th largest logit from below) ...
-      float ms = -INFINITY;
-      {
-        const Span<DT> sp(row, V);
-        const uint4* body = reinterpret_cast<const uint4*>(row + (size_t)sp.head * K::kES);
-#pragma unroll 4
-        for (int i = tid; i < sp.nvec; i += 4 * kFiltThreads) {
-          const uint4 w = body[i];
-          if constexpr (DT == SPEC_BF16) {
-            __nv_bfloat162 a = __hmax2(__hmax2(as_bf2(w.x), as_bf2(w.y)), __hmax2(as_bf2(w.z), as_bf2(w.w)));
-            const uint32_t b = bf2_bits(a);
-            ms = fmaxf(ms, fmaxf(K::value(b & 0xFFFFu), K::value(b >> 16)));
-          } else {
-            ms = fmaxf(ms, fmaxf(fmaxf(__uint_as_float(w.x), __uint_as_float(w.y)),
-                                 fmaxf(__uint_as_float(w.z), __uint_as_float(w.w))));
-          }
-        }
-      }
+      // pass A with C: the max, the non-finite check, and every logit >= the
+      // k-th largest sampled thread max to the list
       const float lb = rank_bound(ms, k);
       if (tid == 0) s_n = 0;
       __syncthreads();
-      // ... then pass A with C: the max, the non-finite check, and every logit
-      // >= lb to the list
-      auto put = [&](uint32_t h, int v) {
-        const int slot = atomicAdd(&s_n, 1);
-        if (slot < kCap) s_cand[slot] = ((unsigned long long)v << 32) | h;
-      };
       if constexpr (DT == SPEC_BF16) {
         __nv_bfloat162 mx = as_bf2(K::kNegInf * 0x00010001u);
         const __nv_bfloat162 lb2 = __float2bfloat162_rn(lb);
@@ -466,6 +520,85 @@ __global__ void __launch_bounds__(kFiltThreads, 2) filter_kernel(const __grid_co
           if (x >= lb) put(h, v);
         });
       }
+    } else if (fused_p) {
+      // pass A with C for top-p alone: the max, the non-finite check, the row's
+      // mass on the reference m_s (a compensated fp32 sum per thread; rescaled
+      // to the row max below) and the logits above a sampled thread-max rank
+      const float lb = rank_bound(ms, kRankPS);
+      const float nrs = -ref_of(m_s, c);
+      if (tid == 0) s_n = 0;
+      __syncthreads();
+      // a vector's weights are summed by a fixed tree, and only that sum
+      // enters the compensated sum: a short serial chain per 16 bytes
+      float sf = 0.f, cf = 0.f;
+      auto kahan = [&](float y) {
+        y -= cf;
+        const float t = sf + y;
+        cf = (t - sf) - y;
+        sf = t;
+      };
+      auto wt = [&](float x) { return ex2(stretch(fmaf(x, c, nrs), ks)); };
+      auto one = [&](uint32_t h, int v) {   // a head or tail element
+        const float x = K::value(h);
+        kahan(wt(x));
+        if (x >= lb) put(h, v);
+      };
+      if constexpr (DT == SPEC_BF16) {
+        __nv_bfloat162 mx = as_bf2(K::kNegInf * 0x00010001u);
+        const __nv_bfloat162 lb2 = __float2bfloat162_rn(lb);
+        each_vec_at<DT>(
+            row, V,
+            [&](uint32_t h, int v) {
+              mx = __hmax2_nan(mx, as_bf2(h * 0x00010001u));
+              one(h, v);
+            },
+            [&](const uint4& q, int v) {
+              const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+              float e[8];
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                mx = __hmax2_nan(mx, as_bf2(w[j]));
+                e[2 * j] = wt(K::value(w[j] & 0xFFFFu));
+                e[2 * j + 1] = wt(K::value(w[j] >> 16));
+              }
+              kahan(((e[0] + e[1]) + (e[2] + e[3])) + ((e[4] + e[5]) + (e[6] + e[7])));
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const uint32_t in = __hge2_mask(as_bf2(w[j]), lb2);
+                if (in) {
+                  if (in & 0xFFFFu) put(w[j] & 0xFFFFu, v + 2 * j);
+                  if (in >> 16) put(w[j] >> 16, v + 2 * j + 1);
+                }
+              }
+            });
+        const uint32_t b = bf2_bits(mx);
+        const float lo = K::value(b & 0xFFFFu), hi = K::value(b >> 16);
+        bad = (lo != lo) || (hi != hi) || lo == INFINITY || hi == INFINITY;
+        mt = fmaxf(lo, hi);
+      } else {
+        auto chk = [&](float x) {
+          bad |= (x != x) || x == INFINITY;
+          mt = fmaxf(mt, x);
+        };
+        each_vec_at<DT>(
+            row, V,
+            [&](uint32_t h, int v) {
+              chk(K::value(h));
+              one(h, v);
+            },
+            [&](const uint4& q, int v) {
+              const float x[4] = {__uint_as_float(q.x), __uint_as_float(q.y), __uint_as_float(q.z),
+                                  __uint_as_float(q.w)};
+#pragma unroll
+              for (int j = 0; j < 4; ++j) chk(x[j]);
+              kahan((wt(x[0]) + wt(x[1])) + (wt(x[2]) + wt(x[3])));
+              const uint32_t u[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                if (x[j] >= lb) put(u[j], v + j);
+            });
+      }
+      tot_s = block_dsum((double)sf - (double)cf);
     } else if constexpr (DT == SPEC_BF16) {
       __nv_bfloat162 mx = as_bf2(K::kNegInf * 0x00010001u);
       each_word<DT>(row, V, [&](uint32_t h) { mx = __hmax2_nan(mx, as_bf2(h * 0x00010001u)); },
@@ -562,43 +695,32 @@ __global__ void __launch_bounds__(kFiltThreads, 2) filter_kernel(const __grid_co
 
     // top-p: the key of t* (radix descent on fixed-point masses)
     if (use_p) {
-      const float c = scale_of(T);
-      const float c_lo = (float)(1.4426950408889634 / (double)T - (double)c);
-      const float ks = scale_k(c, c_lo);
       const float nr = -ref_of(m, c);
-      int lg = 0;
-      while ((1 << lg) < V) ++lg;
-      const float unit = __int_as_float((127 + 61 - lg) << 23);   // 2^(61 - ceil(log2 V))
       auto weight = [&](float x) -> unsigned long long {
         const float w = ex2(stretch(fmaf(x, c, nr), ks));
         return __float2ull_rz(w * unit);
       };
       double need = -1.0;                                      // known before the levels when >= 0
       if (!use_k) {
-        // pass C: the row's total mass, and the logits at or above a bound
-        const float lb = rank_bound(mt, kRankP);
-        if (tid == 0) { s_n = 0; s_sum = 0ull; }
-        __syncthreads();
-        float sf = 0.f, cf = 0.f;                              // compensated (Kahan) fp32 sum
-        each_raw_at<DT>(row, V, [&](uint32_t h, int v) {
-          const float x = K::value(h);
-          const float y = ex2(stretch(fmaf(x, c, nr), ks)) - cf;
-          const float t = sf + y;
-          cf = (t - sf) - y;
-          sf = t;
-          if (x >= lb) {
-            const int slot = atomicAdd(&s_n, 1);
-            if (slot < kCap) s_cand[slot] = ((unsigned long long)v << 32) | h;
-          }
-        });
-        double dv = (double)sf - (double)cf;                   // fixed-order fp64 reduction
-#pragma unroll
-        for (int off = 16; off >= 1; off >>= 1) dv += __shfl_xor_sync(0xffffffffu, dv, off);
-        if (lane == 0) s_dsum[warp] = dv;
-        __syncthreads();
-        double tot = 0.0;
-        for (int w = 0; w < kFiltThreads / 32; ++w) tot += s_dsum[w];
-        __syncthreads();
+        double tot;                                            // the row's mass on the row max
+        if (fused_p) {   // pass A summed it on m_s: 2^{(R(m_s) - R(m))(1 + ks)} rescales it
+          tot = tot_s * exp2(((double)ref_of(m_s, c) - (double)ref_of(m, c)) * (1.0 + (double)ks));
+        } else {
+          // pass C: the row's total mass, and the logits at or above a bound
+          const float lb = rank_bound(mt, kRankP);
+          if (tid == 0) s_n = 0;
+          __syncthreads();
+          float sf = 0.f, cf = 0.f;                            // compensated (Kahan) fp32 sum
+          each_raw_at<DT>(row, V, [&](uint32_t h, int v) {
+            const float x = K::value(h);
+            const float y = ex2(stretch(fmaf(x, c, nr), ks)) - cf;
+            const float t = sf + y;
+            cf = (t - sf) - y;
+            sf = t;
+            if (x >= lb) put(h, v);
+          });
+          tot = block_dsum((double)sf - (double)cf);         // fixed-order fp64 reduction
+        }
         const double want = (double)tp * tot * (double)unit;
         if (s_n <= kCap) {   // the list's own mass: t* is on it when that reaches the target
           if (tid == 0) s_sum = 0ull;

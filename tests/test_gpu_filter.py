@@ -170,3 +170,25 @@ def test_top_ties_overflow_the_candidate_list(o, dev, dtype):
     if dtype == "bf16":
         rows = W.bf16_rne_bits(rows)
     check(o, dev, rows, dtype == "bf16", k, p, T, f"top ties {dtype}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_top_p_alone_sampled_reference(o, dev, dtype):
+    """Top-p alone sums the row's mass on the max of a quarter-row sample (the
+    16-byte vectors of every fourth block of 512), rescaled to the row max.
+    Elements 4096..8191 lie outside that sample for both dtypes here.  Row 0:
+    a spike 200 above the sample (the weights overflow: exact fallback); row 1:
+    every sampled logit -inf (no finite reference: the unfused passes); row 2:
+    the max outside the sample (the rescale); row 3: an ordinary row."""
+    rng = np.random.default_rng(17)
+    n, V = 4, 30000
+    rows = rng.normal(0, 1, (n, V)).astype(np.float32)
+    rows[0, 5000] = 200.0
+    rows[1, :4096] = -np.inf
+    rows[1, 8192:] = -np.inf
+    rows[2, 6000] = 6.0
+    p = np.array([0.9, 0.9, 0.8, 0.95], np.float32)
+    T = np.full(n, 0.7, np.float32)
+    if dtype == "bf16":
+        rows = W.bf16_rne_bits(rows)
+    check(o, dev, rows, dtype == "bf16", None, p, T, f"sampled reference {dtype}")
