@@ -38,6 +38,8 @@ struct Acc {
 
 __device__ __forceinline__ void acc_reset(Acc& a) { a.m = -INFINITY; a.s = 0.f; }
 
+__device__ __forceinline__ float2 f2(float a, float b) { return make_float2(a, b); }
+
 // Add logits x[0..n) to a running (m, s) with the shared exponent rule.
 template <int N>
 __device__ __forceinline__ void acc_add(Acc& a, const float (&x)[N], float c, float ks) {
@@ -50,10 +52,22 @@ __device__ __forceinline__ void acc_add(Acc& a, const float (&x)[N], float c, fl
   }
   if (a.m == -INFINITY) return;
   const float nr = -ref_of(a.m, c);
-  float t = 0.f;
+  if constexpr (N % 2 == 0) {   // packed fp32 pairs: the same roundings per lane
+    const float2 C2 = f2(c, c), K2 = f2(ks, ks), NR2 = f2(nr, nr);
+    float2 t2 = f2(0.f, 0.f);
 #pragma unroll
-  for (int k = 0; k < N; ++k) t += ex2(stretch(fmaf(x[k], c, nr), ks));
-  a.s += t;
+    for (int k = 0; k < N; k += 2) {
+      float2 e = __ffma2_rn(f2(x[k], x[k + 1]), C2, NR2);
+      e = __ffma2_rn(e, K2, e);                           // stretch
+      t2 = __fadd2_rn(t2, f2(ex2(e.x), ex2(e.y)));
+    }
+    a.s += t2.x + t2.y;
+  } else {
+    float t = 0.f;
+#pragma unroll
+    for (int k = 0; k < N; ++k) t += ex2(stretch(fmaf(x[k], c, nr), ks));
+    a.s += t;
+  }
 }
 
 // Merge two partials (the online-softmax rule).
@@ -208,18 +222,47 @@ __global__ void __launch_bounds__(kDivThreads, 1) divergence_kernel(const __grid
     const float lsp = log2f(fp.s), lsq = log2f(fq.s);
     const float nrp = -ref_of(fp.m, c), nrq = -ref_of(fq.m, c);
     Sums sm{0.f, 0.f, 0.f, 0.f, 0.f};
+    const float2 C2 = f2(c, c), K2 = f2(ks, ks), NRP2 = f2(nrp, nrp), NRQ2 = f2(nrq, nrq);
+    const float2 RP2 = f2(rp, rp), RQ2 = f2(rq, rq), NLSP2 = f2(-lsp, -lsp), NLSQ2 = f2(-lsq, -lsq);
+    const float2 M1 = f2(-1.f, -1.f);
     for_pair<DT>(trow, drow, V, vec, [&](auto& xt, auto& xd) {
       constexpr int n = sizeof(xt) / sizeof(float);
       Sums v{0.f, 0.f, 0.f, 0.f, 0.f};        // the vector's terms first, then the thread's sums
+      if constexpr (n % 2 == 0) {
+        // token pairs in packed fp32 (each lane rounds as the scalar form);
+        // the KL and entropy terms stay per token, guarded for p or q = 0
+        float2 vA = f2(0.f, 0.f), vL1 = f2(0.f, 0.f);
 #pragma unroll
-      for (int k = 0; k < n; ++k) {
-        const float a1 = stretch(fmaf(xt[k], c, nrp), ks), a2 = stretch(fmaf(xd[k], c, nrq), ks);
-        const float p = ex2(a1) * rp, q = ex2(a2) * rq;
-        const float lp = a1 - lsp, lq = a2 - lsq;   // log2 p, log2 q
-        v.A += fminf(p, q);
-        v.L1 += fabsf(p - q);
-        if (p > 0.f) { v.kpq += p * (lp - lq); v.H -= p * lp; }
-        if (q > 0.f) v.kqp += q * (lq - lp);
+        for (int k = 0; k < n; k += 2) {
+          float2 a1 = __ffma2_rn(f2(xt[k], xt[k + 1]), C2, NRP2);
+          a1 = __ffma2_rn(a1, K2, a1);
+          float2 a2 = __ffma2_rn(f2(xd[k], xd[k + 1]), C2, NRQ2);
+          a2 = __ffma2_rn(a2, K2, a2);
+          const float2 p = __fmul2_rn(f2(ex2(a1.x), ex2(a1.y)), RP2);
+          const float2 q = __fmul2_rn(f2(ex2(a2.x), ex2(a2.y)), RQ2);
+          const float2 lp = __fadd2_rn(a1, NLSP2), lq = __fadd2_rn(a2, NLSQ2);   // log2 p, log2 q
+          const float2 d = __ffma2_rn(lq, M1, lp);          // log2 p - log2 q
+          const float2 pq = __ffma2_rn(q, M1, p);           // p - q
+          vA = __fadd2_rn(vA, f2(fminf(p.x, q.x), fminf(p.y, q.y)));
+          vL1 = __fadd2_rn(vL1, f2(fabsf(pq.x), fabsf(pq.y)));
+          if (p.x > 0.f) { v.kpq = fmaf(p.x, d.x, v.kpq); v.H = fmaf(-p.x, lp.x, v.H); }
+          if (q.x > 0.f) v.kqp = fmaf(-q.x, d.x, v.kqp);
+          if (p.y > 0.f) { v.kpq = fmaf(p.y, d.y, v.kpq); v.H = fmaf(-p.y, lp.y, v.H); }
+          if (q.y > 0.f) v.kqp = fmaf(-q.y, d.y, v.kqp);
+        }
+        v.A = vA.x + vA.y;
+        v.L1 = vL1.x + vL1.y;
+      } else {
+#pragma unroll
+        for (int k = 0; k < n; ++k) {
+          const float a1 = stretch(fmaf(xt[k], c, nrp), ks), a2 = stretch(fmaf(xd[k], c, nrq), ks);
+          const float p = ex2(a1) * rp, q = ex2(a2) * rq;
+          const float lp = a1 - lsp, lq = a2 - lsq;   // log2 p, log2 q
+          v.A += fminf(p, q);
+          v.L1 += fabsf(p - q);
+          if (p > 0.f) { v.kpq += p * (lp - lq); v.H -= p * lp; }
+          if (q > 0.f) v.kqp += q * (lq - lp);
+        }
       }
       sm.A += v.A; sm.L1 += v.L1; sm.kpq += v.kpq; sm.kqp += v.kqp; sm.H += v.H;
     });
